@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark of the INT8 paged KV-cache hot path on GB300.
+
+One step = one layer's decode step of the canonical GQA workload (32
+sequences, contexts U[512, 2048] + 1 appended token, 32 query / 8 KV heads,
+d 128, bf16, block 16, shuffled block pool):
+
+    kvq_quantize_append (1 new token per sequence)  ->  kvq_paged_decode
+
+The same step is timed on the native-BF16 twin (kvq_cache_append_kv16 ->
+kvq_paged_decode_kv16) for the steps/s A/B, and through the C ABI with host
+buffers (pinned H2D of the step's inputs and D2H of the output inside the
+timed region) for the end-to-end figure.  L2 is flushed (512 MB write)
+between timed steps; each step is timed with CUDA events on the launching
+stream.  A context sweep (2K/8K/32K, 16 sequences) compares the INT8 decode
+with the BF16 twin.  The FP64 CPU oracle is timed on a bounded sample of the
+same workload as the CPU baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload (the path needs no exchange between GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "INT8-KV paged decode HBM GB/s (% of GB300 peak); decode steps/s vs BF16 KV"
+UNIT = "GB/s"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ("kvq_decode.cuh", "kvq_decode_int8.cu", "kvq_ptx.cuh", "kvq_combine.cu",
+                  "kvq_api.cu", "kvq_internal.h")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_int8_canonical_traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="canonical", choices=list(W.NAMES))
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "int8_quantized_paged_tokenwise_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def config_of(w: W.Workload, extra=None):
+    c = {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+         "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+         "kv_dtype": "int8+fp16-scale", "act_dtype": w.dtype,
+         "context_tokens": int(w.context_lens.sum()), "max_context": w.max_context_len,
+         "append_tokens_per_step": w.append_tokens(), "l2": "flushed (512 MB write) between steps"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------- CPU oracle ---
+def time_oracle(w: W.Workload, budget_s: float, start_seq: int = 0, max_seqs: int | None = None):
+    """The FP64 oracle as it stands, single thread: quantize-append of the
+    step's token + decode (it re-quantizes the context from the unpaged token
+    arrays) for whole sequences until the time budget is spent."""
+    import oracle
+    oracle.build()
+    nb, bt, _ = w.tables()
+    bytes_done, t_total, n = 0, 0.0, 0
+    b = start_seq
+    while (max_seqs is None or n < max_seqs) and (t_total < budget_s or n == 0):
+        b = b % w.num_seqs
+        k, v = w.seq_kv(b)
+        q = w.seq_q(b)
+        L = len(k)
+        kc = np.zeros((nb, w.num_kv_heads, 16, w.head_dim), np.int8)
+        ks = np.zeros((nb, w.num_kv_heads, 16), np.uint16)
+        t0 = time.perf_counter()
+        oracle.quantize_append(k[L - 1:], v[L - 1:], w.dtype, w.slots(b, L - 1, L), kc, kc.copy(),
+                               ks, ks.copy(), 16)
+        oracle.decode_sequence(q, k, v, w.dtype, w.sm_scale)
+        t_total += time.perf_counter() - t0
+        bytes_done += L * w.num_kv_heads * (2 * w.head_dim + 4) + w.pages(L) * 4 + \
+            2 * w.num_q_heads * w.head_dim * 2
+        n += 1
+        b += 1
+    return bytes_done / t_total / 1e9, n, t_total
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = W.make(args.workload)
+    per_step = 4
+    for i in range(args.warmup):
+        time_oracle(w, 0.0, start_seq=i * per_step, max_seqs=per_step)
+    vals, times = [], []
+    for i in range(args.steps):
+        gbs, n, t = time_oracle(w, 0.0, start_seq=(args.warmup + i) * per_step, max_seqs=per_step)
+        vals.append(gbs)
+        times.append(t)
+    total_bytes = sum(v * t for v, t in zip(vals, times))
+    value = total_bytes / sum(times)
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, {"sample": f"{per_step} sequences per step"}),
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} whole sequences of the {w.name} workload per step "
+                                   "(quantize-append of the step token + decode, all heads)"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- clocks ---
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------- GPU ---
+class GpuWorkload:
+    """A workload resident in HBM: INT8 cache, BF16 twin cache, tables, q and
+    the step's new tokens, plus pinned host copies for the end-to-end arm."""
+
+    def __init__(self, w: W.Workload, dev):
+        import torch
+        import int8_quantized_paged_tokenwise_gb300 as kvq
+        self.torch, self.kvq, self.w, self.dev = torch, kvq, w, dev
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+        self.tdt = tdt
+
+        def up(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(tdt)
+
+        nb, bt, _ = w.tables()
+        self.int8 = kvq.alloc_int8_cache(nb, w.num_kv_heads, w.head_dim, dev)
+        self.kv16 = kvq.alloc_kv16_cache(nb, w.num_kv_heads, w.head_dim, tdt, dev)
+        for b in range(w.num_seqs):
+            k, v = w.seq_kv(b)
+            n = int(w.prefix_lens[b])
+            if n == 0:
+                continue
+            s = torch.from_numpy(w.slots(b, 0, n)).to(dev)
+            kd, vd = up(k[:n]), up(v[:n])
+            kvq.kvq_quantize_append(kd, vd, s, *self.int8)
+            kvq.kvq_cache_append_kv16(kd, vd, s, *self.kv16)
+        ks, vs, ss = [], [], []
+        if w.append:
+            for b in range(w.num_seqs):
+                k, v = w.seq_kv(b)
+                L = int(w.context_lens[b])
+                ks.append(k[L - 1:L]); vs.append(v[L - 1:L]); ss.append(w.slots(b, L - 1, L))
+        if w.prefill_tokens:
+            pk, pv = w.prefill_kv()
+            ks.append(pk); vs.append(pv); ss.append(w.prefill_slots())
+        self.k_new_h = np.concatenate(ks) if ks else None
+        self.v_new_h = np.concatenate(vs) if vs else None
+        self.slots_h = np.concatenate(ss).astype(np.int64) if ss else None
+        self.k_new = up(self.k_new_h) if ks else None
+        self.v_new = up(self.v_new_h) if vs else None
+        self.slots = torch.from_numpy(self.slots_h).to(dev) if ss else None
+        self.q_h = w.q_all()
+        self.q = up(self.q_h)
+        self.bt_h = bt
+        self.bt = torch.from_numpy(bt).to(dev)
+        self.cl_h = w.context_lens.astype(np.int32)
+        self.cl = torch.from_numpy(self.cl_h).to(dev)
+        self.out = torch.empty_like(self.q)
+        nbytes = kvq.kvq_decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                w.head_dim, w.max_context_len)
+        self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.split = nbytes > 0
+        torch.cuda.synchronize()
+
+    def append_int8(self):
+        if self.k_new is not None:
+            self.kvq.kvq_quantize_append(self.k_new, self.v_new, self.slots, *self.int8)
+
+    def decode_int8(self):
+        w = self.w
+        self.kvq.kvq_paged_decode(self.q, *self.int8, self.bt, self.cl, w.max_context_len,
+                                  w.sm_scale, out=self.out, workspace=self.ws)
+
+    def append_kv16(self):
+        if self.k_new is not None:
+            self.kvq.kvq_cache_append_kv16(self.k_new, self.v_new, self.slots, *self.kv16)
+
+    def decode_kv16(self):
+        w = self.w
+        self.kvq.kvq_paged_decode_kv16(self.q, *self.kv16, self.bt, self.cl, w.max_context_len,
+                                       w.sm_scale, out=self.out, workspace=self.ws)
+
+    def launches_per_step(self):
+        return (1 if self.k_new is not None else 0) + 1 + (1 if self.split else 0)
+
+
+def time_arm(torch, flush, append, decode, steps, warmup, settle_s=0.0):
+    """Per-step CUDA-event times (ms) of append+decode and of decode alone."""
+    for _ in range(warmup):
+        flush()
+        append()
+        decode()
+    if settle_s > 0:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < settle_s:
+            for _ in range(50):
+                append()
+                decode()
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record()
+        append()
+        ev[i][1].record()
+        decode()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    step = [a.elapsed_time(c) for a, b, c in ev]
+    dec = [b.elapsed_time(c) for a, b, c in ev]
+    return step, dec
+
+
+def time_e2e(torch, g: GpuWorkload, flush, steps, warmup):
+    """Through the public API with host buffers: pinned H2D of the step's
+    inputs (q, new K/V rows, slots, block tables, context lengths), the two
+    calls, D2H of the output -- all inside the timed region."""
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    q_h = pin(g.q_h.view(np.int16))
+    k_h = pin(g.k_new_h.view(np.int16)) if g.k_new is not None else None
+    v_h = pin(g.v_new_h.view(np.int16)) if g.k_new is not None else None
+    s_h = pin(g.slots_h) if g.k_new is not None else None
+    bt_h, cl_h = pin(g.bt_h), pin(g.cl_h)
+    out_h = torch.empty(g.out.shape, dtype=torch.int16).pin_memory()
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + cl_h.numel() * 4
+    if k_h is not None:
+        h2d += k_h.numel() * 2 * 2 + s_h.numel() * 8
+    d2h = out_h.numel() * 2
+
+    def step():
+        g.q.view(torch.int16).copy_(q_h, non_blocking=True)
+        if k_h is not None:
+            g.k_new.view(torch.int16).copy_(k_h, non_blocking=True)
+            g.v_new.view(torch.int16).copy_(v_h, non_blocking=True)
+            g.slots.copy_(s_h, non_blocking=True)
+        g.bt.copy_(bt_h, non_blocking=True)
+        g.cl.copy_(cl_h, non_blocking=True)
+        g.append_int8()
+        g.decode_int8()
+        out_h.copy_(g.out.view(torch.int16), non_blocking=True)
+
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev], h2d, d2h
+
+
+def sweep(torch, kvq, dev, flush, steps):
+    """INT8 vs BF16-twin decode at 2K/8K/32K context (16 seqs, 32/8 heads,
+    d 128, bf16), inputs drawn on the GPU from a seeded generator."""
+    res = []
+    gen = torch.Generator(device=dev)
+    for ctx in (2048, 8192, 32768):
+        gen.manual_seed(ctx)
+        B, Hq, Hkv, D = 16, 32, 8, 128
+        w = W.custom(B, Hq, Hkv, D, "bf16", [ctx] * B, seed=ctx, pool_factor=1)
+        nb, bt, _ = w.tables()
+        kc, vc, ksc, vsc = kvq.alloc_int8_cache(nb, Hkv, D, dev)
+        k16, v16 = kvq.alloc_kv16_cache(nb, Hkv, D, torch.bfloat16, dev)
+        for b in range(B):
+            k = torch.randn((ctx, Hkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            v = torch.randn((ctx, Hkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            s = torch.from_numpy(w.slots(b, 0, ctx)).to(dev)
+            kvq.kvq_quantize_append(k, v, s, kc, vc, ksc, vsc)
+            kvq.kvq_cache_append_kv16(k, v, s, k16, v16)
+        q = torch.randn((B, Hq, D), generator=gen, device=dev, dtype=torch.bfloat16)
+        btd = torch.from_numpy(bt).to(dev)
+        cl = torch.full((B,), ctx, dtype=torch.int32, device=dev)
+        nbytes = kvq.kvq_decode_workspace_bytes(B, Hq, Hkv, D, ctx)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        d8 = lambda: kvq.kvq_paged_decode(q, kc, vc, ksc, vsc, btd, cl, ctx, w.sm_scale,  # noqa
+                                          out=out, workspace=ws)
+        d16 = lambda: kvq.kvq_paged_decode_kv16(q, k16, v16, btd, cl, ctx, w.sm_scale,  # noqa
+                                                out=out, workspace=ws)
+        nop = lambda: None  # noqa: E731
+        _, t8 = time_arm(torch, flush, nop, d8, steps, 3)
+        _, t16 = time_arm(torch, flush, nop, d16, steps, 3)
+        m8, m16 = statistics.mean(t8), statistics.mean(t16)
+        res.append({"context": ctx, "num_seqs": B, "int8_us": round(1e3 * m8, 2),
+                    "bf16_us": round(1e3 * m16, 2),
+                    "int8_gbs": round(w.decode_bytes_int8() / (m8 * 1e-3) / 1e9, 1),
+                    "bf16_gbs": round(w.decode_bytes_kv16() / (m16 * 1e-3) / 1e9, 1),
+                    "int8_speedup_vs_bf16": round(m16 / m8, 3)})
+        del kc, vc, ksc, vsc, k16, v16
+        torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    rank, local_rank, world = dist_env()
+    import torch
+    import int8_quantized_paged_tokenwise_gb300 as kvq
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    kvq.load(build_if_missing=False)
+
+    w = W.make(args.workload)
+    g = GpuWorkload(w, dev)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()  # noqa: E731
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if pg is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local_rank)
+    barrier()
+    t_step, t_dec = time_arm(torch, flush, g.append_int8, g.decode_int8, args.steps, args.warmup,
+                             settle_s=1.5)
+    barrier()
+    clk = clocks.stop()
+    t_step16, t_dec16 = time_arm(torch, flush, g.append_kv16, g.decode_kv16, args.steps,
+                                 args.warmup)
+    t_e2e, h2d, d2h = time_e2e(torch, g, flush, args.steps, args.warmup)
+    barrier()
+
+    step_ms = max_over_ranks(statistics.mean(t_step))
+    dec_ms = max_over_ranks(statistics.mean(t_dec))
+    step16_ms = max_over_ranks(statistics.mean(t_step16))
+    dec16_ms = max_over_ranks(statistics.mean(t_dec16))
+    e2e_ms = max_over_ranks(statistics.mean(t_e2e))
+    step_bytes = w.append_bytes_int8() + w.decode_bytes_int8()
+    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    dec_gbs = w.decode_bytes_int8() / (dec_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("source_hash") == decode_source_hash() and tr.get("workload") == w.name:
+            traffic = tr.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+    sw = None
+    if not args.no_sweep:
+        sw = sweep(torch, kvq, dev, flush, max(5, min(args.steps, 20)))
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
+        gbs, n, t = time_oracle(w, budget_s=12.0)
+        cpu = {"value": round(gbs, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first {n} of {w.num_seqs} sequences of the {w.name} workload "
+                         f"(quantize-append of the step token + decode of all heads), "
+                         f"{t:.1f} s single-thread FP64"}
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 codes x fp16 (tensor cores), fp32 accumulate", "data": "synthetic",
+        "config": config_of(w, {"parallelism": f"replicas x{world}"}),
+        "decode_gbs": round(dec_gbs, 2),
+        "decode_pct_of_measured_peak": round(100 * dec_gbs / peak, 2),
+        "decode_pct_of_nominal_8tbs": round(100 * dec_gbs / 8000.0, 2),
+        "decode_us": round(1e3 * dec_ms, 3),
+        "bytes_per_decoded_token": round(w.decode_bytes_int8() / w.num_seqs),
+        "steps_per_s": round(1e3 / step_ms, 1),
+        "bf16_twin": {"steps_per_s": round(1e3 / step16_ms, 1), "decode_us": round(1e3 * dec16_ms, 3),
+                      "decode_gbs": round(w.decode_bytes_kv16() / (dec16_ms * 1e-3) / 1e9, 2)},
+        "int8_vs_bf16_steps_per_s": round(step16_ms / step_ms, 3),
+        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(dec_gbs / peak, 4), "traffic": traffic,
+                     "peak_kind": peak_kind,
+                     "kernel": "kvq_paged_decode (decode + split-K combine), algorithmic bytes "
+                               f"{w.decode_bytes_int8()} per launch"},
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": args.steps * g.launches_per_step(),
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "context_sweep": sw,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

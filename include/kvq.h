@@ -1,0 +1,234 @@
+/*
+ * kvq.h -- C ABI of libkvq: tokenwise symmetric INT8 paged KV cache for LLM
+ * decode on GB300 (sm_103a).
+ *
+ * The library has two hot operations and a 16-bit twin of the second:
+ *
+ *   kvq_quantize_append    quantize-on-write of new K/V rows into a paged
+ *                          INT8 cache with one FP16 scale per (page, KV head,
+ *                          token).
+ *   kvq_paged_decode       fused paged decode attention over the INT8 cache:
+ *                          page walk through a block table, dequantization in
+ *                          registers, FP32 accumulation, online softmax, and
+ *                          a split-K (flash-decoding) variant with a combine
+ *                          kernel for long contexts and small batches.
+ *   kvq_paged_decode_kv16  the same decode over a native 16-bit cache (A/B).
+ *
+ * Where the operations are defined (page title, then section):
+ *   [MI] "feat: opt-in INT8 KV-cache quantization" (MoE-Infinity PR #183),
+ *        "What landed" -- tokenwise symmetric INT8 with upward-rounded FP16
+ *        scales, no -128, exact zero, element error <= stored_scale/2 + 1e-6;
+ *        paged INT8 decode with FP16 scales and FP32 accumulation, MHA/GQA;
+ *        "Precision & memory" -- one FP16 scale per (layer, page, KV head,
+ *        token); 33,280 bytes per 16-token, 8-head, d=128 page.
+ *   [ML] "fix(cuda/kv): correct Int8 KV per-token scale ..." (mlxcel PR
+ *        #717), "The Int8 bug and fix" -- scale = absmax/127, 1.0 only for
+ *        an all-zero token; the largest coordinate maps to +-127.
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions common to every call
+ * ---------------------------------------------------------------------------
+ *  - Pointers: every tensor pointer is a DEVICE pointer owned by the caller.
+ *    The library never frees or retains them.  Calls are asynchronous on
+ *    `stream` (a cudaStream_t; NULL = legacy default stream) and never
+ *    synchronize, except kvq_get_error.
+ *  - Allocation: no call allocates device memory.  Split-K scratch is the
+ *    caller's `workspace` (size from kvq_decode_workspace_bytes).
+ *  - One layer per call: per-layer caches are separate base pointers.
+ *  - Cache layout (one layer), block_size bs = 16, D = head_dim:
+ *        payload     int8   [num_blocks][num_kv_heads][bs][D]     (K and V)
+ *        scale plane uint16 [num_blocks][num_kv_heads][bs]        (FP16 bits)
+ *    A token with slot s lives in block s / bs at offset s % bs.  Each
+ *    (block, KV head) tile of the payload is bs*D contiguous bytes.
+ *    Page bytes (K+V, all heads) = bs*Hkv*(2*D + 4): 33,280 at (16, 8, 128).
+ *    16-bit twin cache: dtype [num_blocks][num_kv_heads][bs][D].
+ *  - Block table: int32 [num_seqs][max_blocks_per_seq], row-major; entry i of
+ *    row b is the physical block of logical page i of sequence b.
+ *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - Errors: host-detectable problems (NULL pointers, bad sizes, misaligned
+ *    pointers, unsupported shapes, small workspace) return a status and launch
+ *    nothing.  Device-detectable problems (slot, block id or context length
+ *    out of range) skip the offending item, never fault, and set a bit in a
+ *    per-device error word that kvq_get_error reads and clears.  There is no
+ *    fallback path: an unsupported input is an error.
+ *  - Supported: head_dim 64 or 128; block_size 16; Hq/Hkv in 1..8;
+ *    num_seqs <= 4096; FP16 or BF16 activations.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* kvq_stream_t;
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARGUMENT = 1,   /* NULL pointer, negative size, misaligned  */
+  KVQ_ERR_UNSUPPORTED = 2,        /* shape outside the supported set          */
+  KVQ_ERR_CUDA = 3,               /* a CUDA runtime call failed               */
+  KVQ_ERR_WORKSPACE_TOO_SMALL = 4,
+  KVQ_ERR_DEVICE_INDEX = 5,       /* kvq_get_error: an index was out of range */
+  KVQ_ERR_DEVICE_TIMEOUT = 6      /* kvq_get_error: a bounded wait gave up    */
+} kvq_status;
+
+typedef enum { KVQ_FP16 = 0, KVQ_BF16 = 1 } kvq_dtype;
+
+/* Bits of the device error word (kvq_get_error). */
+#define KVQ_DEVERR_SLOT 0x1u        /* slot >= num_blocks * block_size          */
+#define KVQ_DEVERR_BLOCK 0x2u       /* block id < 0 or >= num_blocks            */
+#define KVQ_DEVERR_CONTEXT 0x4u     /* context_len < 0 or > max_blocks * bs     */
+#define KVQ_DEVERR_TIMEOUT 0x8u     /* an mbarrier wait hit its limit           */
+
+/*
+ * kvq_quantize_append -- tokenwise symmetric INT8 quantize-on-write.
+ * Defined by [MI] "What landed" and [ML] "The Int8 bug and fix".
+ *
+ * For each new token t < num_tokens and KV head j, separately for K and V,
+ * with row x = k[t][j][0..D) (resp. v):
+ *     a = max_d |x_d|
+ *     s = 1.0                                  if a == 0
+ *         smallest FP16 value >= a / 127       otherwise (upward rounding;
+ *                                              saturates at 65504)
+ *     code_d = clamp(round_half_even(x_d / s), -127, 127)
+ * then stores the D codes and the FP16 bits of s at slot slot_mapping[t].
+ * Codes and scales are bit-identical to an exact-arithmetic evaluation.
+ *
+ *   k, v            [num_tokens][num_kv_heads][head_dim] of `dtype`; heads
+ *                   are contiguous (stride head_dim); consecutive tokens are
+ *                   k_token_stride / v_token_stride ELEMENTS apart
+ *                   (>= num_kv_heads*head_dim, multiple of 4); 8-byte aligned.
+ *   slot_mapping    int64 [num_tokens]; negative = skip the token;
+ *                   >= num_blocks*block_size sets KVQ_DEVERR_SLOT (skipped).
+ *   k_cache,v_cache int8 payload (layout above), 16-byte aligned.
+ *   k_scale,v_scale uint16 scale planes (layout above), 16-byte aligned.
+ * num_tokens == 0 is a no-op.  Tokens mapped to the same slot race.
+ */
+kvq_status kvq_quantize_append(const void* k, const void* v, int64_t k_token_stride,
+                               int64_t v_token_stride, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, kvq_dtype dtype,
+                               const int64_t* slot_mapping, int8_t* k_cache, int8_t* v_cache,
+                               uint16_t* k_scale, uint16_t* v_scale, int32_t num_blocks,
+                               int32_t block_size, kvq_stream_t stream);
+
+/*
+ * kvq_paged_decode -- fused paged decode attention over the INT8 cache.
+ * Defined by [MI] "What landed" (INT8 + FP16-scale paged decode, FP32
+ * accumulation, MHA/GQA, checked against dequantized softmax attention).
+ *
+ * For each sequence b with L = context_lens[b] and query head h (KV head j):
+ *     k_hat_t = s_k[t] * code_k[t],  v_hat_t = s_v[t] * code_v[t]
+ *     z_t     = sm_scale * <q[b][h], k_hat_t>,   t < L
+ *     out[b][h] = sum_t softmax(z)_t * v_hat_t        (0 when L == 0)
+ * Token t of sequence b is read from block block_tables[b][t / 16], offset
+ * t % 16.  Arithmetic: codes and q in FP16 on the tensor cores, FP32
+ * accumulation and softmax, output rounded to `dtype`.
+ *
+ *   q, out          [num_seqs][num_q_heads][head_dim] of `dtype`, contiguous,
+ *                   16-byte aligned.
+ *   block_tables    int32 [num_seqs][max_blocks_per_seq].
+ *   context_lens    int32 [num_seqs] (device); max_context_len is a host-side
+ *                   upper bound on every entry (used by the launcher; an entry
+ *                   above max_blocks_per_seq*16 sets KVQ_DEVERR_CONTEXT and
+ *                   that sequence's output is left unspecified).
+ *   workspace       device scratch of >= kvq_decode_workspace_bytes(...)
+ *                   bytes (may be NULL when that is 0), 256-byte aligned, not
+ *                   shared by calls that overlap on the GPU.
+ * The launcher picks the partition size (pages per CTA work item) from
+ * num_seqs, num_kv_heads, max_context_len and the SM count; sequences longer
+ * than one partition go through split-K partials and a combine kernel.
+ */
+kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            const int8_t* k_cache, const int8_t* v_cache,
+                            const uint16_t* k_scale, const uint16_t* v_scale,
+                            int32_t num_blocks, int32_t block_size,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t max_context_len,
+                            float sm_scale, void* out, void* workspace,
+                            size_t workspace_bytes, kvq_stream_t stream);
+
+/* Scratch bytes kvq_paged_decode needs for these sizes on the current device
+ * (0 when no sequence can be split). */
+size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_context_len);
+
+/* The partition size (pages per work item) the launcher picks on the current
+ * device; 0 on invalid input. */
+int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_kv_heads,
+                                   int32_t max_context_len);
+
+/* kvq_paged_decode with the partition size forced (a multiple of 4, >= 4);
+ * used to test every launcher variant.  Workspace from
+ * kvq_decode_workspace_bytes_split with the same partition size. */
+kvq_status kvq_paged_decode_split(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  const int8_t* k_cache, const int8_t* v_cache,
+                                  const uint16_t* k_scale, const uint16_t* v_scale,
+                                  int32_t num_blocks, int32_t block_size,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t max_context_len,
+                                  float sm_scale, void* out, void* workspace,
+                                  size_t workspace_bytes, int32_t partition_pages,
+                                  kvq_stream_t stream);
+
+size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_context_len, int32_t partition_pages);
+
+/*
+ * kvq_paged_decode_kv16 -- the same decode over a native 16-bit cache (K and
+ * V in `dtype`, no scales); the A/B twin of kvq_paged_decode.  Arguments as
+ * kvq_paged_decode; k_cache/v_cache are [num_blocks][num_kv_heads][16][D] of
+ * `dtype`.  Workspace from kvq_decode_workspace_bytes (same sizes).
+ * Arithmetic: q, K, V, P in `dtype` on the tensor cores, FP32 accumulation.
+ */
+kvq_status kvq_paged_decode_kv16(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 const void* k_cache, const void* v_cache, int32_t num_blocks,
+                                 int32_t block_size, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                 int32_t max_context_len, float sm_scale, void* out,
+                                 void* workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+kvq_status kvq_paged_decode_kv16_split(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, const void* k_cache,
+                                       const void* v_cache, int32_t num_blocks,
+                                       int32_t block_size, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t max_context_len, float sm_scale, void* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t partition_pages, kvq_stream_t stream);
+
+/* Scatter copy of new 16-bit K/V rows into the twin's cache (no
+ * quantization): the write half of the 16-bit A/B path.  Arguments as
+ * kvq_quantize_append; caches are [num_blocks][num_kv_heads][16][D] of dtype. */
+kvq_status kvq_cache_append_kv16(const void* k, const void* v, int64_t k_token_stride,
+                                 int64_t v_token_stride, int32_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_dim, kvq_dtype dtype,
+                                 const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                 int32_t num_blocks, int32_t block_size, kvq_stream_t stream);
+
+/* Synchronizes `stream`, then reads and clears the current device's error
+ * word.  *flags (may be NULL) receives the KVQ_DEVERR_* bits.  Returns
+ * KVQ_OK when no bit was set, KVQ_ERR_DEVICE_TIMEOUT if the timeout bit was
+ * set, else KVQ_ERR_DEVICE_INDEX. */
+kvq_status kvq_get_error(kvq_stream_t stream, uint32_t* flags);
+
+/* Static, NUL-terminated description of a status code. */
+const char* kvq_status_string(kvq_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

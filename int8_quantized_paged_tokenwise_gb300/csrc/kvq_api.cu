@@ -1,0 +1,449 @@
+// C ABI of libkvq (declared in include/kvq.h): argument validation, the
+// decode launcher, TMA descriptor construction, and the device error word.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+using namespace kvq;
+
+// Per-device error word: kernels OR KVQ_DEVERR_* bits into it, kvq_get_error
+// reads and clears it.
+__device__ unsigned int g_kvq_error_word = 0u;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxPartitionPages = 1024;
+constexpr int kMaxAutoPartitionPages = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  unsigned int* err = nullptr;
+  // occupancy cache: [variant][last smem] -> ctas per SM
+  size_t occ_smem[6] = {0, 0, 0, 0, 0, 0};
+  int occ_ctas[6] = {0, 0, 0, 0, 0, 0};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+kvq_status cuda_fail() { return KVQ_ERR_CUDA; }
+
+// Initializes the current device's state once; returns nullptr on failure.
+DeviceState* device_state() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (st.ready) return &st;
+  if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), g_kvq_error_word) != cudaSuccess)
+    return nullptr;
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return nullptr;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  // opt every decode variant into the largest shared-memory footprint it can use
+  for (int D : {64, 128}) {
+    for (bool bf : {false, true}) {
+      if (decode_configure_int8(D, bf, decode_smem_bytes_int8(D, kMaxSeqs, kMaxPartitionPages)) !=
+              cudaSuccess ||
+          decode_configure_kv16(D, bf, decode_smem_bytes_kv16(D, kMaxSeqs, kMaxPartitionPages)) !=
+              cudaSuccess)
+        return nullptr;
+    }
+  }
+  st.ready = true;
+  return &st;
+}
+
+int ctas_per_sm(DeviceState* st, bool int8, int D, bool bf16, size_t smem) {
+  // variants: int8 D128/D64 (activation dtype does not change the footprint),
+  // kv16 D128/D64 x fp16/bf16
+  int v = int8 ? (D == 128 ? 0 : 1) : (2 + (D == 128 ? 0 : 1) * 2 + (bf16 ? 1 : 0));
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st->occ_smem[v] != smem || st->occ_ctas[v] == 0) {
+    int n = 0;
+    cudaError_t e = int8 ? decode_occupancy_int8(D, bf16, smem, &n)
+                         : decode_occupancy_kv16(D, bf16, smem, &n);
+    if (e != cudaSuccess || n <= 0) return 0;
+    st->occ_smem[v] = smem;
+    st->occ_ctas[v] = n;
+  }
+  return st->occ_ctas[v];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Pages per partition chosen by the launcher: enough work items to fill the
+// GPU several times over (by an upper bound on the work, since only
+// max_context_len is known on the host), in [8, 64] pages, and no larger
+// than the longest sequence needs.
+int32_t auto_partition_pages(int32_t B, int32_t Hkv, int32_t max_ctx, int sms) {
+  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
+  if (pages_max <= 0) return kWarps;
+  const int64_t slots = (int64_t)sms * 3;
+  const int64_t target_items = 8 * slots;
+  const int64_t est = (int64_t)B * Hkv * pages_max;
+  int64_t P = cdiv(est, target_items);
+  int64_t p2 = 8;
+  while (p2 < P && p2 < kMaxAutoPartitionPages) p2 <<= 1;
+  const int64_t cap = cdiv(pages_max, kWarps) * kWarps;   // a single partition suffices
+  return (int32_t)(p2 < cap ? p2 : cap);
+}
+
+struct WsLayout {
+  size_t prefix = 0, lse = 0, o = 0, total = 0;
+  bool split = false;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WsLayout workspace_layout(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_ctx,
+                          int32_t P) {
+  WsLayout w;
+  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
+  const int64_t parts_max = pages_max > 0 ? cdiv(pages_max, P) : 1;
+  if (parts_max <= 1 || B == 0) return w;
+  const int64_t sp_max = (int64_t)B * parts_max;
+  const int64_t G = Hq / Hkv;
+  w.split = true;
+  w.prefix = 0;
+  w.lse = round_up((size_t)B * 4, 256);
+  w.o = w.lse + round_up((size_t)(sp_max * Hkv * G) * 4, 256);
+  w.total = w.o + (size_t)(sp_max * Hkv * G * D) * 4;
+  return w;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int elem_bytes, int D, int64_t rows) {
+  const CUtensorMapDataType dt =
+      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const int row_bytes = D * elem_bytes;
+  const int sub = row_bytes < 128 ? row_bytes : 128;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(sub / elem_bytes), (cuuint32_t)kBlockSize};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = sub == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Shared validation of the decode arguments (both caches).
+kvq_status check_decode(const void* q, kvq_dtype dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                        int32_t D, const void* kc, const void* vc, const void* ks,
+                        const void* vs, bool int8, int32_t num_blocks, int32_t bs,
+                        const int32_t* bt, int32_t max_blocks, const int32_t* cl,
+                        int32_t max_ctx, float sm_scale, const void* out) {
+  if (dtype != KVQ_FP16 && dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARGUMENT;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || num_blocks <= 0 || max_ctx < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (bs != kBlockSize) return KVQ_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (Hq / Hkv > kMaxGroup) return KVQ_ERR_UNSUPPORTED;
+  if (B > kMaxSeqs) return KVQ_ERR_UNSUPPORTED;
+  if ((int64_t)num_blocks * Hkv * kBlockSize > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+  if (B == 0) return KVQ_OK;
+  if (max_blocks <= 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if ((int64_t)max_ctx > (int64_t)max_blocks * kBlockSize) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!q || !kc || !vc || !bt || !cl || !out) return KVQ_ERR_INVALID_ARGUMENT;
+  if (int8 && (!ks || !vs)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(kc, 16) || !aligned(vc, 16) ||
+      !aligned(bt, 4) || !aligned(cl, 4))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (int8 && (!aligned(ks, 16) || !aligned(vs, 16))) return KVQ_ERR_INVALID_ARGUMENT;
+  return KVQ_OK;
+}
+
+kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, int32_t Hq,
+                         int32_t Hkv, int32_t D, const void* kc, const void* vc,
+                         const uint16_t* ks, const uint16_t* vs, int32_t num_blocks,
+                         int32_t bs, const int32_t* bt, int32_t max_blocks, const int32_t* cl,
+                         int32_t max_ctx, float sm_scale, void* out, void* ws, size_t ws_bytes,
+                         int32_t P, cudaStream_t stream) {
+  kvq_status s = check_decode(q, dtype, B, Hq, Hkv, D, kc, vc, ks, vs, int8, num_blocks, bs, bt,
+                              max_blocks, cl, max_ctx, sm_scale, out);
+  if (s != KVQ_OK || B == 0) return s;
+  DeviceState* st = device_state();
+  if (!st) return cuda_fail();
+  if (P == 0) P = auto_partition_pages(B, Hkv, max_ctx, st->sms);
+  if (P < kWarps || P % kWarps != 0 || P > kMaxPartitionPages) return KVQ_ERR_INVALID_ARGUMENT;
+  const bool bf16 = dtype == KVQ_BF16;
+  const WsLayout wl = workspace_layout(B, Hq, Hkv, D, max_ctx, P);
+  if (wl.split) {
+    if (ws_bytes < wl.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+    if (!ws || !aligned(ws, 256)) return KVQ_ERR_INVALID_ARGUMENT;
+  }
+
+  CUtensorMap tmk, tmv;
+  const int64_t rows = (int64_t)num_blocks * Hkv * kBlockSize;
+  const int eb = int8 ? 1 : 2;
+  if (!make_map(&tmk, kc, eb, D, rows) || !make_map(&tmv, vc, eb, D, rows)) return cuda_fail();
+
+  DecodeParams p{};
+  p.q = q;
+  p.out = out;
+  p.k_scale = ks;
+  p.v_scale = vs;
+  p.block_tables = bt;
+  p.context_lens = cl;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.prefix_out = wl.split ? reinterpret_cast<int32_t*>(w + wl.prefix) : nullptr;
+  p.part_lse = wl.split ? reinterpret_cast<float*>(w + wl.lse) : nullptr;
+  p.part_o = wl.split ? reinterpret_cast<float*>(w + wl.o) : nullptr;
+  p.err = st->err;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.max_blocks = max_blocks;
+  p.max_ctx = max_ctx;
+  p.num_blocks = num_blocks;
+  p.P = P;
+  p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
+
+  const size_t smem =
+      int8 ? decode_smem_bytes_int8(D, B, P) : decode_smem_bytes_kv16(D, B, P);
+  const int occ = ctas_per_sm(st, int8, D, bf16, smem);
+  if (occ <= 0) return cuda_fail();
+  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
+  const int64_t items_max = (int64_t)B * Hkv * (pages_max > 0 ? cdiv(pages_max, P) : 1);
+  const int64_t slots = (int64_t)st->sms * occ;
+  const int grid = (int)(items_max < slots ? items_max : slots);
+  cudaError_t e = int8 ? decode_launch_int8(D, bf16, &tmk, &tmv, p, grid, smem, stream)
+                       : decode_launch_kv16(D, bf16, &tmk, &tmv, p, grid, smem, stream);
+  if (e != cudaSuccess) return cuda_fail();
+  if (wl.split) {
+    CombineParams cp{};
+    cp.part_o = p.part_o;
+    cp.part_lse = p.part_lse;
+    cp.prefix = p.prefix_out;
+    cp.out = out;
+    cp.B = B;
+    cp.Hq = Hq;
+    cp.Hkv = Hkv;
+    cp.G = p.G;
+    if (combine_launch(D, bf16, cp, stream) != cudaSuccess) return cuda_fail();
+  }
+  return KVQ_OK;
+}
+
+kvq_status check_append(const void* k, const void* v, int64_t ks, int64_t vs, int32_t T,
+                        int32_t Hkv, int32_t D, kvq_dtype dtype, const int64_t* slots,
+                        const void* kc, const void* vc, int32_t num_blocks, int32_t bs) {
+  if (dtype != KVQ_FP16 && dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARGUMENT;
+  if (T < 0 || Hkv <= 0 || num_blocks <= 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (bs != kBlockSize) return KVQ_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
+  if (T == 0) return KVQ_OK;
+  if (!k || !v || !slots || !kc || !vc) return KVQ_ERR_INVALID_ARGUMENT;
+  if (ks < (int64_t)Hkv * D || vs < (int64_t)Hkv * D || ks % 4 || vs % 4)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(k, 8) || !aligned(v, 8) || !aligned(slots, 8) || !aligned(kc, 16) ||
+      !aligned(vc, 16))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_quantize_append(const void* k, const void* v, int64_t k_token_stride,
+                               int64_t v_token_stride, int32_t num_tokens, int32_t num_kv_heads,
+                               int32_t head_dim, kvq_dtype dtype, const int64_t* slot_mapping,
+                               int8_t* k_cache, int8_t* v_cache, uint16_t* k_scale,
+                               uint16_t* v_scale, int32_t num_blocks, int32_t block_size,
+                               kvq_stream_t stream) {
+  kvq_status s = check_append(k, v, k_token_stride, v_token_stride, num_tokens, num_kv_heads,
+                              head_dim, dtype, slot_mapping, k_cache, v_cache, num_blocks,
+                              block_size);
+  if (s != KVQ_OK || num_tokens == 0) return s;
+  if (!k_scale || !v_scale || !aligned(k_scale, 16) || !aligned(v_scale, 16))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  DeviceState* st = device_state();
+  if (!st) return cuda_fail();
+  QuantParams p{};
+  p.k = k;
+  p.v = v;
+  p.k_stride = k_token_stride;
+  p.v_stride = v_token_stride;
+  p.slots = slot_mapping;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.num_rows = (int64_t)num_tokens * num_kv_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_slots = (int64_t)num_blocks * kBlockSize;
+  p.err = st->err;
+  if (quantize_append_launch(head_dim, dtype == KVQ_BF16, p,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_append_kv16(const void* k, const void* v, int64_t k_token_stride,
+                                 int64_t v_token_stride, int32_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_dim, kvq_dtype dtype,
+                                 const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                 int32_t num_blocks, int32_t block_size, kvq_stream_t stream) {
+  kvq_status s = check_append(k, v, k_token_stride, v_token_stride, num_tokens, num_kv_heads,
+                              head_dim, dtype, slot_mapping, k_cache, v_cache, num_blocks,
+                              block_size);
+  if (s != KVQ_OK || num_tokens == 0) return s;
+  DeviceState* st = device_state();
+  if (!st) return cuda_fail();
+  QuantParams p{};
+  p.k = k;
+  p.v = v;
+  p.k_stride = k_token_stride;
+  p.v_stride = v_token_stride;
+  p.slots = slot_mapping;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.num_rows = (int64_t)num_tokens * num_kv_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_slots = (int64_t)num_blocks * kBlockSize;
+  p.err = st->err;
+  if (append_kv16_launch(head_dim, p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return KVQ_OK;
+}
+
+kvq_status kvq_paged_decode_split(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  const int8_t* k_cache, const int8_t* v_cache,
+                                  const uint16_t* k_scale, const uint16_t* v_scale,
+                                  int32_t num_blocks, int32_t block_size,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t max_context_len,
+                                  float sm_scale, void* out, void* workspace,
+                                  size_t workspace_bytes, int32_t partition_pages,
+                                  kvq_stream_t stream) {
+  if (partition_pages <= 0) return KVQ_ERR_INVALID_ARGUMENT;
+  return decode_common(true, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+                       v_cache, k_scale, v_scale, num_blocks, block_size, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
+                       workspace, workspace_bytes, partition_pages,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            const int8_t* k_cache, const int8_t* v_cache,
+                            const uint16_t* k_scale, const uint16_t* v_scale,
+                            int32_t num_blocks, int32_t block_size,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t max_context_len,
+                            float sm_scale, void* out, void* workspace, size_t workspace_bytes,
+                            kvq_stream_t stream) {
+  return decode_common(true, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+                       v_cache, k_scale, v_scale, num_blocks, block_size, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
+                       workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_paged_decode_kv16_split(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, const void* k_cache,
+                                       const void* v_cache, int32_t num_blocks,
+                                       int32_t block_size, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t max_context_len, float sm_scale, void* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t partition_pages, kvq_stream_t stream) {
+  if (partition_pages <= 0) return KVQ_ERR_INVALID_ARGUMENT;
+  return decode_common(false, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+                       v_cache, nullptr, nullptr, num_blocks, block_size, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
+                       workspace, workspace_bytes, partition_pages,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_paged_decode_kv16(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 const void* k_cache, const void* v_cache, int32_t num_blocks,
+                                 int32_t block_size, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                 int32_t max_context_len, float sm_scale, void* out,
+                                 void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  return decode_common(false, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+                       v_cache, nullptr, nullptr, num_blocks, block_size, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
+                       workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_kv_heads,
+                                   int32_t max_context_len) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0) return 0;
+  DeviceState* st = device_state();
+  if (!st) return 0;
+  return auto_partition_pages(num_seqs, num_kv_heads, max_context_len, st->sms);
+}
+
+size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_context_len, int32_t partition_pages) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
+      partition_pages < kWarps || num_q_heads % num_kv_heads)
+    return 0;
+  return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                          partition_pages)
+      .total;
+}
+
+size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_context_len) {
+  const int32_t P = kvq_decode_partition_pages(num_seqs, num_kv_heads, max_context_len);
+  if (P <= 0) return 0;
+  return kvq_decode_workspace_bytes_split(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                          max_context_len, P);
+}
+
+kvq_status kvq_get_error(kvq_stream_t stream, uint32_t* flags) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_kvq_error_word, sizeof v) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (v != 0 && cudaMemcpyToSymbol(g_kvq_error_word, &zero, sizeof zero) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  if (flags) *flags = v;
+  if (v == 0) return KVQ_OK;
+  return (v & KVQ_DEVERR_TIMEOUT) ? KVQ_ERR_DEVICE_TIMEOUT : KVQ_ERR_DEVICE_INDEX;
+}
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case KVQ_ERR_CUDA: return "CUDA runtime error";
+    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case KVQ_ERR_DEVICE_INDEX: return "device-side index out of range";
+    case KVQ_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t kvq_version(void) { return 100; }
+
+}  // extern "C"

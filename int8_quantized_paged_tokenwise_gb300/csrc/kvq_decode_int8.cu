@@ -1,0 +1,43 @@
+// Instantiations of the INT8-cache decode kernel (head_dim 64/128, FP16/BF16
+// activations) and their host-side launch helpers.
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+namespace {
+template <int D, bool BF16>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(&paged_decode_kernel<D, true, BF16>);
+}
+const void* pick(int D, bool bf16) {
+  if (D == 128) return bf16 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+  return bf16 ? kernel_ptr<64, true>() : kernel_ptr<64, false>();
+}
+}  // namespace
+
+size_t decode_smem_bytes_int8(int D, int B, int P) {
+  return D == 128 ? SmemLayout<128, true>::total(B, P) : SmemLayout<64, true>::total(B, P);
+}
+
+cudaError_t decode_configure_int8(int D, bool bf16, size_t smem) {
+  return cudaFuncSetAttribute(pick(D, bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
+}
+
+cudaError_t decode_occupancy_int8(int D, bool bf16, size_t smem, int* n) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, pick(D, bf16), kThreads, smem);
+}
+
+cudaError_t decode_launch_int8(int D, bool bf16, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                               const DecodeParams& p, int grid, size_t smem, cudaStream_t s) {
+  if (D == 128) {
+    if (bf16) paged_decode_kernel<128, true, true><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+    else paged_decode_kernel<128, true, false><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+  } else {
+    if (bf16) paged_decode_kernel<64, true, true><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+    else paged_decode_kernel<64, true, false><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,43 @@
+// Instantiations of the 16-bit-cache decode kernel (the A/B twin) and their
+// host-side launch helpers.
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+namespace {
+template <int D, bool BF16>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(&paged_decode_kernel<D, false, BF16>);
+}
+const void* pick(int D, bool bf16) {
+  if (D == 128) return bf16 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+  return bf16 ? kernel_ptr<64, true>() : kernel_ptr<64, false>();
+}
+}  // namespace
+
+size_t decode_smem_bytes_kv16(int D, int B, int P) {
+  return D == 128 ? SmemLayout<128, false>::total(B, P) : SmemLayout<64, false>::total(B, P);
+}
+
+cudaError_t decode_configure_kv16(int D, bool bf16, size_t smem) {
+  return cudaFuncSetAttribute(pick(D, bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
+}
+
+cudaError_t decode_occupancy_kv16(int D, bool bf16, size_t smem, int* n) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, pick(D, bf16), kThreads, smem);
+}
+
+cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                               const DecodeParams& p, int grid, size_t smem, cudaStream_t s) {
+  if (D == 128) {
+    if (bf16) paged_decode_kernel<128, false, true><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+    else paged_decode_kernel<128, false, false><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+  } else {
+    if (bf16) paged_decode_kernel<64, false, true><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+    else paged_decode_kernel<64, false, false><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvq
