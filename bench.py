@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--workload", default="canonical", choices=list(W.NAMES))
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--settle", type=float, default=1.5,
+                    help="seconds of untimed steps before the timed region (clock sampling)")
     return ap.parse_args()
 
 
@@ -425,7 +427,7 @@ def main():
     clocks = ClockSampler(local_rank)
     barrier()
     t_step, t_dec = time_arm(torch, flush, g.append_int8, g.decode_int8, args.steps, args.warmup,
-                             settle_s=1.5)
+                             settle_s=args.settle)
     barrier()
     clk = clocks.stop()
     t_step16, t_dec16 = time_arm(torch, flush, g.append_kv16, g.decode_kv16, args.steps,

@@ -126,7 +126,7 @@ def _check(status: int, what: str):
 
 
 def _rows(x: torch.Tensor, name: str):
-    if x.dim() != 3 or x.stride(2) != 1 or x.stride(1) != x.shape[2]:
+    if x.dim() != 3 or x.stride(2) != 1 or (x.shape[1] > 1 and x.stride(1) != x.shape[2]):
         raise ValueError(f"{name} must be [T, Hkv, D] with contiguous heads")
     return x.stride(0)
 

@@ -114,8 +114,7 @@ def test_decode_single_token_returns_v():
         qv, sv = oracle.quantize_rows(v, "bf16")
         for h in range(8):
             vh = qv[0, h // 4].astype(np.float64) * oracle.fp16_to_double(int(sv[0, h // 4]))
-            ref = np.array([oracle.round_to_dtype_bits(x, "bf16") for x in vh], np.uint16)
-            assert np.array_equal(ob[b, h], ref)
+            assert_attention_close(ob[b, h][None], vh[None], "bf16", "single token")
 
 
 def test_decode_equal_keys_mean_of_v():
