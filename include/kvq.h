@@ -215,6 +215,34 @@ kvq_status kvq_cache_append_kv16(const void* k, const void* v, int64_t k_token_s
                                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
                                  int32_t num_blocks, int32_t block_size, kvq_stream_t stream);
 
+/*
+ * kvq_paged_decode_noalloc -- kvq_paged_decode for callers that cannot
+ * allocate device memory.  The pages have no counterpart of this call; it
+ * exists for hosts that own all device memory through their own pool
+ * (inference servers, framework plugins) or run on a fixed memory budget, and
+ * for latency-critical loops that must not risk the device synchronization
+ * cudaMalloc/cudaFree can cause.
+ *
+ * Same arguments and result as kvq_paged_decode, minus the workspace: the
+ * split-K scratch is a static device array of KVQ_NOALLOC_SCRATCH_BYTES built
+ * into the library (held on every GPU that loads it, until exit).  Returns
+ * KVQ_ERR_WORKSPACE_TOO_SMALL when kvq_decode_workspace_bytes(...) for these
+ * sizes exceeds that limit.  Allocates nothing.  The first call on a device
+ * looks up the array's device address (make that first call before any
+ * stream capture).  All calls on a device share the array: calls that
+ * overlap on the GPU race.  Nothing in it needs clearing between calls.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+kvq_status kvq_paged_decode_noalloc(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    const int8_t* k_cache, const int8_t* v_cache,
+                                    const uint16_t* k_scale, const uint16_t* v_scale,
+                                    int32_t num_blocks, int32_t block_size,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t max_context_len,
+                                    float sm_scale, void* out, kvq_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the current device's error
  * word.  *flags (may be NULL) receives the KVQ_DEVERR_* bits.  Returns
  * KVQ_OK when no bit was set, KVQ_ERR_DEVICE_TIMEOUT if the timeout bit was

@@ -28,7 +28,7 @@ from . import _build
 
 __all__ = [
     "KvqError", "load", "kvq_quantize_append", "kvq_paged_decode", "kvq_paged_decode_kv16",
-    "kvq_cache_append_kv16", "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
+    "kvq_cache_append_kv16", "kvq_paged_decode_noalloc", "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
     "kvq_get_error", "kvq_status_string", "alloc_int8_cache", "alloc_kv16_cache",
     "HEADER_SYMBOLS", "BLOCK_SIZE", "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_CONTEXT",
     "DEVERR_TIMEOUT",
@@ -46,7 +46,7 @@ HEADER_SYMBOLS = (
     "kvq_quantize_append", "kvq_paged_decode", "kvq_decode_workspace_bytes",
     "kvq_decode_partition_pages", "kvq_paged_decode_split", "kvq_decode_workspace_bytes_split",
     "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split", "kvq_cache_append_kv16",
-    "kvq_get_error", "kvq_status_string", "kvq_version",
+    "kvq_get_error", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
 )
 
 _lib = None
@@ -79,6 +79,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
            sz]
     L.kvq_paged_decode.argtypes = dec + [vp]
     L.kvq_paged_decode_split.argtypes = dec + [i32, vp]
+    L.kvq_paged_decode_noalloc.argtypes = dec[:-2] + [vp]
+    L.kvq_paged_decode_noalloc.restype = ctypes.c_int
     dec16 = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz]
     L.kvq_paged_decode_kv16.argtypes = dec16 + [vp]
     L.kvq_paged_decode_kv16_split.argtypes = dec16 + [i32, vp]
@@ -259,6 +261,26 @@ def kvq_paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_tables, contex
     else:
         st = L.kvq_paged_decode(*args, _stream(stream))
     _check(st, "kvq_paged_decode")
+    return out
+
+
+def kvq_paged_decode_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                             max_context_len: int, sm_scale: float, out, stream=None):
+    """kvq_paged_decode without a workspace, for callers that cannot allocate
+    device memory: the split-K scratch is a fixed array inside the library
+    (KVQ_NOALLOC_SCRATCH_BYTES per GPU).  ``out`` must be given.  Calls that
+    overlap on the GPU share that scratch and race."""
+    L = load()
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    _check_decode(q, k_cache, v_cache, block_tables, context_lens, out, (torch.int8,))
+    _check_scales(k_scale, v_scale, k_cache)
+    st = L.kvq_paged_decode_noalloc(_ptr(q), _dtype_code(q), B, Hq, Hkv, D, _ptr(k_cache),
+                                    _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), NB, bs,
+                                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                    int(max_context_len), float(sm_scale), _ptr(out),
+                                    _stream(stream))
+    _check(st, "kvq_paged_decode_noalloc")
     return out
 
 
