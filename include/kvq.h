@@ -158,12 +158,12 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
 size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len);
 
-/* The partition size (pages per work item) the launcher picks on the current
- * device; 0 on invalid input. */
+/* The partition size (pages per work item; one warp processes one item) the
+ * launcher picks on the current device; 0 on invalid input. */
 int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_kv_heads,
                                    int32_t max_context_len);
 
-/* kvq_paged_decode with the partition size forced (a multiple of 4, >= 4);
+/* kvq_paged_decode with the partition size forced (pages per work item, >= 1);
  * used to test every launcher variant.  Workspace from
  * kvq_decode_workspace_bytes_split with the same partition size. */
 kvq_status kvq_paged_decode_split(const void* q, kvq_dtype dtype, int32_t num_seqs,

@@ -18,7 +18,7 @@ __device__ unsigned int g_kvq_error_word = 0u;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxPartitionPages = 1024;
+constexpr int kMaxPartitionPages = 1 << 16;
 constexpr int kMaxAutoPartitionPages = 64;
 
 struct DeviceState {
@@ -59,9 +59,9 @@ DeviceState* device_state() {
   // opt every decode variant into the largest shared-memory footprint it can use
   for (int D : {64, 128}) {
     for (bool bf : {false, true}) {
-      if (decode_configure_int8(D, bf, decode_smem_bytes_int8(D, kMaxSeqs, kMaxPartitionPages)) !=
+      if (decode_configure_int8(D, bf, decode_smem_bytes_int8(D, kMaxSeqs, kMaxGroup)) !=
               cudaSuccess ||
-          decode_configure_kv16(D, bf, decode_smem_bytes_kv16(D, kMaxSeqs, kMaxPartitionPages)) !=
+          decode_configure_kv16(D, bf, decode_smem_bytes_kv16(D, kMaxSeqs, kMaxGroup)) !=
               cudaSuccess)
         return nullptr;
     }
@@ -90,21 +90,20 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Pages per partition chosen by the launcher: enough work items to fill the
-// GPU several times over (by an upper bound on the work, since only
-// max_context_len is known on the host), in [8, 64] pages, and no larger
-// than the longest sequence needs.
+// Pages per partition (one warp's work item) chosen by the launcher: about
+// three items per resident warp over an upper bound of the work (only
+// max_context_len is known on the host), a power of two in [8, 64] so that
+// skewed batches still split their longest sequences, and no larger than the
+// longest sequence needs.
 int32_t auto_partition_pages(int32_t B, int32_t Hkv, int32_t max_ctx, int sms) {
   const int64_t pages_max = cdiv(max_ctx, kBlockSize);
-  if (pages_max <= 0) return kWarps;
-  const int64_t slots = (int64_t)sms * 3;
-  const int64_t target_items = 8 * slots;
+  if (pages_max <= 0) return 8;
+  const int64_t warps = (int64_t)sms * 3 * kWarps;
   const int64_t est = (int64_t)B * Hkv * pages_max;
-  int64_t P = cdiv(est, target_items);
+  const int64_t want = cdiv(est, 3 * warps);
   int64_t p2 = 8;
-  while (p2 < P && p2 < kMaxAutoPartitionPages) p2 <<= 1;
-  const int64_t cap = cdiv(pages_max, kWarps) * kWarps;   // a single partition suffices
-  return (int32_t)(p2 < cap ? p2 : cap);
+  while (p2 < want && p2 < kMaxAutoPartitionPages) p2 <<= 1;
+  return (int32_t)(p2 < pages_max ? p2 : pages_max);
 }
 
 struct WsLayout {
@@ -185,7 +184,7 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   DeviceState* st = device_state();
   if (!st) return cuda_fail();
   if (P == 0) P = auto_partition_pages(B, Hkv, max_ctx, st->sms);
-  if (P < kWarps || P % kWarps != 0 || P > kMaxPartitionPages) return KVQ_ERR_INVALID_ARGUMENT;
+  if (P < 1 || P > kMaxPartitionPages) return KVQ_ERR_INVALID_ARGUMENT;
   const bool bf16 = dtype == KVQ_BF16;
   const WsLayout wl = workspace_layout(B, Hq, Hkv, D, max_ctx, P);
   if (wl.split) {
@@ -221,13 +220,14 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
 
   const size_t smem =
-      int8 ? decode_smem_bytes_int8(D, B, P) : decode_smem_bytes_kv16(D, B, P);
+      int8 ? decode_smem_bytes_int8(D, B, p.G) : decode_smem_bytes_kv16(D, B, p.G);
   const int occ = ctas_per_sm(st, int8, D, bf16, smem);
   if (occ <= 0) return cuda_fail();
   const int64_t pages_max = cdiv(max_ctx, kBlockSize);
   const int64_t items_max = (int64_t)B * Hkv * (pages_max > 0 ? cdiv(pages_max, P) : 1);
   const int64_t slots = (int64_t)st->sms * occ;
-  const int grid = (int)(items_max < slots ? items_max : slots);
+  const int64_t ctas_needed = cdiv(items_max, kWarps);       // one item per warp at least
+  const int grid = (int)(ctas_needed < slots ? ctas_needed : slots);
   cudaError_t e = int8 ? decode_launch_int8(D, bf16, &tmk, &tmv, p, grid, smem, stream)
                        : decode_launch_kv16(D, bf16, &tmk, &tmv, p, grid, smem, stream);
   if (e != cudaSuccess) return cuda_fail();
@@ -404,7 +404,7 @@ size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
                                         int32_t num_kv_heads, int32_t head_dim,
                                         int32_t max_context_len, int32_t partition_pages) {
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
-      partition_pages < kWarps || num_q_heads % num_kv_heads)
+      partition_pages < 1 || num_q_heads % num_kv_heads)
     return 0;
   return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
                           partition_pages)

@@ -9,29 +9,41 @@
 // and the split into partitions with a log-sum-exp combine are the
 // flash-decoding formulation of the same sum.
 //
-// Structure (one CTA = 4 warps, persistent over a flat list of work items):
-//  * work item = (sequence-partition, KV head); a sequence of L tokens has
-//    max(1, ceil(ceil(L/16) / P)) partitions of P pages.  Every CTA rebuilds
-//    the partition prefix from context_lens in shared memory and strides over
-//    the items, so skewed context lengths need no host-side planning.
-//  * each warp owns every 4th page of the item and a private ring of S
-//    stages; lane 0 streams its pages with TMA: the K and V tiles of the
-//    (page, KV head) as 2-D tensor copies with the 128-/64-byte swizzle (so
-//    that the ldmatrix reads below are bank-conflict free) and, for INT8, the
-//    two 32-byte scale rows as 1-D bulk copies, all completing on one
-//    mbarrier.  Waits are bounded (error bit + clean exit on timeout).
+// Structure:
+//  * work item = (sequence, KV head, partition of P pages), processed by ONE
+//    warp; a sequence of L tokens has max(1, ceil(ceil(L/16) / P)) partitions.
+//    Every CTA rebuilds the partition prefix from context_lens in shared
+//    memory; warps then stride over the flat item list independently (no
+//    CTA-wide synchronization after start-up), so skewed context lengths need
+//    no host-side planning.
+//  * each warp keeps one continuous stream of page loads across its items:
+//    lane 0 issues, S pages ahead of the consumer, TMA copies of the
+//    (page, KV head) K and V tiles (2-D tensor copies with the 128-/64-byte
+//    swizzle so that the ldmatrix reads are bank-conflict free) and, for INT8,
+//    the two 32-byte scale rows (1-D bulk copies), all completing on the
+//    stage's mbarrier; an item's first page also brings the item's query rows.
+//    Block ids come from the block table 32 pages at a time, the next item's
+//    first chunk prefetched.  Waits are bounded (error bit + exit on timeout).
 //  * QK^T and PV run on the tensor cores (mma.sync m16n8k16, FP32 accumulate)
-//    with the GQA group as the M dimension (padded to 16) so each page is
+//    with the GQA group as the M dimension (padded to 16), so each page is
 //    read once for all query heads of its KV head.  INT8 codes become exact
-//    FP16 integers with two byte permutes and one subtraction; K scales
-//    multiply the FP32 scores, V scales multiply the converted V pairs.
-//  * at the end of an item the warps merge (m, l, O) through shared memory
-//    and write either the final output or a normalized partial + log2-sum-exp
-//    for the combine kernel.
+//    FP16 integers with a byte permute and a subtraction; K scales multiply
+//    the FP32 scores, V scales multiply the converted V pairs.
+//  * at the end of an item the warp writes the final output (one partition)
+//    or a normalized partial + log2-sum-exp for the combine kernel.
 #pragma once
 
 #include "kvq_internal.h"
 #include "kvq_ptx.cuh"
+
+// Pages in flight per warp and the CTAs per SM the register budget targets
+// (INT8 cache; the 16-bit twin uses 2 stages and 3 CTAs).
+#ifndef KVQ_INT8_STAGES
+#define KVQ_INT8_STAGES 2
+#endif
+#ifndef KVQ_INT8_MIN_CTAS
+#define KVQ_INT8_MIN_CTAS 4
+#endif
 
 namespace kvq {
 
@@ -43,13 +55,12 @@ struct TileCfg {
   static constexpr int kSubTiles = kRowBytes / kSubRow;       // TMA copies per tile
   static constexpr int kSubBytes = kBlockSize * kSubRow;
   static constexpr int kTile = kBlockSize * kRowBytes;        // bytes of one K (or V) tile
-  static constexpr int kStages = INT8 ? 3 : 2;
+  static constexpr int kStages = INT8 ? KVQ_INT8_STAGES : 2;  // pages in flight per warp
   static constexpr int kStageBytes = 2 * kTile;               // K tile then V tile
   static constexpr int kScaleBytes = INT8 ? 2 * kBlockSize * 2 : 0;  // K then V scale rows
   static constexpr uint32_t kTxBytes = 2 * kTile + kScaleBytes;
-  static constexpr int kChunks = kRowBytes / 16;              // 16-byte chunks per row
   static constexpr uint32_t kSwzMask = kSubRow == 128 ? 0x70u : 0x30u;
-  static constexpr int kMinCtas = (INT8 && D == 64) ? 4 : 3;   // 170-register cap otherwise
+  static constexpr int kMinCtas = INT8 ? KVQ_INT8_MIN_CTAS : 3;
 };
 
 // Byte offset inside a (K or V) tile of 16-byte chunk `c` of token row `t`,
@@ -61,43 +72,59 @@ __device__ __forceinline__ uint32_t tile_off(int t, int c) {
   return off ^ ((off >> 3) & C::kSwzMask);
 }
 
-template <int D, bool INT8>
-__host__ __device__ constexpr size_t decode_smem_layout_tiles() {
-  return (size_t)kWarps * TileCfg<D, INT8>::kStages * TileCfg<D, INT8>::kStageBytes;
-}
-
-// Shared-memory carve-up (offsets from a 1024-aligned base).
+// Shared-memory carve-up (byte offsets from a 1024-aligned base).  Per warp:
+// S page stages, one raw query slot (the TMA target, G*D*2 bytes) and a query
+// fragment buffer ([k-step][lane] pairs of the MMA B operand, D*16 bytes;
+// lanes of padded heads hold zeros).
 template <int D, bool INT8>
 struct SmemLayout {
   using C = TileCfg<D, INT8>;
-  static constexpr size_t kTiles = 0;
-  static constexpr size_t kTilesBytes = decode_smem_layout_tiles<D, INT8>();
-  static constexpr size_t kScales = kTiles + kTilesBytes;
-  static constexpr size_t kScalesBytes = (size_t)kWarps * C::kStages * C::kScaleBytes;
-  static constexpr size_t kBars = (kScales + kScalesBytes + 15) & ~(size_t)15;
-  static constexpr size_t kBarsBytes = (size_t)kWarps * C::kStages * 8;
-  static constexpr size_t kStats = kBars + kBarsBytes;           // m, l per warp and head
-  static constexpr size_t kStatsBytes = (size_t)2 * kWarps * kMaxGroup * 4;
-  static constexpr size_t kMisc = kStats + kStatsBytes;          // abort flag + pad
-  static constexpr size_t kBlk = kMisc + 16;                     // int32 [P]
-  // the merge buffer [W][G][D] float reuses the tile region
-  static_assert((size_t)kWarps * kMaxGroup * D * 4 <= kTilesBytes, "merge must fit");
-  __host__ __device__ static size_t prefix_off(int P) { return kBlk + (size_t)P * 4; }
-  __host__ __device__ static size_t total(int B, int P) { return prefix_off(P) + (size_t)B * 4 + 1024; }
+  static constexpr uint32_t kFragBytes = (uint32_t)D * 16;   // (D/16) k-steps x 32 lanes x 8 B
+  size_t tiles, q, qfrag, scales, bars, stage_blk, misc, seq, total_bytes;
+  uint32_t q_bytes;  // one item's query rows: G * D * 2
+  __host__ __device__ SmemLayout(int B, int G) {
+    q_bytes = (uint32_t)(G * D * 2);
+    tiles = 0;
+    q = tiles + (size_t)kWarps * C::kStages * C::kStageBytes;
+    qfrag = q + (size_t)kWarps * q_bytes;
+    scales = qfrag + (size_t)kWarps * kFragBytes;
+    bars = (scales + (size_t)kWarps * C::kStages * C::kScaleBytes + 15) & ~(size_t)15;
+    stage_blk = bars + (size_t)kWarps * C::kStages * 8;
+    misc = stage_blk + (size_t)kWarps * C::kStages * 4;
+    seq = (misc + 16 + 15) & ~(size_t)15;            // prefix[B], lens[B]
+    total_bytes = seq + (size_t)B * 8 + 1024;        // + alignment slack of the base
+  }
 };
 
 template <bool BF16>
-__device__ __forceinline__ void store_out4(void* out, int64_t idx, float a, float b, float c,
-                                           float d) {
-  uint2 v;
-  if constexpr (BF16) {
-    v.x = bf2_as_u32(__floats2bfloat162_rn(a, b));
-    v.y = bf2_as_u32(__floats2bfloat162_rn(c, d));
-  } else {
-    v.x = h2_as_u32(__floats2half2_rn(a, b));
-    v.y = h2_as_u32(__floats2half2_rn(c, d));
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) return bf2_as_u32(__floats2bfloat162_rn(a, b));
+  else return h2_as_u32(__floats2half2_rn(a, b));
+}
+
+// One work item's coordinates.
+struct ItemInfo {
+  int b, j, sp, pg0, npg, nparts, L;
+};
+
+__device__ __forceinline__ ItemInfo item_info(int64_t item, const int* prefix, const int* lens,
+                                              int B, int Hkv, int P) {
+  ItemInfo it;
+  it.sp = (int)(item / Hkv);
+  it.j = (int)(item - (int64_t)it.sp * Hkv);
+  int lo = 0, hi = B - 1;                       // first b with prefix[b] > sp
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] > it.sp) hi = mid; else lo = mid + 1;
   }
-  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) = v;
+  it.b = lo;
+  const int sp0 = lo > 0 ? prefix[lo - 1] : 0;
+  it.nparts = prefix[lo] - sp0;
+  it.L = lens[lo];
+  it.pg0 = (it.sp - sp0) * P;
+  const int pages = (it.L + kBlockSize - 1) / kBlockSize;
+  it.npg = max(0, min(P, pages - it.pg0));
+  return it;
 }
 
 // INT8: QBF16 = activations are bf16 (converted to FP16 for the tensor cores);
@@ -107,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
   using C = TileCfg<D, INT8>;
-  using Lay = SmemLayout<D, INT8>;
+  const SmemLayout<D, INT8> lay(p.B, p.G);
   constexpr bool MMA_BF16 = (!INT8) && QBF16;
   constexpr int S = C::kStages;
   constexpr int KSTEPS = D / 16;       // MMA k-steps over the head dim
@@ -116,15 +143,11 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* tiles = smem + Lay::kTiles;
-  uint16_t* scales = reinterpret_cast<uint16_t*>(smem + Lay::kScales);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
-  float* st_m = reinterpret_cast<float*>(smem + Lay::kStats);
-  float* st_l = st_m + kWarps * kMaxGroup;
-  int* abort_flag = reinterpret_cast<int*>(smem + Lay::kMisc);
-  int* blk_s = reinterpret_cast<int*>(smem + Lay::kBlk);
-  int* prefix = reinterpret_cast<int*>(smem + Lay::prefix_off(p.P));
-  float* merge = reinterpret_cast<float*>(tiles);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
+  int* stage_blk = reinterpret_cast<int*>(smem + lay.stage_blk);
+  int* misc = reinterpret_cast<int*>(smem + lay.misc);
+  int* prefix = reinterpret_cast<int*>(smem + lay.seq);
+  int* lens = prefix + p.B;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -137,368 +160,413 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   if (tid == 0) {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
-    *abort_flag = 0;
   }
   if (tid < kWarps * S) mbar_init(smem_u32(&bars[tid]), 1);
+  // Programmatic dependent launch: let the combine kernel be scheduled as this
+  // grid drains, and wait here until the previous kernel in the stream (e.g.
+  // the quantize-append that wrote the newest tokens) has completed and its
+  // writes are visible, before reading any input.
+  griddep_launch_dependents();
+  griddep_wait();
 
-  // ---- partition prefix over sequences (inclusive), built by every CTA ----
+  // ---- partition prefix over sequences (inclusive) and clamped lengths ----
   {
-    auto parts_of = [&](int b, bool flag) {
-      int L = __ldg(&p.context_lens[b]);
-      if (L < 0 || L > max_tok) {
-        if (flag) atomicOr(p.err, 0x4u);
-        L = L < 0 ? 0 : max_tok;
-      }
-      const int pages = (L + kBlockSize - 1) / kBlockSize;
-      return max(1, (pages + P - 1) / P);
-    };
     const int per = (B + kThreads - 1) / kThreads;   // consecutive sequences per thread
     const int b0 = tid * per, b1 = min(B, b0 + per);
     int sum = 0;
-    for (int b = b0; b < b1; ++b) sum += parts_of(b, true);
+    for (int b = b0; b < b1; ++b) {
+      int L = __ldg(&p.context_lens[b]);
+      if (L < 0 || L > max_tok) {
+        atomicOr(p.err, 0x4u);
+        L = L < 0 ? 0 : max_tok;
+      }
+      lens[b] = L;
+      const int pages = (L + kBlockSize - 1) / kBlockSize;
+      sum += max(1, (pages + P - 1) / P);
+    }
     int incl = sum;                                  // block-wide scan of per-thread sums
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
       if (lane >= o) incl += y;
     }
-    int* wsum = reinterpret_cast<int*>(st_m);
-    if (lane == 31) wsum[warp] = incl;
+    if (lane == 31) misc[warp] = incl;
     __syncthreads();
     int run = incl - sum;
-    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int w = 0; w < warp; ++w) run += misc[w];
     for (int b = b0; b < b1; ++b) {
-      run += parts_of(b, false);
+      const int pages = (lens[b] + kBlockSize - 1) / kBlockSize;
+      run += max(1, (pages + P - 1) / P);
       prefix[b] = run;
     }
   }
   fence_mbar_init();
-  fence_proxy_async_smem();
   __syncthreads();
   if (blockIdx.x == 0 && p.prefix_out != nullptr)
     for (int b = tid; b < B; b += kThreads) p.prefix_out[b] = prefix[b];
 
-  const int total_sp = B > 0 ? prefix[B - 1] : 0;
-  const int64_t n_items = (int64_t)total_sp * Hkv;
-  uint32_t phase = 0;  // bit s = parity of the next wait on stage s of this warp
+  const int64_t n_items = B > 0 ? (int64_t)prefix[B - 1] * Hkv : 0;
+  const int64_t wg = (int64_t)blockIdx.x * kWarps + warp;     // this warp's first item
+  const int64_t nw = (int64_t)gridDim.x * kWarps;             // item stride
 
-  const uint32_t tiles_u32 = smem_u32(tiles);
-  const uint32_t scales_u32 = smem_u32(scales);
+  const uint32_t tiles_u32 = smem_u32(smem + lay.tiles) + warp * S * C::kStageBytes;
+  const uint32_t q_u32 = smem_u32(smem + lay.q) + warp * lay.q_bytes;
+  uint2* qfrag = reinterpret_cast<uint2*>(smem + lay.qfrag + (size_t)warp * lay.kFragBytes);
+  const uint32_t qfrag_lane_u32 = smem_u32(qfrag) + 8 * lane;   // + 256 * ks
+  if (lane >= 4 * G)                                             // padded heads: zero columns
+    for (int ks = 0; ks < KSTEPS; ++ks) qfrag[ks * 32 + lane] = make_uint2(0, 0);
+  const uint32_t scales_u32 = smem_u32(smem + lay.scales) + warp * S * C::kScaleBytes;
+  const uint16_t* scales_w =
+      reinterpret_cast<const uint16_t*>(smem + lay.scales) + warp * S * (C::kScaleBytes / 2);
+  const uint32_t bars_u32 = smem_u32(&bars[warp * S]);
+  int* blk_w = stage_blk + warp * S;
 
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int sp = (int)(item / Hkv);
-    const int j = (int)(item - (int64_t)sp * Hkv);
-    // sequence = first b with prefix[b] > sp
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (prefix[mid] > sp) hi = mid; else lo = mid + 1;
-    }
-    const int b = lo;
-    const int sp0 = b > 0 ? prefix[b - 1] : 0;
-    const int part = sp - sp0;
-    const int nparts = prefix[b] - sp0;
-    int L = __ldg(&p.context_lens[b]);
-    L = L < 0 ? 0 : (L > max_tok ? max_tok : L);
-    const int pages_b = (L + kBlockSize - 1) / kBlockSize;
-    const int pg0 = part * P;
-    const int npg = max(0, min(P, pages_b - pg0));
+  // ---------------------------------------------------------------- issuer
+  // Warp-uniform state; lane 0 performs the copies.  The block ids of the
+  // current 32-page chunk live one per lane (blk_cur); the first chunk of the
+  // following item is prefetched into blk_nxt.
+  int64_t is_item = wg;
+  int is_ord = 0, is_pg = 0, is_chunk = 0;
+  int q_issued = -1, q_consumed = -1;   // ordinals: last item whose query was copied / read
+  ItemInfo is_it{};
+  int blk_cur = -1, blk_nxt = -1;
+  uint32_t n_issued = 0, n_done = 0;
+  int is_slot = 0;                       // stage the next issued page goes to
+  int cs_slot = 0;                       // stage the consumer reads next
+  uint32_t cs_phase = 0;                 // parity of that wait (flips each pass over the ring)
 
-    __syncthreads();                        // merge buffer of the previous item consumed
-    if (*abort_flag) break;
-    for (int t = tid; t < npg; t += kThreads) {
-      int blk = __ldg(&p.block_tables[(int64_t)b * p.max_blocks + pg0 + t]);
+  auto load_chunk = [&](const ItemInfo& it, int base) -> int {
+    const int pg = base + lane;
+    int blk = -1;
+    if (pg < it.npg) {
+      blk = __ldg(&p.block_tables[(int64_t)it.b * p.max_blocks + it.pg0 + pg]);
       if (blk < 0 || blk >= p.num_blocks) {
         atomicOr(p.err, 0x2u);
         blk = -1;
       }
-      blk_s[t] = blk;
     }
-    fence_proxy_async_smem();
-    __syncthreads();
+    return blk;
+  };
+  auto next_item_chunk = [&](int64_t item) -> int {
+    if (item >= n_items) return -1;
+    return load_chunk(item_info(item, prefix, lens, B, Hkv, P), 0);
+  };
+  if (is_item < n_items) {
+    is_it = item_info(is_item, prefix, lens, B, Hkv, P);
+    blk_cur = load_chunk(is_it, 0);
+    blk_nxt = next_item_chunk(is_item + nw);
+  }
 
-    // ---- per-warp page stream ----
-    const int nk = npg > warp ? (npg - warp + kWarps - 1) / kWarps : 0;
-    const int row_base = j * kBlockSize;   // + blk * Hkv * 16
-    auto issue = [&](int k) {              // lane 0 only
-      const int s = k % S;
-      const int lp = warp + k * kWarps;
-      const int blk = blk_s[lp];
-      const uint32_t bar = smem_u32(&bars[warp * S + s]);
-      if (blk < 0) {
-        mbar_arrive(bar);
-        return;
-      }
-      mbar_arrive_expect_tx(bar, C::kTxBytes);
-      const uint32_t kdst = tiles_u32 + (uint32_t)((warp * S + s) * C::kStageBytes);
-      const uint32_t vdst = kdst + C::kTile;
-      const int y = blk * Hkv * kBlockSize + row_base;
-#pragma unroll
-      for (int st = 0; st < C::kSubTiles; ++st) {
-        tma_load_2d(kdst + st * C::kSubBytes, &tmK, st * (C::kSubRow / C::kElem), y, bar);
-        tma_load_2d(vdst + st * C::kSubBytes, &tmV, st * (C::kSubRow / C::kElem), y, bar);
-      }
-      if constexpr (INT8) {
-        const int64_t srow = ((int64_t)blk * Hkv + j) * kBlockSize;
-        const uint32_t sdst = scales_u32 + (uint32_t)((warp * S + s) * C::kScaleBytes);
-        bulk_load(sdst, p.k_scale + srow, kBlockSize * 2, bar);
-        bulk_load(sdst + kBlockSize * 2, p.v_scale + srow, kBlockSize * 2, bar);
-      }
-    };
-    if (lane == 0)
-      for (int k = 0; k < min(S, nk); ++k) issue(k);
-
-    // ---- query fragments (rows g < G of the padded 16-row A operand) ----
-    uint32_t qa0[KSTEPS], qa2[KSTEPS];
-    {
-      const bool has = g < G && nk > 0;
-      const uint16_t* qrow =
-          static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Hq + (int64_t)j * G + g) * D;
-#pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        if constexpr (INT8) {
-          // logical k {2c,2c+1,2c+8,2c+9} of step ks <-> head-dim 16ks+4c+{0..3}
-          uint2 v = has ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c))
-                        : make_uint2(0, 0);
-          if constexpr (QBF16) {
-            qa0[ks] = h2_as_u32(__floats2half2_rn(__uint_as_float(v.x << 16),
-                                                  __uint_as_float(v.x & 0xFFFF0000u)));
-            qa2[ks] = h2_as_u32(__floats2half2_rn(__uint_as_float(v.y << 16),
-                                                  __uint_as_float(v.y & 0xFFFF0000u)));
-          } else {
-            qa0[ks] = v.x;
-            qa2[ks] = v.y;
-          }
-        } else {
-          // natural order: k {2c,2c+1} <-> 16ks+2c, k {2c+8,2c+9} <-> 16ks+8+2c
-          qa0[ks] = has ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c)) : 0u;
-          qa2[ks] = has ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * c))
-                        : 0u;
+  // Issue pages while fewer than S are in flight; an item's first page (which
+  // also copies the item's query rows into the single raw query slot) waits
+  // until the previously copied query rows have been read by the consumer.
+  auto refill = [&]() {
+    while (n_issued - n_done < (uint32_t)S) {
+      while (is_item < n_items && is_pg >= is_it.npg) {   // next item with pages
+        is_item += nw;
+        ++is_ord;
+        is_pg = 0;
+        is_chunk = 0;
+        if (is_item < n_items) {
+          is_it = item_info(is_item, prefix, lens, B, Hkv, P);
+          blk_cur = blk_nxt;
+          blk_nxt = next_item_chunk(is_item + nw);
         }
       }
+      if (is_item >= n_items || (is_pg == 0 && q_issued > q_consumed)) return;
+      if (is_pg >= is_chunk + 32) {
+        is_chunk += 32;
+        blk_cur = load_chunk(is_it, is_chunk);
+      }
+      const int blk = __shfl_sync(0xFFFFFFFFu, blk_cur, is_pg - is_chunk);
+      const int s = is_slot;
+      is_slot = is_slot + 1 == S ? 0 : is_slot + 1;
+      if (lane == 0) {
+        const uint32_t bar = bars_u32 + 8 * s;
+        blk_w[s] = blk;
+        const uint32_t qbytes = is_pg == 0 ? lay.q_bytes : 0u;
+        if (blk < 0) {
+          if (qbytes) {
+            mbar_arrive_expect_tx(bar, qbytes);
+          } else {
+            mbar_arrive(bar);
+          }
+        } else {
+          mbar_arrive_expect_tx(bar, C::kTxBytes + qbytes);
+          const uint32_t kdst = tiles_u32 + s * C::kStageBytes;
+          const int y = (blk * Hkv + is_it.j) * kBlockSize;
+#pragma unroll
+          for (int st = 0; st < C::kSubTiles; ++st) {
+            tma_load_2d(kdst + st * C::kSubBytes, &tmK, st * (C::kSubRow / C::kElem), y, bar);
+            tma_load_2d(kdst + C::kTile + st * C::kSubBytes, &tmV,
+                        st * (C::kSubRow / C::kElem), y, bar);
+          }
+          if constexpr (INT8) {
+            const int64_t srow = ((int64_t)blk * Hkv + is_it.j) * kBlockSize;
+            const uint32_t sdst = scales_u32 + s * C::kScaleBytes;
+            bulk_load(sdst, p.k_scale + srow, kBlockSize * 2, bar);
+            bulk_load(sdst + kBlockSize * 2, p.v_scale + srow, kBlockSize * 2, bar);
+          }
+        }
+        if (qbytes) {
+          const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) +
+                                 ((int64_t)is_it.b * p.Hq + (int64_t)is_it.j * G) * D;
+          bulk_load(q_u32, qsrc, qbytes, bar);
+        }
+      }
+      if (is_pg == 0) q_issued = is_ord;
+      ++n_issued;
+      ++is_pg;
     }
+  };
+  refill();
 
-    float m_run = -INFINITY, l_run = 0.f;
+  // -------------------------------------------------------------- consumer
+  int ord = 0;
+  bool aborted = false;
+  for (int64_t item = wg; item < n_items && !aborted; item += nw, ++ord) {
+    const ItemInfo it = item_info(item, prefix, lens, B, Hkv, P);
+    // Running softmax state of the two query heads this thread's columns hold
+    // (heads 2c and 2c+1 of the KV head's group), and the output accumulator
+    // O^T[d][head]: o[4cb + e] for 16-wide head-dim block cb, e = (row, col)
+    // of the MMA quad: e0 (row g, col 2c), e1 (g, 2c+1), e2 (g+8, 2c),
+    // e3 (g+8, 2c+1).
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[NOUT];
 #pragma unroll
     for (int i = 0; i < NOUT; ++i) o[i] = 0.f;
+    const bool has_head = g < G;   // this lane provides a real query column
 
-    bool timed_out = false;
-    int k = 0;
-    for (; k < nk; ++k) {
-      const int s = k % S;
-      const uint32_t bar = smem_u32(&bars[warp * S + s]);
-      const uint32_t par = (phase >> s) & 1u;
-      if (!mbar_wait_bounded(bar, par)) {
-        timed_out = true;
+    for (int pg = 0; pg < it.npg; ++pg) {
+      const int s = cs_slot;
+      const uint32_t par = cs_phase;
+      if (++cs_slot == S) {
+        cs_slot = 0;
+        cs_phase ^= 1u;
+      }
+      if (!mbar_wait_bounded(bars_u32 + 8 * s, par)) {
+        aborted = true;
         break;
       }
-      phase ^= 1u << s;
-      const int lp = warp + k * kWarps;
-      const int blk = blk_s[lp];
-      if (blk >= 0) {
-        const uint32_t kt = tiles_u32 + (uint32_t)((warp * S + s) * C::kStageBytes);
-        const uint32_t vt = kt + C::kTile;
-        const int tok0 = (pg0 + lp) * kBlockSize;
-        const int nvalid = min(kBlockSize, L - tok0);
-
-        // ---------------- S = Q K^T (16 padded heads x 16 tokens) ----------------
-        float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        if constexpr (INT8) {
-#pragma unroll
-          for (int kk = 0; kk < KSTEPS / 2; ++kk) {
-            // matrices: tokens 0-7 / 8-15 of chunk 2kk, then of chunk 2kk+1
-            const int t = (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int ch = 2 * kk + (lane >> 4);
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(kt + tile_off<C>(t, ch), r0, r1, r2, r3);
-            uint32_t b0, b1;
-            i8x4_to_h2x2<0x4140u, 0x4342u>(r0, b0, b1);
-            mma_16816<false>(sc[0][0], sc[0][1], qa0[2 * kk], qa2[2 * kk], b0, b1);
-            i8x4_to_h2x2<0x4140u, 0x4342u>(r1, b0, b1);
-            mma_16816<false>(sc[1][0], sc[1][1], qa0[2 * kk], qa2[2 * kk], b0, b1);
-            i8x4_to_h2x2<0x4140u, 0x4342u>(r2, b0, b1);
-            mma_16816<false>(sc[0][0], sc[0][1], qa0[2 * kk + 1], qa2[2 * kk + 1], b0, b1);
-            i8x4_to_h2x2<0x4140u, 0x4342u>(r3, b0, b1);
-            mma_16816<false>(sc[1][0], sc[1][1], qa0[2 * kk + 1], qa2[2 * kk + 1], b0, b1);
-          }
-        } else {
+      if (pg == 0) {
+        // query fragments (the MMA B operand, column g = head g < G), from the
+        // raw rows to this lane's slots of the fragment buffer
+        if (has_head) {
+          const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + lay.q) +
+                               (size_t)warp * (lay.q_bytes / 2) + g * D;
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
-            // matrices: tokens 0-7 chunk 2ks, 0-7 chunk 2ks+1, 8-15 chunk 2ks, 8-15 chunk 2ks+1
-            const int t = (lane & 7) + (lane >> 4) * 8;
-            const int ch = 2 * ks + ((lane >> 3) & 1);
+            uint2 f;
+            if constexpr (INT8) {
+              // logical k {2c,2c+1,2c+8,2c+9} of step ks <-> head-dim 16ks+4c+{0..3}
+              const uint2 v = *reinterpret_cast<const uint2*>(qs + 16 * ks + 4 * c);
+              if constexpr (QBF16) {
+                f.x = h2_as_u32(__floats2half2_rn(__uint_as_float(v.x << 16),
+                                                  __uint_as_float(v.x & 0xFFFF0000u)));
+                f.y = h2_as_u32(__floats2half2_rn(__uint_as_float(v.y << 16),
+                                                  __uint_as_float(v.y & 0xFFFF0000u)));
+              } else {
+                f = v;
+              }
+            } else {
+              // natural order: k {2c,2c+1} <-> 16ks+2c, k {2c+8,2c+9} <-> 16ks+8+2c
+              f.x = *reinterpret_cast<const uint32_t*>(qs + 16 * ks + 2 * c);
+              f.y = *reinterpret_cast<const uint32_t*>(qs + 16 * ks + 8 + 2 * c);
+            }
+            qfrag[ks * 32 + lane] = f;
+          }
+        }
+        q_consumed = ord;
+      }
+      const int blk = blk_w[s];
+      if (blk >= 0) {
+        const uint32_t kt = tiles_u32 + s * C::kStageBytes;
+        const uint32_t vt = kt + C::kTile;
+        const int nvalid = min(kBlockSize, it.L - (it.pg0 + pg) * kBlockSize);
+        // ldmatrix row address: matrices (tokens 0-7, chunk 2i), (8-15, 2i),
+        // (0-7, 2i+1), (8-15, 2i+1) for lanes 0-7, 8-15, 16-23, 24-31
+        const int lt = (lane & 7) + ((lane >> 3) & 1) * 8;
+
+        // ---------- S[token][head] = K Q^T: M = 16 tokens, N = 8 heads ----------
+        // two accumulators (even/odd k-steps) halve the dependent MMA chain
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < (INT8 ? KSTEPS / 2 : 0); ++kk) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kt + tile_off<C>(lt, 2 * kk + (lane >> 4)), r0, r1, r2, r3);
+          const uint2 qa = lds_u2(qfrag_lane_u32 + 256 * (2 * kk));
+          const uint2 qb = lds_u2(qfrag_lane_u32 + 256 * (2 * kk + 1));
+          if constexpr (INT8) {
+            // r0/r1: tokens g / g+8, head-dim 16(2kk)+4c+{0..3}; r2/r3: next chunk
+            uint32_t a0, a2, a1, a3;
+            i8x4_to_h2x2<0x4140u, 0x4342u>(r0, a0, a2);
+            i8x4_to_h2x2<0x4140u, 0x4342u>(r1, a1, a3);
+            mma_16816_acc<false>(sa, a0, a1, a2, a3, qa.x, qa.y);
+            i8x4_to_h2x2<0x4140u, 0x4342u>(r2, a0, a2);
+            i8x4_to_h2x2<0x4140u, 0x4342u>(r3, a1, a3);
+            mma_16816_acc<false>(sb, a0, a1, a2, a3, qb.x, qb.y);
+          }
+        }
+        if constexpr (!INT8) {
+          // 16-bit tiles: one 16-byte chunk holds 8 elements, so k-step ks spans
+          // chunks 2ks and 2ks+1 and (r0, r1, r2, r3) is directly its A operand
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
             uint32_t r0, r1, r2, r3;
-            ldsm_x4(kt + tile_off<C>(t, ch), r0, r1, r2, r3);
-            mma_16816<MMA_BF16>(sc[0][0], sc[0][1], qa0[ks], qa2[ks], r0, r1);
-            mma_16816<MMA_BF16>(sc[1][0], sc[1][1], qa0[ks], qa2[ks], r2, r3);
+            ldsm_x4(kt + tile_off<C>(lt, 2 * ks + (lane >> 4)), r0, r1, r2, r3);
+            const uint2 qa = lds_u2(qfrag_lane_u32 + 256 * ks);
+            // a0: token g, d 16ks+2c..; a1: token g+8; a2: token g, d 16ks+8+2c..; a3: g+8
+            if (ks & 1) mma_16816_acc<MMA_BF16>(sb, r0, r1, r2, r3, qa.x, qa.y);
+            else mma_16816_acc<MMA_BF16>(sa, r0, r1, r2, r3, qa.x, qa.y);
           }
         }
 
-        // scores in log2 units; thread holds head g, tokens 8nb + 2c + e
-        float z[2][2];
+        // scores in log2 units: z0 (token g, head 2c), z1 (g, 2c+1), z2 (g+8, 2c), z3
+        float ksg = p.scale_log2, ksg8 = p.scale_log2;
         if constexpr (INT8) {
-          const uint16_t* ksc = scales + (warp * S + s) * (C::kScaleBytes / 2);
-          const float2 k01 = __half22float2(
-              u32_as_h2(reinterpret_cast<const uint32_t*>(ksc)[c]));
-          const float2 k89 = __half22float2(
-              u32_as_h2(reinterpret_cast<const uint32_t*>(ksc)[4 + c]));
-          z[0][0] = sc[0][0] * (k01.x * p.scale_log2);
-          z[0][1] = sc[0][1] * (k01.y * p.scale_log2);
-          z[1][0] = sc[1][0] * (k89.x * p.scale_log2);
-          z[1][1] = sc[1][1] * (k89.y * p.scale_log2);
-        } else {
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) z[nb][e] = sc[nb][e] * p.scale_log2;
+          const uint16_t* ksc = scales_w + s * (C::kScaleBytes / 2);
+          ksg *= __half2float(__ushort_as_half(ksc[g]));
+          ksg8 *= __half2float(__ushort_as_half(ksc[g + 8]));
         }
+        float z0 = (sa[0] + sb[0]) * ksg, z1 = (sa[1] + sb[1]) * ksg;
+        float z2 = (sa[2] + sb[2]) * ksg8, z3 = (sa[3] + sb[3]) * ksg8;
         if (nvalid < kBlockSize) {
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-              if (8 * nb + 2 * c + e >= nvalid) z[nb][e] = -INFINITY;
+          if (g >= nvalid) z0 = z1 = -INFINITY;
+          if (g + 8 >= nvalid) z2 = z3 = -INFINITY;
         }
 
-        // ---------------- online softmax (per head g, over the 4 c-lanes) --------
-        float mx = fmaxf(fmaxf(z[0][0], z[0][1]), fmaxf(z[1][0], z[1][1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = fast_exp2(m_run - m_new);
-        float pr[2][2];
+        // ---------- online softmax per head column (reduce over the 8 g-lanes) ----------
+        float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+        const float p0 = fast_exp2(z0 - mn0), p1 = fast_exp2(z1 - mn1);
+        const float p2 = fast_exp2(z2 - mn0), p3 = fast_exp2(z3 - mn1);
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(0xFFFFFFFFu, (al0 != 1.f) || (al1 != 1.f))) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) pr[nb][e] = fast_exp2(z[nb][e] - m_new);
-        l_run = l_run * alpha + ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
-        m_run = m_new;
-        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-#pragma unroll
-          for (int i = 0; i < NOUT; ++i) o[i] *= alpha;
+          for (int cb = 0; cb < D / 16; ++cb) {
+            o[4 * cb + 0] *= al0;
+            o[4 * cb + 1] *= al1;
+            o[4 * cb + 2] *= al0;
+            o[4 * cb + 3] *= al1;
+          }
         }
 
-        // ---------------- O += P V ----------------
+        // P^T as the B operand: b0 = P[tokens 2c, 2c+1][head g], b1 = tokens 2c+8, 2c+9
+        const uint32_t pb0 = movmatrix_trans(pack2<MMA_BF16>(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(pack2<MMA_BF16>(p2, p3));
+
+        // ---------- O^T[d][head] += V^T P^T: M = 16 head-dims, N = 8 heads ----------
         if constexpr (INT8) {
-          const uint32_t pa0 = h2_as_u32(__floats2half2_rn(pr[0][0], pr[0][1]));
-          const uint32_t pa2 = h2_as_u32(__floats2half2_rn(pr[1][0], pr[1][1]));
-          const uint16_t* vsc = scales + (warp * S + s) * (C::kScaleBytes / 2) + kBlockSize;
+          const uint16_t* vsc = scales_w + s * (C::kScaleBytes / 2) + kBlockSize;
           const __half2 vs01 = u32_as_h2(reinterpret_cast<const uint32_t*>(vsc)[c]);
           const __half2 vs89 = u32_as_h2(reinterpret_cast<const uint32_t*>(vsc)[4 + c]);
 #pragma unroll
           for (int kk = 0; kk < KSTEPS / 2; ++kk) {
-            const int t = (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int ch = 2 * kk + (lane >> 4);
             uint32_t r[4];
-            ldsm_x4_trans(vt + tile_off<C>(t, ch), r[0], r[1], r[2], r[3]);
+            ldsm_x4_trans(vt + tile_off<C>(lt, 2 * kk + (lane >> 4)), r[0], r[1], r[2], r[3]);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              // r[2h]: tokens 2c,2c+1 (b0);  r[2h+1]: tokens 2c+8,2c+9 (b1);
-              // bytes {t0 d0, t0 d1, t1 d0, t1 d1} with d0 = 16ch + 2g (even).
-              uint32_t e0, od0, e1, od1;
-              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h], e0, od0);
-              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h + 1], e1, od1);
-              e0 = h2_as_u32(__hmul2(u32_as_h2(e0), vs01));
+              // r[2h]: tokens 2c, 2c+1; r[2h+1]: tokens 2c+8, 2c+9; bytes
+              // {t0 d0, t0 d1, t1 d0, t1 d1} with d0 = 16cb + 2g (row g), d1 = d0 + 1 (row g+8)
+              uint32_t ev0, od0, ev1, od1;
+              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h], ev0, od0);
+              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h + 1], ev1, od1);
+              ev0 = h2_as_u32(__hmul2(u32_as_h2(ev0), vs01));
               od0 = h2_as_u32(__hmul2(u32_as_h2(od0), vs01));
-              e1 = h2_as_u32(__hmul2(u32_as_h2(e1), vs89));
+              ev1 = h2_as_u32(__hmul2(u32_as_h2(ev1), vs89));
               od1 = h2_as_u32(__hmul2(u32_as_h2(od1), vs89));
               const int cb = 2 * kk + h;
-              // even-d tile: d = 16cb + 4c + {0, 2};  odd-d tile: d = 16cb + 4c + {1, 3}
-              mma_16816<false>(o[4 * cb + 0], o[4 * cb + 2], pa0, pa2, e0, e1);
-              mma_16816<false>(o[4 * cb + 1], o[4 * cb + 3], pa0, pa2, od0, od1);
+              float* oq = o + 4 * cb;
+              mma_16816_acc<false>(*reinterpret_cast<float(*)[4]>(oq), ev0, od0, ev1, od1, pb0, pb1);
             }
           }
         } else {
-          uint32_t pa0, pa2;
-          if constexpr (MMA_BF16) {
-            pa0 = bf2_as_u32(__floats2bfloat162_rn(pr[0][0], pr[0][1]));
-            pa2 = bf2_as_u32(__floats2bfloat162_rn(pr[1][0], pr[1][1]));
-          } else {
-            pa0 = h2_as_u32(__floats2half2_rn(pr[0][0], pr[0][1]));
-            pa2 = h2_as_u32(__floats2half2_rn(pr[1][0], pr[1][1]));
-          }
+          // matrices: (tokens 0-7, chunk 2pp), (0-7, 2pp+1), (8-15, 2pp), (8-15, 2pp+1)
+          const int vtk = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
           for (int pp = 0; pp < D / 16; ++pp) {
-            // matrices: tokens 0-7 / 8-15 of chunk 2pp, then of chunk 2pp+1
-            const int t = (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int ch = 2 * pp + (lane >> 4);
             uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(vt + tile_off<C>(t, ch), r0, r1, r2, r3);
-            // n-tile 2pp: d = 16pp + 2c + {0,1};  n-tile 2pp+1: d = 16pp + 8 + 2c + {0,1}
-            mma_16816<MMA_BF16>(o[4 * pp + 0], o[4 * pp + 1], pa0, pa2, r0, r1);
-            mma_16816<MMA_BF16>(o[4 * pp + 2], o[4 * pp + 3], pa0, pa2, r2, r3);
+            ldsm_x4_trans(vt + tile_off<C>(vtk, 2 * pp + ((lane >> 3) & 1)), r0, r1, r2, r3);
+            // rows g: d = 16pp + g; rows g+8: d = 16pp + 8 + g
+            float* oq = o + 4 * pp;
+            mma_16816_acc<MMA_BF16>(*reinterpret_cast<float(*)[4]>(oq), r0, r1, r2, r3, pb0, pb1);
           }
         }
       }
+      ++n_done;
       __syncwarp();
-      if (lane == 0 && k + S < nk) issue(k + S);
+      refill();
     }
-    if (timed_out) {
-      // give up on this item: record, drain this warp's copies still in flight
-      if (lane == 0) {
-        atomicOr(p.err, 0x8u);
-        atomicExch(abort_flag, 1);
-      }
-      for (int k2 = k; k2 < min(nk, k + S); ++k2) {
-        const int s2 = k2 % S;
-        mbar_wait_bounded(smem_u32(&bars[warp * S + s2]), (phase >> s2) & 1u);
-        phase ^= 1u << s2;
-      }
-    }
+    if (aborted) break;
 
-    // ---- merge the warps' (m, l, O) and write ----
-    l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
-    l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 2);
-    __syncthreads();                         // every warp is done with its stages
-    if (c == 0 && g < kMaxGroup) {
-      st_m[warp * kMaxGroup + g] = m_run;
-      st_l[warp * kMaxGroup + g] = l_run;
+    // ---- finalize the item: this warp holds the whole partition ----
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
+      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
     }
-    if (g < G) {
-      float* mrow = merge + ((size_t)warp * kMaxGroup + g) * D;
-      if constexpr (INT8) {
 #pragma unroll
-        for (int cb = 0; cb < D / 16; ++cb)
-          *reinterpret_cast<float4*>(mrow + 16 * cb + 4 * c) =
-              make_float4(o[4 * cb], o[4 * cb + 1], o[4 * cb + 2], o[4 * cb + 3]);
-      } else {
+    for (int hh = 0; hh < 2; ++hh) {
+      const int head = 2 * c + hh;              // this thread's column
+      if (head >= G) continue;
+      const float l = hh ? l1 : l0;
+      const float m = hh ? m1 : m0;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int64_t hrow = (int64_t)it.b * p.Hq + (int64_t)it.j * G + head;
+      if (it.nparts == 1) {
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + hrow * D;
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt)
-          *reinterpret_cast<float2*>(mrow + 8 * nt + 2 * c) = make_float2(o[2 * nt], o[2 * nt + 1]);
-      }
-    }
-    __syncthreads();
-    const int64_t hbase = (int64_t)b * p.Hq + (int64_t)j * G;
-    for (int idx = tid; idx < G * (D / 4); idx += kThreads) {
-      const int gg = idx / (D / 4);
-      const int d = (idx - gg * (D / 4)) * 4;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, st_m[w * kMaxGroup + gg]);
-      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f, lsum = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float f = fast_exp2(st_m[w * kMaxGroup + gg] - M);
-          lsum += f * st_l[w * kMaxGroup + gg];
-          const float4 v =
-              *reinterpret_cast<const float4*>(merge + ((size_t)w * kMaxGroup + gg) * D + d);
-          acc0 += f * v.x; acc1 += f * v.y; acc2 += f * v.z; acc3 += f * v.w;
+        for (int cb = 0; cb < D / 16; ++cb) {
+          const float v0 = o[4 * cb + hh] * inv, v1 = o[4 * cb + 2 + hh] * inv;
+          if constexpr (INT8) {  // rows g, g+8 <-> d = 16cb + 2g, 16cb + 2g + 1
+            *reinterpret_cast<uint32_t*>(dst + 16 * cb + 2 * g) = pack2<QBF16>(v0, v1);
+          } else {               // rows g, g+8 <-> d = 16cb + g, 16cb + 8 + g
+            const uint32_t pk = pack2<QBF16>(v0, v1);
+            dst[16 * cb + g] = (uint16_t)(pk & 0xFFFFu);
+            dst[16 * cb + 8 + g] = (uint16_t)(pk >> 16);
+          }
         }
-      }
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      if (nparts == 1) {
-        store_out4<QBF16>(p.out, (hbase + gg) * D + d, acc0 * inv, acc1 * inv, acc2 * inv,
-                          acc3 * inv);
       } else {
-        const int64_t prow = ((int64_t)sp * Hkv + j) * G + gg;
-        *reinterpret_cast<float4*>(p.part_o + prow * D + d) =
-            make_float4(acc0 * inv, acc1 * inv, acc2 * inv, acc3 * inv);
-        if (d == 0) p.part_lse[prow] = lsum > 0.f ? M + __log2f(lsum) : -INFINITY;
+        const int64_t prow = ((int64_t)it.sp * Hkv + it.j) * G + head;
+        float* dst = p.part_o + prow * D;
+#pragma unroll
+        for (int cb = 0; cb < D / 16; ++cb) {
+          const float v0 = o[4 * cb + hh] * inv, v1 = o[4 * cb + 2 + hh] * inv;
+          if constexpr (INT8) {
+            *reinterpret_cast<float2*>(dst + 16 * cb + 2 * g) = make_float2(v0, v1);
+          } else {
+            dst[16 * cb + g] = v0;
+            dst[16 * cb + 8 + g] = v1;
+          }
+        }
+        if (g == 0) p.part_lse[prow] = l > 0.f ? m + __log2f(l) : -INFINITY;
       }
     }
-    fence_proxy_async_smem();                // merge writes precede the next TMA fills
+  }
+
+  if (aborted) {
+    // A wait gave up: record it, then wait (bounded) for this warp's copies
+    // still in flight so that none lands after the CTA has exited.
+    if (lane == 0) atomicOr(p.err, 0x8u);
+    // the failed wait's stage is the one before cs_slot (cs_slot/cs_phase advanced)
+    int s = cs_slot == 0 ? S - 1 : cs_slot - 1;
+    uint32_t ph = cs_slot == 0 ? (cs_phase ^ 1u) : cs_phase;
+    for (; n_done < n_issued; ++n_done) {
+      mbar_wait_bounded(bars_u32 + 8 * s, ph);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
   }
 }
 

@@ -15,8 +15,9 @@ const void* pick(int D, bool bf16) {
 }
 }  // namespace
 
-size_t decode_smem_bytes_kv16(int D, int B, int P) {
-  return D == 128 ? SmemLayout<128, false>::total(B, P) : SmemLayout<64, false>::total(B, P);
+size_t decode_smem_bytes_kv16(int D, int B, int G) {
+  return D == 128 ? SmemLayout<128, false>(B, G).total_bytes
+                  : SmemLayout<64, false>(B, G).total_bytes;
 }
 
 cudaError_t decode_configure_kv16(int D, bool bf16, size_t smem) {
@@ -30,14 +31,25 @@ cudaError_t decode_occupancy_kv16(int D, bool bf16, size_t smem, int* n) {
 
 cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                const DecodeParams& p, int grid, size_t smem, cudaStream_t s) {
+  // programmatic stream serialization: the launch may overlap the tail of the
+  // previous kernel in the stream; the kernel waits (griddepcontrol) before
+  // reading any input
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (D == 128) {
-    if (bf16) paged_decode_kernel<128, false, true><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
-    else paged_decode_kernel<128, false, false><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
-  } else {
-    if (bf16) paged_decode_kernel<64, false, true><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
-    else paged_decode_kernel<64, false, false><<<grid, kThreads, smem, s>>>(*tmk, *tmv, p);
+    return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, false, true>, *tmk, *tmv, p)
+                : cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, false, false>, *tmk, *tmv, p);
   }
-  return cudaGetLastError();
+  return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, false, true>, *tmk, *tmv, p)
+              : cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, false, false>, *tmk, *tmv, p);
 }
 
 }  // namespace kvq

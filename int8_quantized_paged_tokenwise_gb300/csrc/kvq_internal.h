@@ -45,7 +45,7 @@ struct DecodeParams {
   int32_t max_blocks;       // block-table row length
   int32_t max_ctx;          // host upper bound on context_lens
   int32_t num_blocks;
-  int32_t P;                // pages per partition (multiple of kWarps)
+  int32_t P;                // pages per partition (one warp's work item)
   float scale_log2;         // sm_scale * log2(e)
 };
 
@@ -58,12 +58,12 @@ struct CombineParams {
 };
 
 // decode (kvq_decode_int8.cu / kvq_decode_kv16.cu); D = head_dim, smem in bytes.
-size_t decode_smem_bytes_int8(int D, int B, int P);
+size_t decode_smem_bytes_int8(int D, int B, int G);
 cudaError_t decode_configure_int8(int D, bool bf16, size_t smem);
 cudaError_t decode_occupancy_int8(int D, bool bf16, size_t smem, int* n);
 cudaError_t decode_launch_int8(int D, bool bf16, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
-size_t decode_smem_bytes_kv16(int D, int B, int P);
+size_t decode_smem_bytes_kv16(int D, int B, int G);
 cudaError_t decode_configure_kv16(int D, bool bf16, size_t smem);
 cudaError_t decode_occupancy_kv16(int D, bool bf16, size_t smem, int* n);
 cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* tmk, const CUtensorMap* tmv,

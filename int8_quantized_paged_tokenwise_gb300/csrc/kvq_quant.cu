@@ -78,6 +78,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Qu
   const int64_t row = gthread / LPR;
   const int sub = lane % LPR;
   const bool in_range = row < p.num_rows;
+  // the next kernel in the stream (a decode launched with programmatic stream
+  // serialization) may be scheduled now; it waits for this grid's completion
+  griddep_launch_dependents();
 
   int64_t t = 0, slot = -1;
   int j = 0;

@@ -244,7 +244,7 @@ def test_decode_host_validation():
                                     P(vc.data_ptr()), P(ks.data_ptr()), P(vs.data_ptr()), case.nb,
                                     16, P(case.bt.data_ptr()), case.bt.shape[1],
                                     P(case.cl.data_ptr()), 100, 0.125, P(out.data_ptr()), None, 0,
-                                    6, None) == 1     # not a multiple of 4
+                                    0, None) == 1     # no partition size
     torch.cuda.synchronize()
     assert kvq.kvq_get_error() == (0, 0)
 
