@@ -139,9 +139,10 @@ kvq_status kvq_quantize_append(const void* k, const void* v, int64_t k_token_str
  *   workspace       device scratch of >= kvq_decode_workspace_bytes(...)
  *                   bytes (may be NULL when that is 0), 256-byte aligned, not
  *                   shared by calls that overlap on the GPU.
- * The launcher picks the partition size (pages per CTA work item) from
- * num_seqs, num_kv_heads, max_context_len and the SM count; sequences longer
- * than one partition go through split-K partials and a combine kernel.
+ * Work is split into items of (sequence, KV head, partition of P pages); the
+ * kernel chooses P from the exact context lengths (kvq_decode_partition_pages
+ * describes how); sequences longer than one partition go through split-K
+ * partials and a combine kernel.
  */
 kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -154,14 +155,19 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
                             size_t workspace_bytes, kvq_stream_t stream);
 
 /* Scratch bytes kvq_paged_decode needs for these sizes on the current device
- * (0 when no sequence can be split). */
+ * (0 when no sequence can be split).  Passing more lets the kernel choose
+ * finer partitions (see below). */
 size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len);
 
-/* The partition size (pages per work item; one warp processes one item) the
- * launcher picks on the current device; 0 on invalid input. */
-int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_kv_heads,
-                                   int32_t max_context_len);
+/* The partition size (pages per work item; one warp processes one item) that
+ * kvq_decode_workspace_bytes sizes the workspace for on the current device;
+ * 0 on invalid input.  kvq_paged_decode itself lets the kernel pick the
+ * partition size from the exact context lengths: among a fixed set of
+ * candidate sizes whose partition count fits the given workspace, the one
+ * that best balances the work items over the resident warps. */
+int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t max_context_len);
 
 /* kvq_paged_decode with the partition size forced (pages per work item, >= 1);
  * used to test every launcher variant.  Workspace from

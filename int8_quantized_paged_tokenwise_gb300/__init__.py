@@ -91,7 +91,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.kvq_decode_workspace_bytes.restype = sz
     L.kvq_decode_workspace_bytes_split.argtypes = [i32, i32, i32, i32, i32, i32]
     L.kvq_decode_workspace_bytes_split.restype = sz
-    L.kvq_decode_partition_pages.argtypes = [i32, i32, i32]
+    L.kvq_decode_partition_pages.argtypes = [i32, i32, i32, i32, i32]
     L.kvq_decode_partition_pages.restype = i32
     L.kvq_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.kvq_get_error.restype = ctypes.c_int
@@ -214,8 +214,10 @@ def kvq_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, ma
                                             max_context_len))
 
 
-def kvq_decode_partition_pages(num_seqs, num_kv_heads, max_context_len) -> int:
-    return int(load().kvq_decode_partition_pages(num_seqs, num_kv_heads, max_context_len))
+def kvq_decode_partition_pages(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               max_context_len) -> int:
+    return int(load().kvq_decode_partition_pages(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 max_context_len))
 
 
 def _check_decode(q, k_cache, v_cache, block_tables, context_lens, out, cache_dtypes):

@@ -108,25 +108,60 @@ int32_t auto_partition_pages(int32_t B, int32_t Hkv, int32_t max_ctx, int sms) {
 
 struct WsLayout {
   size_t prefix = 0, lse = 0, o = 0, total = 0;
-  bool split = false;
+  int64_t sp_cap = 0;   // sequence-partitions the partial buffers hold
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WsLayout workspace_layout(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_ctx,
-                          int32_t P) {
+// Workspace: inclusive partition prefix int32 [B], then per sequence-partition
+// the log2-sum-exp float [sp][Hkv][G] and the normalized partial output
+// float [sp][Hkv][G][D].
+WsLayout layout_for_cap(int32_t B, int32_t Hkv, int32_t G, int32_t D, int64_t sp_cap) {
   WsLayout w;
-  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
-  const int64_t parts_max = pages_max > 0 ? cdiv(pages_max, P) : 1;
-  if (parts_max <= 1 || B == 0) return w;
-  const int64_t sp_max = (int64_t)B * parts_max;
-  const int64_t G = Hq / Hkv;
-  w.split = true;
+  w.sp_cap = sp_cap;
   w.prefix = 0;
   w.lse = round_up((size_t)B * 4, 256);
-  w.o = w.lse + round_up((size_t)(sp_max * Hkv * G) * 4, 256);
-  w.total = w.o + (size_t)(sp_max * Hkv * G * D) * 4;
+  w.o = w.lse + round_up((size_t)(sp_cap * Hkv * G) * 4, 256);
+  w.total = w.o + (size_t)(sp_cap * Hkv * G * D) * 4;
   return w;
+}
+
+// Largest partial capacity that fits `bytes` (at least B: one partition per
+// sequence needs no partials).
+int64_t cap_for_bytes(int32_t B, int32_t Hkv, int32_t G, int32_t D, size_t bytes) {
+  const size_t per = (size_t)Hkv * G * (D + 1) * 4;
+  const size_t head = round_up((size_t)B * 4, 256) + 256;
+  int64_t s = bytes > head ? (int64_t)((bytes - head) / per) : 0;
+  while (s > B && layout_for_cap(B, Hkv, G, D, s).total > bytes) --s;
+  return s > B ? s : B;
+}
+
+// Bytes needed when every sequence may be split into partitions of P pages
+// (0 when no sequence can be split).
+size_t bytes_for_partition(int32_t B, int32_t Hkv, int32_t G, int32_t D, int32_t max_ctx,
+                           int32_t P) {
+  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
+  const int64_t parts_max = pages_max > 0 ? cdiv(pages_max, P) : 1;
+  if (parts_max <= 1 || B == 0) return 0;
+  return layout_for_cap(B, Hkv, G, D, (int64_t)B * parts_max).total;
+}
+
+// Partition size the default workspace is sized for: the launcher heuristic,
+// or a finer size when that still fits in 16 MiB (room for the kernel to pick
+// a better-balanced size from the exact lengths).
+int32_t workspace_partition_pages(int32_t B, int32_t Hkv, int32_t G, int32_t D, int32_t max_ctx,
+                                  int sms) {
+  const int32_t heur = auto_partition_pages(B, Hkv, max_ctx, sms);
+  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
+  if (pages_max <= 0 || B <= 0) return heur;
+  const size_t budget = (size_t)16 << 20;
+  const int64_t per_seq_part = (int64_t)Hkv * G * (D + 1) * 4;
+  const int64_t k = (int64_t)(budget - round_up((size_t)B * 4, 256) - 512) / (per_seq_part * B);
+  int64_t p_budget = k >= 1 ? cdiv(pages_max, k) : pages_max;
+  if (p_budget < 4) p_budget = 4;
+  while (p_budget < pages_max && bytes_for_partition(B, Hkv, G, D, max_ctx, (int32_t)p_budget) > budget)
+    ++p_budget;
+  return (int32_t)(p_budget < heur ? p_budget : heur);
 }
 
 bool make_map(CUtensorMap* m, const void* base, int elem_bytes, int D, int64_t rows) {
@@ -183,31 +218,48 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   if (s != KVQ_OK || B == 0) return s;
   DeviceState* st = device_state();
   if (!st) return cuda_fail();
-  if (P == 0) P = auto_partition_pages(B, Hkv, max_ctx, st->sms);
-  if (P < 1 || P > kMaxPartitionPages) return KVQ_ERR_INVALID_ARGUMENT;
   const bool bf16 = dtype == KVQ_BF16;
-  const WsLayout wl = workspace_layout(B, Hq, Hkv, D, max_ctx, P);
-  if (wl.split) {
-    if (ws_bytes < wl.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-    if (!ws || !aligned(ws, 256)) return KVQ_ERR_INVALID_ARGUMENT;
+  const int32_t G = Hq / Hkv;
+  WsLayout wl;
+  if (P == 0) {
+    // the kernel picks the partition size within the workspace's capacity
+    // minimum: room for the launcher heuristic's partitions (the size
+    // kvq_decode_workspace_bytes recommends may allow finer ones)
+    const int32_t P_min = auto_partition_pages(B, Hkv, max_ctx, st->sms);
+    const size_t need = bytes_for_partition(B, Hkv, G, D, max_ctx, P_min);
+    if (ws_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t cap = (ws && cdiv(max_ctx, kBlockSize) > 1) ? cap_for_bytes(B, Hkv, G, D, ws_bytes)
+                                                              : B;
+    wl = layout_for_cap(B, Hkv, G, D, cap);
+  } else {
+    if (P < 1 || P > kMaxPartitionPages) return KVQ_ERR_INVALID_ARGUMENT;
+    const size_t need = bytes_for_partition(B, Hkv, G, D, max_ctx, P);
+    if (ws_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t pages_max = cdiv(max_ctx, kBlockSize);
+    wl = layout_for_cap(B, Hkv, G, D, need ? (int64_t)B * cdiv(pages_max, P) : B);
   }
+  const bool split = wl.sp_cap > B;
+  if (split && (!ws || !aligned(ws, 256))) return KVQ_ERR_INVALID_ARGUMENT;
 
-  CUtensorMap tmk, tmv;
+  CUtensorMap maps[2];
   const int64_t rows = (int64_t)num_blocks * Hkv * kBlockSize;
   const int eb = int8 ? 1 : 2;
-  if (!make_map(&tmk, kc, eb, D, rows) || !make_map(&tmv, vc, eb, D, rows)) return cuda_fail();
+  if (!make_map(&maps[0], kc, eb, D, rows) || !make_map(&maps[1], vc, eb, D, rows))
+    return cuda_fail();
 
   DecodeParams p{};
   p.q = q;
   p.out = out;
+  p.k_cache = kc;
+  p.v_cache = vc;
   p.k_scale = ks;
   p.v_scale = vs;
   p.block_tables = bt;
   p.context_lens = cl;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  p.prefix_out = wl.split ? reinterpret_cast<int32_t*>(w + wl.prefix) : nullptr;
-  p.part_lse = wl.split ? reinterpret_cast<float*>(w + wl.lse) : nullptr;
-  p.part_o = wl.split ? reinterpret_cast<float*>(w + wl.o) : nullptr;
+  p.prefix_out = split ? reinterpret_cast<int32_t*>(w + wl.prefix) : nullptr;
+  p.part_lse = split ? reinterpret_cast<float*>(w + wl.lse) : nullptr;
+  p.part_o = split ? reinterpret_cast<float*>(w + wl.o) : nullptr;
   p.err = st->err;
   p.B = B;
   p.Hq = Hq;
@@ -217,21 +269,21 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   p.max_ctx = max_ctx;
   p.num_blocks = num_blocks;
   p.P = P;
+  p.sp_cap = (int32_t)(wl.sp_cap < INT32_MAX ? wl.sp_cap : INT32_MAX);
   p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
 
   const size_t smem =
       int8 ? decode_smem_bytes_int8(D, B, p.G) : decode_smem_bytes_kv16(D, B, p.G);
   const int occ = ctas_per_sm(st, int8, D, bf16, smem);
   if (occ <= 0) return cuda_fail();
-  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
-  const int64_t items_max = (int64_t)B * Hkv * (pages_max > 0 ? cdiv(pages_max, P) : 1);
+  const int64_t items_max = wl.sp_cap * Hkv;
   const int64_t slots = (int64_t)st->sms * occ;
   const int64_t ctas_needed = cdiv(items_max, kWarps);       // one item per warp at least
   const int grid = (int)(ctas_needed < slots ? ctas_needed : slots);
-  cudaError_t e = int8 ? decode_launch_int8(D, bf16, &tmk, &tmv, p, grid, smem, stream)
-                       : decode_launch_kv16(D, bf16, &tmk, &tmv, p, grid, smem, stream);
+  cudaError_t e = int8 ? decode_launch_int8(D, bf16, maps, p, grid, smem, stream)
+                       : decode_launch_kv16(D, bf16, maps, p, grid, smem, stream);
   if (e != cudaSuccess) return cuda_fail();
-  if (wl.split) {
+  if (split) {
     CombineParams cp{};
     cp.part_o = p.part_o;
     cp.part_lse = p.part_lse;
@@ -392,12 +444,15 @@ kvq_status kvq_paged_decode_kv16(const void* q, kvq_dtype dtype, int32_t num_seq
                        workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_kv_heads,
-                                   int32_t max_context_len) {
-  if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0) return 0;
+int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t max_context_len) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
+      num_q_heads % num_kv_heads)
+    return 0;
   DeviceState* st = device_state();
   if (!st) return 0;
-  return auto_partition_pages(num_seqs, num_kv_heads, max_context_len, st->sms);
+  return workspace_partition_pages(num_seqs, num_kv_heads, num_q_heads / num_kv_heads, head_dim,
+                                   max_context_len, st->sms);
 }
 
 size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
@@ -406,14 +461,14 @@ size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
       partition_pages < 1 || num_q_heads % num_kv_heads)
     return 0;
-  return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
-                          partition_pages)
-      .total;
+  return bytes_for_partition(num_seqs, num_kv_heads, num_q_heads / num_kv_heads, head_dim,
+                             max_context_len, partition_pages);
 }
 
 size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len) {
-  const int32_t P = kvq_decode_partition_pages(num_seqs, num_kv_heads, max_context_len);
+  const int32_t P = kvq_decode_partition_pages(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                               max_context_len);
   if (P <= 0) return 0;
   return kvq_decode_workspace_bytes_split(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                           max_context_len, P);

@@ -10,19 +10,21 @@
 namespace kvq {
 namespace {
 
-constexpr int kCombineWarps = 8;
+constexpr int kCombineThreads = 256;
+constexpr int kCombineBatch = 8;   // partitions a thread loads before using any
 
-// One CTA per (query head, sequence).  The partitions are dealt round-robin
-// to the 8 warps; each lane owns D/32 consecutive head dims; the warps'
-// partial sums meet in shared memory.
+// One CTA per (query head, sequence).  Thread t owns 4 consecutive head dims
+// (column group t % (D/4)) of every R-th partition, R = 256 / (D/4); it loads
+// a batch of partitions at once, keeps its own running (max, sum, acc), and the
+// row groups meet in shared memory with the usual rescaling.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
-  constexpr int PER = D / 32;
-  __shared__ float red[kCombineWarps];
-  __shared__ float part[kCombineWarps][D];
-  __shared__ float wpart[kCombineWarps];
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+  constexpr int COLS = D / 4;                      // float4 columns per row
+  constexpr int ROWS = kCombineThreads / COLS;     // partitions in flight per pass
+  __shared__ float s_m[ROWS], s_w[ROWS];
+  __shared__ float4 s_acc[ROWS][COLS];
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int col = tid % COLS, row = tid / COLS;
   griddep_wait();               // the decode grid's partials are complete and visible
   const int sp0 = b > 0 ? p.prefix[b - 1] : 0;
   const int n = p.prefix[b] - sp0;
@@ -31,55 +33,70 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   const int64_t row0 = ((int64_t)sp0 * p.Hkv + j) * p.G + g;   // partition i: + i*Hkv*G
   const int64_t rstride = (int64_t)p.Hkv * p.G;
 
-  float M = -INFINITY;
-  for (int i = tid; i < n; i += kCombineWarps * 32) M = fmaxf(M, p.part_lse[row0 + i * rstride]);
+  float m = -INFINITY, wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = row; i0 < n; i0 += ROWS * kCombineBatch) {
+    float lse[kCombineBatch];
+    float4 v[kCombineBatch];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = red[0];
-#pragma unroll
-  for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red[w]);
-
-  float acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 4
-    for (int i = warp; i < n; i += kCombineWarps) {
-      const int64_t r = row0 + i * rstride;
-      const float w = fast_exp2(p.part_lse[r] - M);
-      wsum += w;
-      const float* src = p.part_o + r * D + lane * PER;
-      if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+    for (int k = 0; k < kCombineBatch; ++k) {
+      const int i = i0 + k * ROWS;
+      if (i < n) {
+        const int64_t r = row0 + i * rstride;
+        lse[k] = p.part_lse[r];
+        v[k] = reinterpret_cast<const float4*>(p.part_o + r * D)[col];
       } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y;
+        lse[k] = -INFINITY;
+        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
+    float bm = m;
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k) bm = fmaxf(bm, lse[k]);
+    if (bm == -INFINITY) continue;
+    const float a = fast_exp2(m - bm);
+    wsum *= a;
+    acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k) {
+      const float w = fast_exp2(lse[k] - bm);
+      wsum += w;
+      acc.x += w * v[k].x; acc.y += w * v[k].y; acc.z += w * v[k].z; acc.w += w * v[k].w;
+    }
+    m = bm;
   }
-#pragma unroll
-  for (int e = 0; e < PER; ++e) part[warp][lane * PER + e] = acc[e];
-  if (lane == 0) wpart[warp] = wsum;
+  s_acc[row][col] = acc;
+  if (col == 0) {
+    s_m[row] = m;
+    s_w[row] = wsum;
+  }
   __syncthreads();
-  if (tid < D / 2) {
-    const int d = 2 * tid;
-    float s0 = 0.f, s1 = 0.f, ws = 0.f;
+  if (row == 0) {
+    float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) {
-      s0 += part[w][d];
-      s1 += part[w][d + 1];
-      ws += wpart[w];
+    for (int r = 0; r < ROWS; ++r) M = fmaxf(M, s_m[r]);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ws = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) {
+        const float a = s_m[r] == -INFINITY ? 0.f : fast_exp2(s_m[r] - M);
+        const float4 x = s_acc[r][col];
+        ws += a * s_w[r];
+        o.x += a * x.x; o.y += a * x.y; o.z += a * x.z; o.w += a * x.w;
+      }
     }
     const float inv = ws > 0.f ? 1.f / ws : 0.f;
-    uint16_t* dst = static_cast<uint16_t*>(p.out) + ((int64_t)b * p.Hq + h) * D + d;
-    uint32_t v;
-    if constexpr (BF16) v = bf2_as_u32(__floats2bfloat162_rn(s0 * inv, s1 * inv));
-    else v = h2_as_u32(__floats2half2_rn(s0 * inv, s1 * inv));
-    *reinterpret_cast<uint32_t*>(dst) = v;
+    uint16_t* dst = static_cast<uint16_t*>(p.out) + ((int64_t)b * p.Hq + h) * D + 4 * col;
+    uint2 out;
+    if constexpr (BF16) {
+      out.x = bf2_as_u32(__floats2bfloat162_rn(o.x * inv, o.y * inv));
+      out.y = bf2_as_u32(__floats2bfloat162_rn(o.z * inv, o.w * inv));
+    } else {
+      out.x = h2_as_u32(__floats2half2_rn(o.x * inv, o.y * inv));
+      out.y = h2_as_u32(__floats2half2_rn(o.z * inv, o.w * inv));
+    }
+    *reinterpret_cast<uint2*>(dst) = out;
   }
 }
 
@@ -89,7 +106,7 @@ cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, cudaStream_
   if (p.B == 0 || p.Hq == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.Hq, p.B);
-  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

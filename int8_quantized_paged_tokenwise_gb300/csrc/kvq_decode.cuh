@@ -63,6 +63,16 @@ struct TileCfg {
   static constexpr int kMinCtas = INT8 ? KVQ_INT8_MIN_CTAS : 3;
 };
 
+// Partition sizes (pages per work item) the kernel chooses among when the
+// caller leaves the choice to it.
+constexpr int kNumCand = 20;
+__host__ __device__ constexpr int cand_pages(int k) {
+  return k == 0 ? 4 : k == 1 ? 5 : k == 2 ? 6 : k == 3 ? 7 : k == 4 ? 8 : k == 5 ? 10
+       : k == 6 ? 12 : k == 7 ? 14 : k == 8 ? 16 : k == 9 ? 20 : k == 10 ? 24 : k == 11 ? 28
+       : k == 12 ? 32 : k == 13 ? 40 : k == 14 ? 48 : k == 15 ? 56 : k == 16 ? 64
+       : k == 17 ? 80 : k == 18 ? 96 : 128;
+}
+
 // Byte offset inside a (K or V) tile of 16-byte chunk `c` of token row `t`,
 // with the TMA swizzle applied (16-byte chunk index XOR row bits).
 template <class C>
@@ -90,8 +100,8 @@ struct SmemLayout {
     scales = qfrag + (size_t)kWarps * kFragBytes;
     bars = (scales + (size_t)kWarps * C::kStages * C::kScaleBytes + 15) & ~(size_t)15;
     stage_blk = bars + (size_t)kWarps * C::kStages * 8;
-    misc = stage_blk + (size_t)kWarps * C::kStages * 4;
-    seq = (misc + 16 + 15) & ~(size_t)15;            // prefix[B], lens[B]
+    misc = stage_blk + (size_t)kWarps * C::kStages * 4;   // 4 ints + reduction buffer
+    seq = (misc + 16 + (size_t)kWarps * (kNumCand + 1) * 4 + 15) & ~(size_t)15;  // prefix, lens
     total_bytes = seq + (size_t)B * 8 + 1024;        // + alignment slack of the base
   }
 };
@@ -152,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;   // MMA fragment coordinates
-  const int B = p.B, Hkv = p.Hkv, G = p.G, P = p.P;
+  const int B = p.B, Hkv = p.Hkv, G = p.G;
   // tokens any sequence may have: the table row and the host's bound (which
   // sized the workspace); a larger context_lens entry is flagged and clamped
   const int max_tok = min(p.max_blocks * kBlockSize, p.max_ctx);
@@ -169,11 +179,21 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   griddep_launch_dependents();
   griddep_wait();
 
-  // ---- partition prefix over sequences (inclusive) and clamped lengths ----
+  // ---- clamped lengths, partition size, partition prefix over sequences ----
+  // P > 0: fixed by the caller.  P == 0: chosen here from the exact lengths,
+  // identically in every CTA: among candidate sizes whose partition count fits
+  // the workspace (p.sp_cap), the one with the lowest modelled time under the
+  // static round-robin assignment of items to warps,
+  //   cost(P) = ceil(items / warps) * (min(P, longest) + 2)   [pages],
+  // the +2 standing for the per-item overhead (query load, partial write).
+  int P = p.P;
   {
     const int per = (B + kThreads - 1) / kThreads;   // consecutive sequences per thread
     const int b0 = tid * per, b1 = min(B, b0 + per);
-    int sum = 0;
+    int cnt[kNumCand];
+#pragma unroll
+    for (int k = 0; k < kNumCand; ++k) cnt[k] = 0;
+    int pmax = 0;
     for (int b = b0; b < b1; ++b) {
       int L = __ldg(&p.context_lens[b]);
       if (L < 0 || L > max_tok) {
@@ -182,6 +202,51 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
       }
       lens[b] = L;
       const int pages = (L + kBlockSize - 1) / kBlockSize;
+      pmax = max(pmax, pages);
+      if (P == 0) {
+#pragma unroll
+        for (int k = 0; k < kNumCand; ++k) cnt[k] += max(1, (pages + cand_pages(k) - 1) / cand_pages(k));
+      }
+    }
+    if (P == 0) {
+      int* red = misc + 4;                           // [kWarps][kNumCand + 1]
+#pragma unroll
+      for (int k = 0; k < kNumCand; ++k) {
+        int v = cnt[k];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        if (lane == 0) red[warp * (kNumCand + 1) + k] = v;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) pmax = max(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
+      if (lane == 0) red[warp * (kNumCand + 1) + kNumCand] = pmax;
+      __syncthreads();
+      if (tid == 0) {
+        int longest = 0;
+        for (int w = 0; w < kWarps; ++w) longest = max(longest, red[w * (kNumCand + 1) + kNumCand]);
+        const int64_t warps = (int64_t)gridDim.x * kWarps;
+        // no split: one partition per sequence (always fits)
+        int best_p = max(longest, 1);
+        int64_t best_cost = ((int64_t)B * Hkv + warps - 1) / warps * (int64_t)(best_p + 2);
+        for (int k = 0; k < kNumCand; ++k) {
+          int sp = 0;
+          for (int w = 0; w < kWarps; ++w) sp += red[w * (kNumCand + 1) + k];
+          if (sp > p.sp_cap || cand_pages(k) >= longest) continue;
+          const int64_t items = (int64_t)sp * Hkv;
+          const int64_t cost = (items + warps - 1) / warps * (int64_t)(cand_pages(k) + 2);
+          if (cost <= best_cost) {
+            best_cost = cost;
+            best_p = cand_pages(k);
+          }
+        }
+        misc[3] = best_p;
+      }
+      __syncthreads();
+      P = misc[3];
+    }
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int pages = (lens[b] + kBlockSize - 1) / kBlockSize;
       sum += max(1, (pages + P - 1) / P);
     }
     int incl = sum;                                  // block-wide scan of per-thread sums
@@ -190,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
       const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
       if (lane >= o) incl += y;
     }
+    __syncthreads();                                 // misc[] free again
     if (lane == 31) misc[warp] = incl;
     __syncthreads();
     int run = incl - sum;
@@ -221,12 +287,27 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   const uint32_t bars_u32 = smem_u32(&bars[warp * S]);
   int* blk_w = stage_blk + warp * S;
 
+  // Each page arrives as copies issued together by lanes 0..3: 2-D tensor TMA
+  // of the K and V tiles (16-bit tiles in 128-byte-wide sub-tiles; a tiled
+  // TMA needs a 128-byte aligned shared destination, which the tiles have)
+  // and, for INT8, 1-D bulk copies of the K and V scale rows (16-byte aligned
+  // destinations).  Per lane: tensor map, x coordinate and destination (+ the
+  // per-stage stride), or the scale plane and destination.
+  constexpr int kTensorCopies = 2 * C::kSubTiles;
+  const CUtensorMap* cp_map = lane < C::kSubTiles ? &tmK : &tmV;
+  const int cp_sub = lane % C::kSubTiles;               // 128-byte column block
+  const int cp_x = cp_sub * (C::kSubRow / C::kElem);
+  const uint32_t cp_dst = tiles_u32 + (lane < C::kSubTiles ? 0 : C::kTile) + cp_sub * C::kSubBytes;
+  const uint16_t* sc_src = lane == kTensorCopies ? p.k_scale : p.v_scale;
+  const uint32_t sc_dst = scales_u32 + (lane == kTensorCopies ? 0 : kBlockSize * 2);
+
   // ---------------------------------------------------------------- issuer
   // Warp-uniform state; lane 0 performs the copies.  The block ids of the
   // current 32-page chunk live one per lane (blk_cur); the first chunk of the
   // following item is prefetched into blk_nxt.
   int64_t is_item = wg;
   int is_ord = 0, is_pg = 0, is_chunk = 0;
+  ItemInfo nx_it{};                      // the item after the issuer's (first chunk in blk_nxt)
   int q_issued = -1, q_consumed = -1;   // ordinals: last item whose query was copied / read
   ItemInfo is_it{};
   int blk_cur = -1, blk_nxt = -1;
@@ -248,8 +329,12 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
     return blk;
   };
   auto next_item_chunk = [&](int64_t item) -> int {
-    if (item >= n_items) return -1;
-    return load_chunk(item_info(item, prefix, lens, B, Hkv, P), 0);
+    if (item >= n_items) {
+      nx_it.npg = 0;
+      return -1;
+    }
+    nx_it = item_info(item, prefix, lens, B, Hkv, P);
+    return load_chunk(nx_it, 0);
   };
   if (is_item < n_items) {
     is_it = item_info(is_item, prefix, lens, B, Hkv, P);
@@ -281,38 +366,27 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
       const int blk = __shfl_sync(0xFFFFFFFFu, blk_cur, is_pg - is_chunk);
       const int s = is_slot;
       is_slot = is_slot + 1 == S ? 0 : is_slot + 1;
+      const uint32_t bar = bars_u32 + 8 * s;
+      const uint32_t qbytes = is_pg == 0 ? lay.q_bytes : 0u;
       if (lane == 0) {
-        const uint32_t bar = bars_u32 + 8 * s;
         blk_w[s] = blk;
-        const uint32_t qbytes = is_pg == 0 ? lay.q_bytes : 0u;
-        if (blk < 0) {
-          if (qbytes) {
-            mbar_arrive_expect_tx(bar, qbytes);
-          } else {
-            mbar_arrive(bar);
-          }
-        } else {
-          mbar_arrive_expect_tx(bar, C::kTxBytes + qbytes);
-          const uint32_t kdst = tiles_u32 + s * C::kStageBytes;
-          const int y = (blk * Hkv + is_it.j) * kBlockSize;
-#pragma unroll
-          for (int st = 0; st < C::kSubTiles; ++st) {
-            tma_load_2d(kdst + st * C::kSubBytes, &tmK, st * (C::kSubRow / C::kElem), y, bar);
-            tma_load_2d(kdst + C::kTile + st * C::kSubBytes, &tmV,
-                        st * (C::kSubRow / C::kElem), y, bar);
-          }
-          if constexpr (INT8) {
-            const int64_t srow = ((int64_t)blk * Hkv + is_it.j) * kBlockSize;
-            const uint32_t sdst = scales_u32 + s * C::kScaleBytes;
-            bulk_load(sdst, p.k_scale + srow, kBlockSize * 2, bar);
-            bulk_load(sdst + kBlockSize * 2, p.v_scale + srow, kBlockSize * 2, bar);
-          }
+        if (blk >= 0) mbar_arrive_expect_tx(bar, C::kTxBytes + qbytes);
+        else if (qbytes) mbar_arrive_expect_tx(bar, qbytes);
+        else mbar_arrive(bar);
+      }
+      if (blk >= 0) {
+        const int row = blk * Hkv + is_it.j;          // (block, KV head) tile index
+        if (lane < kTensorCopies) {
+          tma_load_2d(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * kBlockSize, bar);
+        } else if (INT8 && lane < kTensorCopies + 2) {
+          bulk_load(sc_dst + s * C::kScaleBytes, sc_src + (int64_t)row * kBlockSize,
+                    kBlockSize * 2, bar);
         }
-        if (qbytes) {
-          const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) +
-                                 ((int64_t)is_it.b * p.Hq + (int64_t)is_it.j * G) * D;
-          bulk_load(q_u32, qsrc, qbytes, bar);
-        }
+      }
+      if (qbytes && lane == 4) {
+        const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) +
+                               ((int64_t)is_it.b * p.Hq + (int64_t)is_it.j * G) * D;
+        bulk_load(q_u32, qsrc, qbytes, bar);
       }
       if (is_pg == 0) q_issued = is_ord;
       ++n_issued;

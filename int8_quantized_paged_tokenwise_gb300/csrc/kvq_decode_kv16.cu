@@ -29,7 +29,7 @@ cudaError_t decode_occupancy_kv16(int D, bool bf16, size_t smem, int* n) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, pick(D, bf16), kThreads, smem);
 }
 
-cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* tmk, const CUtensorMap* tmv,
+cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* maps,
                                const DecodeParams& p, int grid, size_t smem, cudaStream_t s) {
   // programmatic stream serialization: the launch may overlap the tail of the
   // previous kernel in the stream; the kernel waits (griddepcontrol) before
@@ -45,11 +45,11 @@ cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* tmk, const C
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (D == 128) {
-    return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, false, true>, *tmk, *tmv, p)
-                : cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, false, false>, *tmk, *tmv, p);
+    return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, false, true>, maps[0], maps[1], p)
+                : cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, false, false>, maps[0], maps[1], p);
   }
-  return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, false, true>, *tmk, *tmv, p)
-              : cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, false, false>, *tmk, *tmv, p);
+  return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, false, true>, maps[0], maps[1], p)
+              : cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, false, false>, maps[0], maps[1], p);
 }
 
 }  // namespace kvq

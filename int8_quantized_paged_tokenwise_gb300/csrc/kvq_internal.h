@@ -33,6 +33,8 @@ struct QuantParams {
 struct DecodeParams {
   const void* q;
   void* out;
+  const void* k_cache;      // payload base pointers (L2 prefetch addresses)
+  const void* v_cache;
   const uint16_t* k_scale;  // INT8 path only
   const uint16_t* v_scale;
   const int32_t* block_tables;
@@ -45,7 +47,8 @@ struct DecodeParams {
   int32_t max_blocks;       // block-table row length
   int32_t max_ctx;          // host upper bound on context_lens
   int32_t num_blocks;
-  int32_t P;                // pages per partition (one warp's work item)
+  int32_t P;                // pages per partition (one warp's work item); 0 = kernel picks
+  int32_t sp_cap;           // sequence-partitions the workspace holds (>= B)
   float scale_log2;         // sm_scale * log2(e)
 };
 
@@ -57,16 +60,17 @@ struct CombineParams {
   int32_t B, Hq, Hkv, G;
 };
 
-// decode (kvq_decode_int8.cu / kvq_decode_kv16.cu); D = head_dim, smem in bytes.
+// decode (kvq_decode_int8.cu / kvq_decode_kv16.cu); D = head_dim, smem in bytes; maps =
+// {K tiles, V tiles}.
 size_t decode_smem_bytes_int8(int D, int B, int G);
 cudaError_t decode_configure_int8(int D, bool bf16, size_t smem);
 cudaError_t decode_occupancy_int8(int D, bool bf16, size_t smem, int* n);
-cudaError_t decode_launch_int8(int D, bool bf16, const CUtensorMap* tmk, const CUtensorMap* tmv,
+cudaError_t decode_launch_int8(int D, bool bf16, const CUtensorMap* maps,
                                const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
 size_t decode_smem_bytes_kv16(int D, int B, int G);
 cudaError_t decode_configure_kv16(int D, bool bf16, size_t smem);
 cudaError_t decode_occupancy_kv16(int D, bool bf16, size_t smem, int* n);
-cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* tmk, const CUtensorMap* tmv,
+cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* maps,
                                const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
 
 // combine (kvq_combine.cu)
