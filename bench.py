@@ -47,7 +47,7 @@ FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SOURCES = ("kvq_decode.cuh", "kvq_decode_int8.cu", "kvq_ptx.cuh", "kvq_combine.cu",
                   "kvq_api.cu", "kvq_internal.h")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_int8_canonical_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_int8_canonical.traffic.txt")
 
 
 def parse_args():
@@ -61,6 +61,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--settle", type=float, default=1.5,
                     help="seconds of untimed steps before the timed region (clock sampling)")
+    ap.add_argument("--profile-arm", choices=["int8", "kv16"], default=None,
+                    help="profiling run: only this decode arm (one cache on the device), "
+                         "warm-up + steps with L2 flushes, a short timing line; no bench line")
     return ap.parse_args()
 
 
@@ -75,6 +78,24 @@ def decode_source_hash() -> str:
         with open(os.path.join(ROOT, "int8_quantized_paged_tokenwise_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary ("key: value"
+    lines), or None when it was taken on other sources or another workload."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                line = line.strip()
+                if line and not line.startswith("#") and ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_hash") == decode_source_hash() and kv.get("workload") == workload:
+            return int(kv["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
 
 
 def measured_peak():
@@ -204,7 +225,7 @@ class GpuWorkload:
     """A workload resident in HBM: INT8 cache, BF16 twin cache, tables, q and
     the step's new tokens, plus pinned host copies for the end-to-end arm."""
 
-    def __init__(self, w: W.Workload, dev):
+    def __init__(self, w: W.Workload, dev, arms=("int8", "kv16")):
         import torch
         import int8_quantized_paged_tokenwise_gb300 as kvq
         self.torch, self.kvq, self.w, self.dev = torch, kvq, w, dev
@@ -215,8 +236,9 @@ class GpuWorkload:
             return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(tdt)
 
         nb, bt, _ = w.tables()
-        self.int8 = kvq.alloc_int8_cache(nb, w.num_kv_heads, w.head_dim, dev)
-        self.kv16 = kvq.alloc_kv16_cache(nb, w.num_kv_heads, w.head_dim, tdt, dev)
+        self.int8 = kvq.alloc_int8_cache(nb, w.num_kv_heads, w.head_dim, dev) if "int8" in arms else None
+        self.kv16 = (kvq.alloc_kv16_cache(nb, w.num_kv_heads, w.head_dim, tdt, dev)
+                     if "kv16" in arms else None)
         for b in range(w.num_seqs):
             k, v = w.seq_kv(b)
             n = int(w.prefix_lens[b])
@@ -224,8 +246,10 @@ class GpuWorkload:
                 continue
             s = torch.from_numpy(w.slots(b, 0, n)).to(dev)
             kd, vd = up(k[:n]), up(v[:n])
-            kvq.kvq_quantize_append(kd, vd, s, *self.int8)
-            kvq.kvq_cache_append_kv16(kd, vd, s, *self.kv16)
+            if self.int8 is not None:
+                kvq.kvq_quantize_append(kd, vd, s, *self.int8)
+            if self.kv16 is not None:
+                kvq.kvq_cache_append_kv16(kd, vd, s, *self.kv16)
         ks, vs, ss = [], [], []
         if w.append:
             for b in range(w.num_seqs):
@@ -388,6 +412,21 @@ def sweep(torch, kvq, dev, flush, steps):
     return res
 
 
+def profile_arm(torch, w, dev, args):
+    """One decode arm alone (for ncu captures of a bounded device footprint)."""
+    g = GpuWorkload(w, dev, arms=(args.profile_arm,))
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()  # noqa: E731
+    nop = lambda: None  # noqa: E731
+    dec = g.decode_int8 if args.profile_arm == "int8" else g.decode_kv16
+    _, t = time_arm(torch, flush, nop, dec, args.steps, args.warmup)
+    nbytes = w.decode_bytes_int8() if args.profile_arm == "int8" else w.decode_bytes_kv16()
+    ms = statistics.mean(t)
+    print(json.dumps({"profile_arm": args.profile_arm, "workload": w.name,
+                      "decode_us": round(1e3 * ms, 2),
+                      "decode_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}))
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -408,6 +447,9 @@ def main():
     kvq.load(build_if_missing=False)
 
     w = W.make(args.workload)
+    if args.profile_arm:
+        profile_arm(torch, w, dev, args)
+        return
     g = GpuWorkload(w, dev)
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.zero_()  # noqa: E731
@@ -444,14 +486,7 @@ def main():
     value = world * step_bytes / (step_ms * 1e-3) / 1e9
     dec_gbs = w.decode_bytes_int8() / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = None
-    try:
-        with open(TRAFFIC_FILE) as f:
-            tr = json.load(f)
-        if tr.get("source_hash") == decode_source_hash() and tr.get("workload") == w.name:
-            traffic = tr.get("traffic_bytes_per_launch")
-    except Exception:
-        pass
+    traffic = read_traffic(w.name)
     sw = None
     if not args.no_sweep:
         sw = sweep(torch, kvq, dev, flush, max(5, min(args.steps, 20)))

@@ -277,6 +277,7 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   const int occ = ctas_per_sm(st, int8, D, bf16, smem);
   if (occ <= 0) return cuda_fail();
   const int64_t items_max = wl.sp_cap * Hkv;
+  if (items_max > INT32_MAX) return KVQ_ERR_UNSUPPORTED;   // the kernel counts items in 32 bits
   const int64_t slots = (int64_t)st->sms * occ;
   const int64_t ctas_needed = cdiv(items_max, kWarps);       // one item per warp at least
   const int grid = (int)(ctas_needed < slots ? ctas_needed : slots);

@@ -84,12 +84,11 @@ __device__ __forceinline__ uint32_t tile_off(int t, int c) {
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).  Per warp:
 // S page stages, one raw query slot (the TMA target, G*D*2 bytes) and a query
-// fragment buffer ([k-step][lane] pairs of the MMA B operand, D*16 bytes;
-// lanes of padded heads hold zeros).
+// fragment buffer ([k-step][lane] pairs of the MMA B operand for the lanes
+// 0..4G-1 of real heads, also G*D*2 bytes; the padded heads read as zeros).
 template <int D, bool INT8>
 struct SmemLayout {
   using C = TileCfg<D, INT8>;
-  static constexpr uint32_t kFragBytes = (uint32_t)D * 16;   // (D/16) k-steps x 32 lanes x 8 B
   size_t tiles, q, qfrag, scales, bars, stage_blk, misc, seq, total_bytes;
   uint32_t q_bytes;  // one item's query rows: G * D * 2
   __host__ __device__ SmemLayout(int B, int G) {
@@ -97,7 +96,7 @@ struct SmemLayout {
     tiles = 0;
     q = tiles + (size_t)kWarps * C::kStages * C::kStageBytes;
     qfrag = q + (size_t)kWarps * q_bytes;
-    scales = qfrag + (size_t)kWarps * kFragBytes;
+    scales = qfrag + (size_t)kWarps * q_bytes;
     bars = (scales + (size_t)kWarps * C::kStages * C::kScaleBytes + 15) & ~(size_t)15;
     stage_blk = bars + (size_t)kWarps * C::kStages * 8;
     misc = stage_blk + (size_t)kWarps * C::kStages * 4;   // 4 ints + reduction buffer
@@ -120,8 +119,10 @@ struct ItemInfo {
 __device__ __forceinline__ ItemInfo item_info(int64_t item, const int* prefix, const int* lens,
                                               int B, int Hkv, int P) {
   ItemInfo it;
-  it.sp = (int)(item / Hkv);
-  it.j = (int)(item - (int64_t)it.sp * Hkv);
+  // item counts stay below 2^31 (checked on the host): 32-bit division
+  const uint32_t u = (uint32_t)item;
+  it.sp = (int)(u / (uint32_t)Hkv);
+  it.j = (int)(u - (uint32_t)it.sp * (uint32_t)Hkv);
   int lo = 0, hi = B - 1;                       // first b with prefix[b] > sp
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
@@ -178,6 +179,23 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   // writes are visible, before reading any input.
   griddep_launch_dependents();
   griddep_wait();
+  // Warm L2 with the small inputs every warp reads first (block tables and
+  // query rows): CTA i prefetches the i-th 4 KB slice of each.
+  if (tid == 0) {
+    const int64_t bt_bytes = (int64_t)p.B * p.max_blocks * 4;
+    const int64_t q_bytes = (int64_t)p.B * p.Hq * D * 2;
+    const int64_t off = (int64_t)blockIdx.x * 4096;
+    if (off < bt_bytes && (bt_bytes & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0) {
+      const int64_t n = bt_bytes - off;
+      prefetch_l2(reinterpret_cast<const uint8_t*>(p.block_tables) + off,
+                  (uint32_t)(n < 4096 ? n : 4096));
+    }
+    if (off < q_bytes) {
+      const int64_t n = q_bytes - off;
+      prefetch_l2(static_cast<const uint8_t*>(p.q) + off, (uint32_t)(n < 4096 ? n : 4096));
+    }
+  }
 
   // ---- clamped lengths, partition size, partition prefix over sequences ----
   // P > 0: fixed by the caller.  P == 0: chosen here from the exact lengths,
@@ -221,25 +239,39 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
       for (int o = 16; o > 0; o >>= 1) pmax = max(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
       if (lane == 0) red[warp * (kNumCand + 1) + kNumCand] = pmax;
       __syncthreads();
-      if (tid == 0) {
+      if (warp == 0) {
+        // lane k scores candidate k (lane kNumCand: no split); warp arg-min,
+        // ties to the larger size
         int longest = 0;
         for (int w = 0; w < kWarps; ++w) longest = max(longest, red[w * (kNumCand + 1) + kNumCand]);
-        const int64_t warps = (int64_t)gridDim.x * kWarps;
-        // no split: one partition per sequence (always fits)
-        int best_p = max(longest, 1);
-        int64_t best_cost = ((int64_t)B * Hkv + warps - 1) / warps * (int64_t)(best_p + 2);
-        for (int k = 0; k < kNumCand; ++k) {
+        const uint32_t warps = (uint32_t)gridDim.x * kWarps;
+        uint32_t cost = 0xFFFFFFFFu;
+        int cand = 0;
+        if (lane < kNumCand) {
+          // branch-free pick of this lane's size (an indexed lookup of the
+          // table would become a divergent jump or a memory access)
+#pragma unroll
+          for (int k = 0; k < kNumCand; ++k) cand = lane == k ? cand_pages(k) : cand;
           int sp = 0;
-          for (int w = 0; w < kWarps; ++w) sp += red[w * (kNumCand + 1) + k];
-          if (sp > p.sp_cap || cand_pages(k) >= longest) continue;
-          const int64_t items = (int64_t)sp * Hkv;
-          const int64_t cost = (items + warps - 1) / warps * (int64_t)(cand_pages(k) + 2);
-          if (cost <= best_cost) {
-            best_cost = cost;
-            best_p = cand_pages(k);
+          for (int w = 0; w < kWarps; ++w) sp += red[w * (kNumCand + 1) + lane];
+          if (sp <= p.sp_cap && cand < longest) {
+            const uint32_t items = (uint32_t)sp * (uint32_t)Hkv;
+            cost = (items + warps - 1) / warps * (uint32_t)(cand + 2);
+          }
+        } else if (lane == kNumCand) {
+          cand = max(longest, 1);
+          cost = ((uint32_t)B * (uint32_t)Hkv + warps - 1) / warps * (uint32_t)(cand + 2);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const uint32_t oc = __shfl_xor_sync(0xFFFFFFFFu, cost, o);
+          const int op = __shfl_xor_sync(0xFFFFFFFFu, cand, o);
+          if (oc < cost || (oc == cost && op > cand)) {
+            cost = oc;
+            cand = op;
           }
         }
-        misc[3] = best_p;
+        if (lane == 0) misc[3] = cand;
       }
       __syncthreads();
       P = misc[3];
@@ -277,10 +309,9 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
 
   const uint32_t tiles_u32 = smem_u32(smem + lay.tiles) + warp * S * C::kStageBytes;
   const uint32_t q_u32 = smem_u32(smem + lay.q) + warp * lay.q_bytes;
-  uint2* qfrag = reinterpret_cast<uint2*>(smem + lay.qfrag + (size_t)warp * lay.kFragBytes);
-  const uint32_t qfrag_lane_u32 = smem_u32(qfrag) + 8 * lane;   // + 256 * ks
-  if (lane >= 4 * G)                                             // padded heads: zero columns
-    for (int ks = 0; ks < KSTEPS; ++ks) qfrag[ks * 32 + lane] = make_uint2(0, 0);
+  uint2* qfrag = reinterpret_cast<uint2*>(smem + lay.qfrag + (size_t)warp * lay.q_bytes);
+  const uint32_t qfrag_lane_u32 = smem_u32(qfrag) + 8 * lane;   // + 32 * G * ks
+  const uint32_t qks = 32u * (uint32_t)G;                        // bytes per k-step
   const uint32_t scales_u32 = smem_u32(smem + lay.scales) + warp * S * C::kScaleBytes;
   const uint16_t* scales_w =
       reinterpret_cast<const uint16_t*>(smem + lay.scales) + warp * S * (C::kScaleBytes / 2);
@@ -447,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
               f.x = *reinterpret_cast<const uint32_t*>(qs + 16 * ks + 2 * c);
               f.y = *reinterpret_cast<const uint32_t*>(qs + 16 * ks + 8 + 2 * c);
             }
-            qfrag[ks * 32 + lane] = f;
+            qfrag[ks * 4 * G + lane] = f;
           }
         }
         q_consumed = ord;
@@ -468,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
         for (int kk = 0; kk < (INT8 ? KSTEPS / 2 : 0); ++kk) {
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kt + tile_off<C>(lt, 2 * kk + (lane >> 4)), r0, r1, r2, r3);
-          const uint2 qa = lds_u2(qfrag_lane_u32 + 256 * (2 * kk));
-          const uint2 qb = lds_u2(qfrag_lane_u32 + 256 * (2 * kk + 1));
+          const uint2 qa = lds_u2_if(has_head, qfrag_lane_u32 + qks * (2 * kk));
+          const uint2 qb = lds_u2_if(has_head, qfrag_lane_u32 + qks * (2 * kk + 1));
           if constexpr (INT8) {
             // r0/r1: tokens g / g+8, head-dim 16(2kk)+4c+{0..3}; r2/r3: next chunk
             uint32_t a0, a2, a1, a3;
@@ -488,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
           for (int ks = 0; ks < KSTEPS; ++ks) {
             uint32_t r0, r1, r2, r3;
             ldsm_x4(kt + tile_off<C>(lt, 2 * ks + (lane >> 4)), r0, r1, r2, r3);
-            const uint2 qa = lds_u2(qfrag_lane_u32 + 256 * ks);
+            const uint2 qa = lds_u2_if(has_head, qfrag_lane_u32 + qks * ks);
             // a0: token g, d 16ks+2c..; a1: token g+8; a2: token g, d 16ks+8+2c..; a3: g+8
             if (ks & 1) mma_16816_acc<MMA_BF16>(sb, r0, r1, r2, r3, qa.x, qa.y);
             else mma_16816_acc<MMA_BF16>(sa, r0, r1, r2, r3, qa.x, qa.y);

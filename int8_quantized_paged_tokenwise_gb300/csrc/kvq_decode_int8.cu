@@ -20,6 +20,11 @@ size_t decode_smem_bytes_int8(int D, int B, int G) {
 }
 
 cudaError_t decode_configure_int8(int D, bool bf16, size_t smem) {
+  // all of the unified L1/shared array as shared memory: the kernel's
+  // occupancy is set by its page stages
+  cudaError_t e = cudaFuncSetAttribute(pick(D, bf16), cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(pick(D, bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem);
 }
