@@ -136,13 +136,17 @@ kvq_status kvq_quantize_append(const void* k, const void* v, int64_t k_token_str
  *                   upper bound on every entry (used by the launcher; an entry
  *                   above max_blocks_per_seq*16 sets KVQ_DEVERR_CONTEXT and
  *                   that sequence's output is left unspecified).
- *   workspace       device scratch of >= kvq_decode_workspace_bytes(...)
- *                   bytes (may be NULL when that is 0), 256-byte aligned, not
- *                   shared by calls that overlap on the GPU.
- * Work is split into items of (sequence, KV head, partition of P pages); the
- * kernel chooses P from the exact context lengths (kvq_decode_partition_pages
- * describes how); sequences longer than one partition go through split-K
- * partials and a combine kernel.
+ *   workspace       device scratch of kvq_decode_workspace_bytes(...) bytes,
+ *                   256-byte aligned, not shared by calls that overlap on the
+ *                   GPU.  NULL (or 0 bytes): no split-K -- one warp per
+ *                   (sequence, KV head), correct but unbalanced.  A smaller
+ *                   non-zero size is accepted down to four work ranges and
+ *                   only lowers the number of warps used.
+ * Work distribution: the (sequence, KV head, page) tiles form one stream,
+ * cut into ranges of R = max(4, ceil(tiles / warps)) pages from the exact
+ * context lengths, one range per resident warp, so every warp reads the same
+ * number of pages.  A sequence whose tiles span two or more ranges goes
+ * through split-K partials and a combine kernel (flash-decoding).
  */
 kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -154,24 +158,24 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
                             float sm_scale, void* out, void* workspace,
                             size_t workspace_bytes, kvq_stream_t stream);
 
-/* Scratch bytes kvq_paged_decode needs for these sizes on the current device
- * (0 when no sequence can be split).  Passing more lets the kernel choose
- * finer partitions (see below). */
+/* Scratch bytes for kvq_paged_decode (and kvq_paged_decode_kv16) with these
+ * sizes on the current device: two partial slots of G rows per work range,
+ * one range per resident warp.  0 when no sequence can span two pages or on
+ * invalid sizes. */
 size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len);
 
-/* The partition size (pages per work item; one warp processes one item) that
- * kvq_decode_workspace_bytes sizes the workspace for on the current device;
- * 0 on invalid input.  kvq_paged_decode itself lets the kernel pick the
- * partition size from the exact context lengths: among a fixed set of
- * candidate sizes whose partition count fits the given workspace, the one
- * that best balances the work items over the resident warps. */
+/* The work-range length (pages) kvq_paged_decode uses on the current device
+ * when every sequence holds max_context_len tokens: max(4, ceil(tiles /
+ * resident warps)); with shorter contexts the kernel uses the value for the
+ * actual total.  0 on invalid input. */
 int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_context_len);
 
-/* kvq_paged_decode with the partition size forced (pages per work item, >= 1);
- * used to test every launcher variant.  Workspace from
- * kvq_decode_workspace_bytes_split with the same partition size. */
+/* kvq_paged_decode with the work-range length forced (partition_pages >= 1
+ * pages per range; ranges are dealt to the warps round-robin), for tests and
+ * tuning.  Workspace from kvq_decode_workspace_bytes_split with the same
+ * length (required, also when nothing ends up split). */
 kvq_status kvq_paged_decode_split(const void* q, kvq_dtype dtype, int32_t num_seqs,
                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   const int8_t* k_cache, const int8_t* v_cache,

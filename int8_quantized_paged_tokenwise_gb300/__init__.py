@@ -246,7 +246,11 @@ def kvq_paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_tables, contex
                      max_context_len: int, sm_scale: float, out=None, workspace=None,
                      partition_pages: int = 0, stream=None):
     """Paged decode over the INT8 cache.  q [B, Hq, D]; block_tables int32
-    [B, max_blocks]; context_lens int32 [B]; returns out [B, Hq, D]."""
+    [B, max_blocks]; context_lens int32 [B]; returns out [B, Hq, D].
+    ``workspace``: None allocates kvq_decode_workspace_bytes; an empty tensor
+    runs without split-K (one warp per (sequence, KV head)).
+    ``partition_pages``: 0 = balanced work ranges; >= 1 forces the range
+    length in pages."""
     L = load()
     B, Hq, D = q.shape
     NB, Hkv, bs, _ = k_cache.shape

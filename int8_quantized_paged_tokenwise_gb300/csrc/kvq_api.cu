@@ -18,16 +18,15 @@ __device__ unsigned int g_kvq_error_word = 0u;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxPartitionPages = 1 << 16;
-constexpr int kMaxAutoPartitionPages = 64;
+constexpr int kMaxRangePages = 1 << 24;   // forced range length accepted by the _split calls
 
 struct DeviceState {
   bool ready = false;
   int sms = 0;
   unsigned int* err = nullptr;
   // occupancy cache: [variant][last smem] -> ctas per SM
-  size_t occ_smem[6] = {0, 0, 0, 0, 0, 0};
-  int occ_ctas[6] = {0, 0, 0, 0, 0, 0};
+  size_t occ_smem[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int occ_ctas[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 };
 
 std::mutex g_mu;
@@ -71,9 +70,8 @@ DeviceState* device_state() {
 }
 
 int ctas_per_sm(DeviceState* st, bool int8, int D, bool bf16, size_t smem) {
-  // variants: int8 D128/D64 (activation dtype does not change the footprint),
-  // kv16 D128/D64 x fp16/bf16
-  int v = int8 ? (D == 128 ? 0 : 1) : (2 + (D == 128 ? 0 : 1) * 2 + (bf16 ? 1 : 0));
+  // variants: {int8, kv16} x {D128, D64} x {fp16, bf16}
+  const int v = (int8 ? 0 : 4) + (D == 128 ? 0 : 2) + (bf16 ? 1 : 0);
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->occ_smem[v] != smem || st->occ_ctas[v] == 0) {
     int n = 0;
@@ -90,78 +88,70 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Pages per partition (one warp's work item) chosen by the launcher: about
-// three items per resident warp over an upper bound of the work (only
-// max_context_len is known on the host), a power of two in [8, 64] so that
-// skewed batches still split their longest sequences, and no larger than the
-// longest sequence needs.
-int32_t auto_partition_pages(int32_t B, int32_t Hkv, int32_t max_ctx, int sms) {
-  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
-  if (pages_max <= 0) return 8;
-  const int64_t warps = (int64_t)sms * 3 * kWarps;
-  const int64_t est = (int64_t)B * Hkv * pages_max;
-  const int64_t want = cdiv(est, 3 * warps);
-  int64_t p2 = 8;
-  while (p2 < want && p2 < kMaxAutoPartitionPages) p2 <<= 1;
-  return (int32_t)(p2 < pages_max ? p2 : pages_max);
-}
-
-struct WsLayout {
-  size_t prefix = 0, lse = 0, o = 0, total = 0;
-  int64_t sp_cap = 0;   // sequence-partitions the partial buffers hold
-};
-
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: inclusive partition prefix int32 [B], then per sequence-partition
-// the log2-sum-exp float [sp][Hkv][G] and the normalized partial output
-// float [sp][Hkv][G][D].
-WsLayout layout_for_cap(int32_t B, int32_t Hkv, int32_t G, int32_t D, int64_t sp_cap) {
+// Page columns of the stream when every sequence holds max_ctx tokens: the
+// bound the host sizes everything for.
+int64_t columns_max(int32_t B, int32_t max_ctx) { return (int64_t)B * cdiv(max_ctx, kBlockSize); }
+
+// Workspace: the range length used (int64, written by the decode kernel),
+// the inclusive page prefix int32 [B], then per work unit (range, KV head)
+// two partial slots of G rows: log2-sum-exp float [2 * units][G] and
+// normalized partial output float [2 * units][G][D].
+struct WsLayout {
+  size_t range = 0, prefix = 0, lse = 0, o = 0, total = 0;
+  int64_t ranges = 0;   // work units the slots hold
+};
+
+WsLayout layout_for(int32_t B, int32_t G, int32_t D, int64_t ranges) {
   WsLayout w;
-  w.sp_cap = sp_cap;
-  w.prefix = 0;
-  w.lse = round_up((size_t)B * 4, 256);
-  w.o = w.lse + round_up((size_t)(sp_cap * Hkv * G) * 4, 256);
-  w.total = w.o + (size_t)(sp_cap * Hkv * G * D) * 4;
+  w.ranges = ranges;
+  w.range = 0;
+  w.prefix = 256;
+  w.lse = w.prefix + round_up((size_t)B * 4, 256);
+  w.o = w.lse + round_up((size_t)(2 * ranges * G) * 4, 256);
+  w.total = w.o + (size_t)(2 * ranges * G * D) * 4;
   return w;
 }
 
-// Largest partial capacity that fits `bytes` (at least B: one partition per
-// sequence needs no partials).
-int64_t cap_for_bytes(int32_t B, int32_t Hkv, int32_t G, int32_t D, size_t bytes) {
-  const size_t per = (size_t)Hkv * G * (D + 1) * 4;
-  const size_t head = round_up((size_t)B * 4, 256) + 256;
-  int64_t s = bytes > head ? (int64_t)((bytes - head) / per) : 0;
-  while (s > B && layout_for_cap(B, Hkv, G, D, s).total > bytes) --s;
-  return s > B ? s : B;
+// Most work units whose slots fit in `bytes` (0 when not even one does).
+int64_t ranges_for_bytes(int32_t B, int32_t G, int32_t D, size_t bytes) {
+  int64_t lo = 0, hi = (int64_t)(bytes / ((size_t)2 * G * D * 4)) + 1;   // fits / does not
+  if (layout_for(B, G, D, hi).total <= bytes) return hi;
+  while (hi - lo > 1) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (layout_for(B, G, D, mid).total <= bytes) lo = mid; else hi = mid;
+  }
+  return lo;
 }
 
-// Bytes needed when every sequence may be split into partitions of P pages
-// (0 when no sequence can be split).
-size_t bytes_for_partition(int32_t B, int32_t Hkv, int32_t G, int32_t D, int32_t max_ctx,
-                           int32_t P) {
-  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
-  const int64_t parts_max = pages_max > 0 ? cdiv(pages_max, P) : 1;
-  if (parts_max <= 1 || B == 0) return 0;
-  return layout_for_cap(B, Hkv, G, D, (int64_t)B * parts_max).total;
+// Warps of a full persistent grid of one decode variant on this device (0
+// on failure).
+int64_t resident_warps(DeviceState* st, bool int8, int D, bool bf16, int32_t B, int32_t G) {
+  const size_t smem = int8 ? decode_smem_bytes_int8(D, B, G) : decode_smem_bytes_kv16(D, B, G);
+  return (int64_t)st->sms * ctas_per_sm(st, int8, D, bf16, smem) * kWarps;
 }
 
-// Partition size the default workspace is sized for: the launcher heuristic,
-// or a finer size when that still fits in 16 MiB (room for the kernel to pick
-// a better-balanced size from the exact lengths).
-int32_t workspace_partition_pages(int32_t B, int32_t Hkv, int32_t G, int32_t D, int32_t max_ctx,
-                                  int sms) {
-  const int32_t heur = auto_partition_pages(B, Hkv, max_ctx, sms);
-  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
-  if (pages_max <= 0 || B <= 0) return heur;
-  const size_t budget = (size_t)16 << 20;
-  const int64_t per_seq_part = (int64_t)Hkv * G * (D + 1) * 4;
-  const int64_t k = (int64_t)(budget - round_up((size_t)B * 4, 256) - 512) / (per_seq_part * B);
-  int64_t p_budget = k >= 1 ? cdiv(pages_max, k) : pages_max;
-  if (p_budget < 4) p_budget = 4;
-  while (p_budget < pages_max && bytes_for_partition(B, Hkv, G, D, max_ctx, (int32_t)p_budget) > budget)
-    ++p_budget;
-  return (int32_t)(p_budget < heur ? p_budget : heur);
+// Work units of the balanced split for a grid of `warps` warps: one range
+// per whole group of Hkv warps (at least one), no more ranges than the stream
+// has columns of kMinRangePages.
+int64_t balanced_units(int64_t warps, int32_t Hkv, int64_t cols_max) {
+  const int64_t groups = warps / Hkv > 0 ? warps / Hkv : 1;
+  const int64_t by_cols = cdiv(cols_max, kMinRangePages);
+  return (int64_t)Hkv * (groups < by_cols ? groups : by_cols);
+}
+
+// Units kvq_paged_decode's balanced split uses at most on this device: for
+// the full grid of whichever decode variant has the most resident warps.
+int64_t balanced_units_max(DeviceState* st, int32_t B, int32_t Hkv, int32_t G, int32_t D,
+                           int32_t max_ctx) {
+  int64_t w = 0;
+  for (bool int8 : {true, false})
+    for (bool bf : {false, true}) {
+      const int64_t x = resident_warps(st, int8, D, bf, B, G);
+      w = x > w ? x : w;
+    }
+  return balanced_units(w, Hkv, columns_max(B, max_ctx));
 }
 
 bool make_map(CUtensorMap* m, const void* base, int elem_bytes, int D, int64_t rows) {
@@ -207,39 +197,75 @@ kvq_status check_decode(const void* q, kvq_dtype dtype, int32_t B, int32_t Hq, i
   return KVQ_OK;
 }
 
+// R == 0: balanced split (or one range per segment without a workspace, or
+// when no sequence can span two pages); R >= 1: ranges of R pages.
 kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, int32_t Hq,
                          int32_t Hkv, int32_t D, const void* kc, const void* vc,
                          const uint16_t* ks, const uint16_t* vs, int32_t num_blocks,
                          int32_t bs, const int32_t* bt, int32_t max_blocks, const int32_t* cl,
                          int32_t max_ctx, float sm_scale, void* out, void* ws, size_t ws_bytes,
-                         int32_t P, cudaStream_t stream) {
+                         int32_t R, cudaStream_t stream) {
   kvq_status s = check_decode(q, dtype, B, Hq, Hkv, D, kc, vc, ks, vs, int8, num_blocks, bs, bt,
                               max_blocks, cl, max_ctx, sm_scale, out);
   if (s != KVQ_OK || B == 0) return s;
+  // the page prefix over sequences is counted in 32 bits
+  if ((int64_t)B * max_blocks > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+  if (R < 0 || R > kMaxRangePages) return KVQ_ERR_INVALID_ARGUMENT;
   DeviceState* st = device_state();
   if (!st) return cuda_fail();
   const bool bf16 = dtype == KVQ_BF16;
   const int32_t G = Hq / Hkv;
+  const size_t smem =
+      int8 ? decode_smem_bytes_int8(D, B, G) : decode_smem_bytes_kv16(D, B, G);
+  const int occ = ctas_per_sm(st, int8, D, bf16, smem);
+  if (occ <= 0) return cuda_fail();
+  const int64_t slots = (int64_t)st->sms * occ;      // CTAs of a full persistent grid
+  const int64_t cols = columns_max(B, max_ctx);
+  const int64_t pages_max = cdiv(max_ctx, kBlockSize);
+
+  DecodeParams p{};
   WsLayout wl;
-  if (P == 0) {
-    // the kernel picks the partition size within the workspace's capacity
-    // minimum: room for the launcher heuristic's partitions (the size
-    // kvq_decode_workspace_bytes recommends may allow finer ones)
-    const int32_t P_min = auto_partition_pages(B, Hkv, max_ctx, st->sms);
-    const size_t need = bytes_for_partition(B, Hkv, G, D, max_ctx, P_min);
-    if (ws_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-    const int64_t cap = (ws && cdiv(max_ctx, kBlockSize) > 1) ? cap_for_bytes(B, Hkv, G, D, ws_bytes)
-                                                              : B;
-    wl = layout_for_cap(B, Hkv, G, D, cap);
+  int64_t grid = 0;
+  if (R == 0 && (ws == nullptr || ws_bytes == 0 || pages_max <= 1)) {
+    p.R = -1;                                       // one unit per (sequence, KV head)
+    p.range_cap = 0;
+    grid = cdiv((int64_t)B * Hkv, kWarps);
+    if (grid > slots) grid = slots;
+  } else if (R == 0) {
+    // as many ranges as groups of Hkv warps of the full grid, within the
+    // workspace's slots; with fewer ranges than sequences the per-sequence
+    // split (above) keeps more warps busy
+    const int64_t cap = ranges_for_bytes(B, G, D, ws_bytes);
+    if (cap < Hkv) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t full = balanced_units(slots * kWarps, Hkv, cols) / Hkv;
+    const int64_t groups = full < cap / Hkv ? full : cap / Hkv;
+    if (groups < B && groups < full) {
+      p.R = -1;
+      p.range_cap = 0;
+      grid = cdiv((int64_t)B * Hkv, kWarps);
+    } else {
+      p.R = 0;
+      p.groups = groups;
+      p.range_cap = groups * Hkv;
+      wl = layout_for(B, G, D, p.range_cap);
+      grid = cdiv(p.range_cap, kWarps);
+    }
+    if (grid > slots) grid = slots;
   } else {
-    if (P < 1 || P > kMaxPartitionPages) return KVQ_ERR_INVALID_ARGUMENT;
-    const size_t need = bytes_for_partition(B, Hkv, G, D, max_ctx, P);
-    if (ws_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-    const int64_t pages_max = cdiv(max_ctx, kBlockSize);
-    wl = layout_for_cap(B, Hkv, G, D, need ? (int64_t)B * cdiv(pages_max, P) : B);
+    p.range_cap = cdiv(cols, R) * Hkv;
+    wl = layout_for(B, G, D, p.range_cap);
+    if (ws == nullptr || ws_bytes < wl.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+    grid = cdiv(p.range_cap, kWarps);
+    if (grid > slots) grid = slots;
+    p.R = R;
   }
-  const bool split = wl.sp_cap > B;
-  if (split && (!ws || !aligned(ws, 256))) return KVQ_ERR_INVALID_ARGUMENT;
+  if (grid < 1) grid = 1;
+  // the kernel counts columns and work units in 32 bits
+  if (cols > INT32_MAX || p.range_cap > INT32_MAX || (int64_t)B * Hkv > INT32_MAX)
+    return KVQ_ERR_UNSUPPORTED;
+  const bool split = p.R >= 0;
+  if (split && (!ws || !aligned(ws, 256) || ws_bytes < wl.total))
+    return KVQ_ERR_INVALID_ARGUMENT;
 
   CUtensorMap maps[2];
   const int64_t rows = (int64_t)num_blocks * Hkv * kBlockSize;
@@ -247,7 +273,6 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   if (!make_map(&maps[0], kc, eb, D, rows) || !make_map(&maps[1], vc, eb, D, rows))
     return cuda_fail();
 
-  DecodeParams p{};
   p.q = q;
   p.out = out;
   p.k_cache = kc;
@@ -257,6 +282,7 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   p.block_tables = bt;
   p.context_lens = cl;
   uint8_t* w = static_cast<uint8_t*>(ws);
+  p.range_out = split ? reinterpret_cast<int64_t*>(w + wl.range) : nullptr;
   p.prefix_out = split ? reinterpret_cast<int32_t*>(w + wl.prefix) : nullptr;
   p.part_lse = split ? reinterpret_cast<float*>(w + wl.lse) : nullptr;
   p.part_o = split ? reinterpret_cast<float*>(w + wl.o) : nullptr;
@@ -264,36 +290,26 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.G = Hq / Hkv;
+  p.G = G;
   p.max_blocks = max_blocks;
   p.max_ctx = max_ctx;
   p.num_blocks = num_blocks;
-  p.P = P;
-  p.sp_cap = (int32_t)(wl.sp_cap < INT32_MAX ? wl.sp_cap : INT32_MAX);
   p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
 
-  const size_t smem =
-      int8 ? decode_smem_bytes_int8(D, B, p.G) : decode_smem_bytes_kv16(D, B, p.G);
-  const int occ = ctas_per_sm(st, int8, D, bf16, smem);
-  if (occ <= 0) return cuda_fail();
-  const int64_t items_max = wl.sp_cap * Hkv;
-  if (items_max > INT32_MAX) return KVQ_ERR_UNSUPPORTED;   // the kernel counts items in 32 bits
-  const int64_t slots = (int64_t)st->sms * occ;
-  const int64_t ctas_needed = cdiv(items_max, kWarps);       // one item per warp at least
-  const int grid = (int)(ctas_needed < slots ? ctas_needed : slots);
-  cudaError_t e = int8 ? decode_launch_int8(D, bf16, maps, p, grid, smem, stream)
-                       : decode_launch_kv16(D, bf16, maps, p, grid, smem, stream);
+  cudaError_t e = int8 ? decode_launch_int8(D, bf16, maps, p, (int)grid, smem, stream)
+                       : decode_launch_kv16(D, bf16, maps, p, (int)grid, smem, stream);
   if (e != cudaSuccess) return cuda_fail();
   if (split) {
     CombineParams cp{};
     cp.part_o = p.part_o;
     cp.part_lse = p.part_lse;
     cp.prefix = p.prefix_out;
+    cp.range = p.range_out;
     cp.out = out;
     cp.B = B;
     cp.Hq = Hq;
     cp.Hkv = Hkv;
-    cp.G = p.G;
+    cp.G = G;
     if (combine_launch(D, bf16, cp, stream) != cudaSuccess) return cuda_fail();
   }
   return KVQ_OK;
@@ -447,13 +463,18 @@ kvq_status kvq_paged_decode_kv16(const void* q, kvq_dtype dtype, int32_t num_seq
 
 int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_context_len) {
-  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
-      num_q_heads % num_kv_heads)
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
+      num_q_heads % num_kv_heads || (head_dim != 64 && head_dim != 128) ||
+      num_q_heads / num_kv_heads > kMaxGroup || num_seqs > kMaxSeqs)
     return 0;
   DeviceState* st = device_state();
   if (!st) return 0;
-  return workspace_partition_pages(num_seqs, num_kv_heads, num_q_heads / num_kv_heads, head_dim,
-                                   max_context_len, st->sms);
+  const int32_t G = num_q_heads / num_kv_heads;
+  const int64_t w = resident_warps(st, true, head_dim, true, num_seqs, G);
+  if (w <= 0) return 0;
+  const int64_t groups = w / num_kv_heads > 0 ? w / num_kv_heads : 1;
+  const int64_t r = cdiv(columns_max(num_seqs, max_context_len), groups);
+  return (int32_t)(r > kMinRangePages ? (r < INT32_MAX ? r : INT32_MAX) : kMinRangePages);
 }
 
 size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
@@ -462,17 +483,25 @@ size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
       partition_pages < 1 || num_q_heads % num_kv_heads)
     return 0;
-  return bytes_for_partition(num_seqs, num_kv_heads, num_q_heads / num_kv_heads, head_dim,
-                             max_context_len, partition_pages);
+  const int32_t G = num_q_heads / num_kv_heads;
+  return layout_for(num_seqs, G, head_dim,
+                    cdiv(columns_max(num_seqs, max_context_len), partition_pages) * num_kv_heads)
+      .total;
 }
 
 size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len) {
-  const int32_t P = kvq_decode_partition_pages(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                               max_context_len);
-  if (P <= 0) return 0;
-  return kvq_decode_workspace_bytes_split(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                          max_context_len, P);
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
+      num_q_heads % num_kv_heads || (head_dim != 64 && head_dim != 128) ||
+      num_q_heads / num_kv_heads > kMaxGroup || num_seqs > kMaxSeqs)
+    return 0;
+  if (cdiv(max_context_len, kBlockSize) <= 1) return 0;   // nothing can be split
+  DeviceState* st = device_state();
+  if (!st) return 0;
+  const int32_t G = num_q_heads / num_kv_heads;
+  return layout_for(num_seqs, G, head_dim,
+                    balanced_units_max(st, num_seqs, num_kv_heads, G, head_dim, max_context_len))
+      .total;
 }
 
 kvq_status kvq_get_error(kvq_stream_t stream, uint32_t* flags) {

@@ -1,9 +1,12 @@
 // Split-K combine: merges the normalized partial outputs of a sequence's
-// partitions with their log2-sum-exp weights,
+// pieces with their log2-sum-exp weights,
 //   M = max_i lse_i,  w_i = 2^(lse_i - M) / sum_k 2^(lse_k - M),
 //   out = sum_i w_i * O_i,
 // the flash-decoding form of one softmax over all of the sequence's tokens.
-// Sequences with a single partition were written by the decode kernel.
+// The pieces of (sequence b, KV head j) are the parts of b's pages in the
+// consecutive column ranges c0..c1 that cover them: unit (c0, j) holds the
+// first piece in its slot 1, units (c0+1..c1, j) the others in slot 0.
+// Sequences inside one range were written by the decode kernel.
 #include "kvq_internal.h"
 #include "kvq_ptx.cuh"
 
@@ -11,27 +14,32 @@ namespace kvq {
 namespace {
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineBatch = 8;   // partitions a thread loads before using any
+constexpr int kCombineBatch = 8;   // pieces a thread loads before using any
 
 // One CTA per (query head, sequence).  Thread t owns 4 consecutive head dims
-// (column group t % (D/4)) of every R-th partition, R = 256 / (D/4); it loads
-// a batch of partitions at once, keeps its own running (max, sum, acc), and the
-// row groups meet in shared memory with the usual rescaling.
+// (column group t % (D/4)) of every ROWS-th piece, ROWS = 256 / (D/4); it
+// loads a batch of pieces at once, keeps its own running (max, sum, acc), and
+// the row groups meet in shared memory with the usual rescaling.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
   constexpr int COLS = D / 4;                      // float4 columns per row
-  constexpr int ROWS = kCombineThreads / COLS;     // partitions in flight per pass
+  constexpr int ROWS = kCombineThreads / COLS;     // pieces in flight per pass
   __shared__ float s_m[ROWS], s_w[ROWS];
   __shared__ float4 s_acc[ROWS][COLS];
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int col = tid % COLS, row = tid / COLS;
   griddep_wait();               // the decode grid's partials are complete and visible
-  const int sp0 = b > 0 ? p.prefix[b - 1] : 0;
-  const int n = p.prefix[b] - sp0;
-  if (n <= 1) return;
+  const int pg0 = b > 0 ? p.prefix[b - 1] : 0;
+  const int pages = p.prefix[b] - pg0;
+  const int64_t R = *p.range;
+  if (pages == 0 || R <= 0) return;
   const int j = h / p.G, g = h - j * p.G;
-  const int64_t row0 = ((int64_t)sp0 * p.Hkv + j) * p.G + g;   // partition i: + i*Hkv*G
-  const int64_t rstride = (int64_t)p.Hkv * p.G;
+  const int64_t c0 = pg0 / R, c1 = (pg0 + pages - 1) / R;   // columns [pg0, pg0 + pages)
+  const int n = (int)(c1 - c0 + 1);
+  if (n <= 1) return;
+  // piece i -> partial row (2 ((c0 + i) Hkv + j) + slot) G + g, slot 1 for i == 0
+  const int64_t row0 = (2 * (c0 * p.Hkv + j) + 1) * p.G + g;
+  const int64_t rstride = 2 * (int64_t)p.Hkv * p.G;
 
   float m = -INFINITY, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -42,7 +50,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     for (int k = 0; k < kCombineBatch; ++k) {
       const int i = i0 + k * ROWS;
       if (i < n) {
-        const int64_t r = row0 + i * rstride;
+        const int64_t r = i == 0 ? row0 : row0 - p.G + i * rstride;
         lse[k] = p.part_lse[r];
         v[k] = reinterpret_cast<const float4*>(p.part_o + r * D)[col];
       } else {

@@ -10,27 +10,32 @@
 // flash-decoding formulation of the same sum.
 //
 // Structure:
-//  * work item = (sequence, KV head, partition of P pages), processed by ONE
-//    warp; a sequence of L tokens has max(1, ceil(ceil(L/16) / P)) partitions.
-//    Every CTA rebuilds the partition prefix from context_lens in shared
-//    memory; warps then stride over the flat item list independently (no
-//    CTA-wide synchronization after start-up), so skewed context lengths need
-//    no host-side planning.
-//  * each warp keeps one continuous stream of page loads across its items:
-//    lane 0 issues, S pages ahead of the consumer, TMA copies of the
+//  * work distribution: the pages of all sequences form one column stream,
+//    cut into ranges of R pages; a unit = (range, KV head) is processed by
+//    one warp, units dealt round-robin with the KV head fastest, so that
+//    neighbouring warps read neighbouring tiles of the same blocks.  By
+//    default there are as many ranges as whole groups of Hkv warps, so every
+//    warp gets the same number of pages whatever the mix of context lengths.
+//    Inside a unit the warp walks "pieces" (the range's part of one
+//    sequence); a piece that holds its whole sequence writes the output, a
+//    partial piece writes a normalized partial + log2-sum-exp into one of the
+//    unit's two slots for the combine kernel.  Every CTA
+//    rebuilds the page prefix over sequences from context_lens in shared
+//    memory; warps then run independently (no CTA-wide synchronization after
+//    start-up) and no host-side planning is needed.
+//  * each warp keeps one continuous stream of page loads across its pieces:
+//    lanes 0..5 issue, S pages ahead of the consumer, TMA copies of the
 //    (page, KV head) K and V tiles (2-D tensor copies with the 128-/64-byte
 //    swizzle so that the ldmatrix reads are bank-conflict free) and, for INT8,
 //    the two 32-byte scale rows (1-D bulk copies), all completing on the
-//    stage's mbarrier; an item's first page also brings the item's query rows.
-//    Block ids come from the block table 32 pages at a time, the next item's
+//    stage's mbarrier; a piece's first page also brings its query rows.
+//    Block ids come from the block table 32 pages at a time, the next piece's
 //    first chunk prefetched.  Waits are bounded (error bit + exit on timeout).
 //  * QK^T and PV run on the tensor cores (mma.sync m16n8k16, FP32 accumulate)
-//    with the GQA group as the M dimension (padded to 16), so each page is
+//    with the GQA group as the N dimension (padded to 8), so each page is
 //    read once for all query heads of its KV head.  INT8 codes become exact
 //    FP16 integers with a byte permute and a subtraction; K scales multiply
 //    the FP32 scores, V scales multiply the converted V pairs.
-//  * at the end of an item the warp writes the final output (one partition)
-//    or a normalized partial + log2-sum-exp for the combine kernel.
 #pragma once
 
 #include "kvq_internal.h"
@@ -63,16 +68,6 @@ struct TileCfg {
   static constexpr int kMinCtas = INT8 ? KVQ_INT8_MIN_CTAS : 3;
 };
 
-// Partition sizes (pages per work item) the kernel chooses among when the
-// caller leaves the choice to it.
-constexpr int kNumCand = 20;
-__host__ __device__ constexpr int cand_pages(int k) {
-  return k == 0 ? 4 : k == 1 ? 5 : k == 2 ? 6 : k == 3 ? 7 : k == 4 ? 8 : k == 5 ? 10
-       : k == 6 ? 12 : k == 7 ? 14 : k == 8 ? 16 : k == 9 ? 20 : k == 10 ? 24 : k == 11 ? 28
-       : k == 12 ? 32 : k == 13 ? 40 : k == 14 ? 48 : k == 15 ? 56 : k == 16 ? 64
-       : k == 17 ? 80 : k == 18 ? 96 : 128;
-}
-
 // Byte offset inside a (K or V) tile of 16-byte chunk `c` of token row `t`,
 // with the TMA swizzle applied (16-byte chunk index XOR row bits).
 template <class C>
@@ -82,6 +77,105 @@ __device__ __forceinline__ uint32_t tile_off(int t, int c) {
   return off ^ ((off >> 3) & C::kSwzMask);
 }
 
+// ---------------------------------------------------------- work walk ---
+// The pages of all sequences form one column stream (sequence-major; prefix[]
+// is its inclusive page prefix over sequences, in shared memory); it is cut
+// into ranges of R columns, and unit u = (range u / Hkv, KV head u % Hkv)
+// goes to warp u mod (grid warps), so neighbouring warps read the same pages
+// of neighbouring KV heads at about the same time.  All counts fit in 32 bits
+// (checked on the host).  The walk state lives in shared memory and is only
+// touched once per piece, keeping the page loop's registers for the math.
+
+// CTA-wide constants of the walk.
+struct WalkConst {
+  int B, Hkv, G;
+  int R;          // columns per range (0: segment mode, a range = one sequence)
+  int T;          // columns in the stream
+  int n;          // units
+  int stride;     // warps in the grid = unit stride of a warp
+  int step_c;     // stride / Hkv
+  int step_j;     // stride % Hkv
+  int pad[3];
+};
+
+// A piece: sequence b, KV head j, pages [pg0, pg0 + npg) of the sequence's L
+// tokens, of work unit `unit`; flags bit 0: it covers the whole sequence,
+// bit 1: it begins the sequence (partial slot 1, else slot 0).  npg == 0:
+// no more pieces.
+struct Piece {
+  int b, j, pg0, npg, L, unit, flags, pad;
+};
+
+// The issuer's position: unit u = (range c, KV head j), the next column x of
+// the range (which ends at x_end) and the sequence b holding x.
+struct Cursor {
+  int u, c, j, b, x, x_end;
+};
+
+// Per warp: the issuer's cursor and the descriptors of the pieces it has
+// computed, indexed by piece ordinal mod 4 (the consumer reads piece k while
+// the issuer holds k + 1 and k + 2).
+struct WarpWalk {
+  Cursor cur;
+  int pad[2];
+  Piece ring[4];
+};
+
+// Column window of unit (k.u, k.c, k.j) and the sequence at its start (x ==
+// x_end when the unit is past the last one or, in segment mode, empty).
+__device__ __forceinline__ void unit_window(const WalkConst& w, const int* prefix, Cursor& k) {
+  if (k.u >= w.n) {
+    k.x = k.x_end = 0;
+    return;
+  }
+  if (w.R == 0) {
+    k.b = k.c;
+    k.x = k.b > 0 ? prefix[k.b - 1] : 0;
+    k.x_end = prefix[k.b];
+    return;
+  }
+  const int64_t x = (int64_t)k.c * w.R;
+  k.x = (int)x;
+  k.x_end = x + w.R < w.T ? (int)(x + w.R) : w.T;
+  int lo = 0, hi = w.B - 1;                   // first b with prefix[b] > x
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] > k.x) hi = mid; else lo = mid + 1;
+  }
+  k.b = lo;
+}
+
+// The piece at the cursor, advancing it (to the warp's following units when
+// the current one is used up).
+__device__ __forceinline__ Piece next_piece(const WalkConst& w, const int* prefix,
+                                            const int* lens, Cursor& k) {
+  Piece pc;
+  pc.npg = 0;
+  while (k.x >= k.x_end) {
+    if (k.u >= w.n) return pc;
+    k.u += w.stride;
+    k.c += w.step_c;
+    k.j += w.step_j;
+    if (k.j >= w.Hkv) {
+      k.j -= w.Hkv;
+      ++k.c;
+    }
+    unit_window(w, prefix, k);
+  }
+  while (prefix[k.b] <= k.x) ++k.b;           // skip sequences without pages
+  const int first = k.b > 0 ? prefix[k.b - 1] : 0;
+  const int pages = prefix[k.b] - first;
+  pc.b = k.b;
+  pc.j = k.j;
+  pc.pg0 = k.x - first;
+  pc.npg = min(pages - pc.pg0, k.x_end - k.x);
+  pc.L = lens[k.b];
+  pc.unit = k.c * w.Hkv + k.j;
+  pc.flags = (pc.pg0 == 0 && pc.npg == pages ? 1 : 0) | (pc.pg0 == 0 ? 2 : 0);
+  k.x += pc.npg;
+  return pc;
+}
+
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).  Per warp:
 // S page stages, one raw query slot (the TMA target, G*D*2 bytes) and a query
 // fragment buffer ([k-step][lane] pairs of the MMA B operand for the lanes
@@ -89,8 +183,8 @@ __device__ __forceinline__ uint32_t tile_off(int t, int c) {
 template <int D, bool INT8>
 struct SmemLayout {
   using C = TileCfg<D, INT8>;
-  size_t tiles, q, qfrag, scales, bars, stage_blk, misc, seq, total_bytes;
-  uint32_t q_bytes;  // one item's query rows: G * D * 2
+  size_t tiles, q, qfrag, scales, bars, stage_blk, misc, walk, seq, total_bytes;
+  uint32_t q_bytes;  // one piece's query rows: G * D * 2
   __host__ __device__ SmemLayout(int B, int G) {
     q_bytes = (uint32_t)(G * D * 2);
     tiles = 0;
@@ -99,8 +193,9 @@ struct SmemLayout {
     scales = qfrag + (size_t)kWarps * q_bytes;
     bars = (scales + (size_t)kWarps * C::kStages * C::kScaleBytes + 15) & ~(size_t)15;
     stage_blk = bars + (size_t)kWarps * C::kStages * 8;
-    misc = stage_blk + (size_t)kWarps * C::kStages * 4;   // 4 ints + reduction buffer
-    seq = (misc + 16 + (size_t)kWarps * (kNumCand + 1) * 4 + 15) & ~(size_t)15;  // prefix, lens
+    misc = stage_blk + (size_t)kWarps * C::kStages * 4;   // 4 ints (scan of warp sums)
+    walk = (misc + 16 + 15) & ~(size_t)15;                 // WalkConst, then per warp WarpWalk
+    seq = walk + sizeof(WalkConst) + (size_t)kWarps * sizeof(WarpWalk);   // page prefix, lengths
     total_bytes = seq + (size_t)B * 8 + 1024;        // + alignment slack of the base
   }
 };
@@ -109,33 +204,6 @@ template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   if constexpr (BF16) return bf2_as_u32(__floats2bfloat162_rn(a, b));
   else return h2_as_u32(__floats2half2_rn(a, b));
-}
-
-// One work item's coordinates.
-struct ItemInfo {
-  int b, j, sp, pg0, npg, nparts, L;
-};
-
-__device__ __forceinline__ ItemInfo item_info(int64_t item, const int* prefix, const int* lens,
-                                              int B, int Hkv, int P) {
-  ItemInfo it;
-  // item counts stay below 2^31 (checked on the host): 32-bit division
-  const uint32_t u = (uint32_t)item;
-  it.sp = (int)(u / (uint32_t)Hkv);
-  it.j = (int)(u - (uint32_t)it.sp * (uint32_t)Hkv);
-  int lo = 0, hi = B - 1;                       // first b with prefix[b] > sp
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] > it.sp) hi = mid; else lo = mid + 1;
-  }
-  it.b = lo;
-  const int sp0 = lo > 0 ? prefix[lo - 1] : 0;
-  it.nparts = prefix[lo] - sp0;
-  it.L = lens[lo];
-  it.pg0 = (it.sp - sp0) * P;
-  const int pages = (it.L + kBlockSize - 1) / kBlockSize;
-  it.npg = max(0, min(P, pages - it.pg0));
-  return it;
 }
 
 // INT8: QBF16 = activations are bf16 (converted to FP16 for the tensor cores);
@@ -158,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   int* stage_blk = reinterpret_cast<int*>(smem + lay.stage_blk);
   int* misc = reinterpret_cast<int*>(smem + lay.misc);
   int* prefix = reinterpret_cast<int*>(smem + lay.seq);
+  WalkConst* wconst = reinterpret_cast<WalkConst*>(smem + lay.walk);
+  WarpWalk* wwalk = reinterpret_cast<WarpWalk*>(smem + lay.walk + sizeof(WalkConst));
   int* lens = prefix + p.B;
 
   const int tid = threadIdx.x;
@@ -197,21 +267,11 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
     }
   }
 
-  // ---- clamped lengths, partition size, partition prefix over sequences ----
-  // P > 0: fixed by the caller.  P == 0: chosen here from the exact lengths,
-  // identically in every CTA: among candidate sizes whose partition count fits
-  // the workspace (p.sp_cap), the one with the lowest modelled time under the
-  // static round-robin assignment of items to warps,
-  //   cost(P) = ceil(items / warps) * (min(P, longest) + 2)   [pages],
-  // the +2 standing for the per-item overhead (query load, partial write).
-  int P = p.P;
+  // ---- clamped lengths and the inclusive page prefix over sequences ----
   {
     const int per = (B + kThreads - 1) / kThreads;   // consecutive sequences per thread
     const int b0 = tid * per, b1 = min(B, b0 + per);
-    int cnt[kNumCand];
-#pragma unroll
-    for (int k = 0; k < kNumCand; ++k) cnt[k] = 0;
-    int pmax = 0;
+    int sum = 0;
     for (int b = b0; b < b1; ++b) {
       int L = __ldg(&p.context_lens[b]);
       if (L < 0 || L > max_tok) {
@@ -219,67 +279,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
         L = L < 0 ? 0 : max_tok;
       }
       lens[b] = L;
-      const int pages = (L + kBlockSize - 1) / kBlockSize;
-      pmax = max(pmax, pages);
-      if (P == 0) {
-#pragma unroll
-        for (int k = 0; k < kNumCand; ++k) cnt[k] += max(1, (pages + cand_pages(k) - 1) / cand_pages(k));
-      }
-    }
-    if (P == 0) {
-      int* red = misc + 4;                           // [kWarps][kNumCand + 1]
-#pragma unroll
-      for (int k = 0; k < kNumCand; ++k) {
-        int v = cnt[k];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        if (lane == 0) red[warp * (kNumCand + 1) + k] = v;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) pmax = max(pmax, __shfl_xor_sync(0xFFFFFFFFu, pmax, o));
-      if (lane == 0) red[warp * (kNumCand + 1) + kNumCand] = pmax;
-      __syncthreads();
-      if (warp == 0) {
-        // lane k scores candidate k (lane kNumCand: no split); warp arg-min,
-        // ties to the larger size
-        int longest = 0;
-        for (int w = 0; w < kWarps; ++w) longest = max(longest, red[w * (kNumCand + 1) + kNumCand]);
-        const uint32_t warps = (uint32_t)gridDim.x * kWarps;
-        uint32_t cost = 0xFFFFFFFFu;
-        int cand = 0;
-        if (lane < kNumCand) {
-          // branch-free pick of this lane's size (an indexed lookup of the
-          // table would become a divergent jump or a memory access)
-#pragma unroll
-          for (int k = 0; k < kNumCand; ++k) cand = lane == k ? cand_pages(k) : cand;
-          int sp = 0;
-          for (int w = 0; w < kWarps; ++w) sp += red[w * (kNumCand + 1) + lane];
-          if (sp <= p.sp_cap && cand < longest) {
-            const uint32_t items = (uint32_t)sp * (uint32_t)Hkv;
-            cost = (items + warps - 1) / warps * (uint32_t)(cand + 2);
-          }
-        } else if (lane == kNumCand) {
-          cand = max(longest, 1);
-          cost = ((uint32_t)B * (uint32_t)Hkv + warps - 1) / warps * (uint32_t)(cand + 2);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const uint32_t oc = __shfl_xor_sync(0xFFFFFFFFu, cost, o);
-          const int op = __shfl_xor_sync(0xFFFFFFFFu, cand, o);
-          if (oc < cost || (oc == cost && op > cand)) {
-            cost = oc;
-            cand = op;
-          }
-        }
-        if (lane == 0) misc[3] = cand;
-      }
-      __syncthreads();
-      P = misc[3];
-    }
-    int sum = 0;
-    for (int b = b0; b < b1; ++b) {
-      const int pages = (lens[b] + kBlockSize - 1) / kBlockSize;
-      sum += max(1, (pages + P - 1) / P);
+      sum += (L + kBlockSize - 1) / kBlockSize;
     }
     int incl = sum;                                  // block-wide scan of per-thread sums
 #pragma unroll
@@ -287,30 +287,69 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
       const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
       if (lane >= o) incl += y;
     }
-    __syncthreads();                                 // misc[] free again
     if (lane == 31) misc[warp] = incl;
     __syncthreads();
     int run = incl - sum;
     for (int w = 0; w < warp; ++w) run += misc[w];
     for (int b = b0; b < b1; ++b) {
-      const int pages = (lens[b] + kBlockSize - 1) / kBlockSize;
-      run += max(1, (pages + P - 1) / P);
+      run += (lens[b] + kBlockSize - 1) / kBlockSize;
       prefix[b] = run;
+    }
+    // ---- constants of the work walk ----
+    if (tid == 0) {
+      WalkConst wc;
+      wc.B = B;
+      wc.Hkv = Hkv;
+      wc.G = G;
+      wc.T = 0;
+      for (int w = 0; w < kWarps; ++w) wc.T += misc[w];
+      wc.stride = (int)gridDim.x * kWarps;
+      wc.step_c = wc.stride / Hkv;
+      wc.step_j = wc.stride - wc.step_c * Hkv;
+      if (p.R < 0) {
+        wc.R = 0;                                  // one range per sequence
+        wc.n = B * Hkv;
+      } else {
+        // balanced: p.groups ranges (about one per group of Hkv warps), so
+        // that every warp gets one unit of ceil(columns / groups) pages
+        const int64_t even = ((int64_t)wc.T + p.groups - 1) / p.groups;
+        wc.R = p.R > 0 ? p.R : (int)(even > kMinRangePages ? even : kMinRangePages);
+        const int64_t n = ((int64_t)wc.T + wc.R - 1) / wc.R * Hkv;
+        if (n > p.range_cap) {
+          // the host sizes the slots for the largest stream its bound
+          // allows; refuse rather than write past them
+          atomicOr(p.err, 0x4u);
+          wc.n = 0;
+        } else {
+          wc.n = (int)n;
+        }
+      }
+      *wconst = wc;
     }
   }
   fence_mbar_init();
   __syncthreads();
-  if (blockIdx.x == 0 && p.prefix_out != nullptr)
-    for (int b = tid; b < B; b += kThreads) p.prefix_out[b] = prefix[b];
 
-  const int64_t n_items = B > 0 ? (int64_t)prefix[B - 1] * Hkv : 0;
-  const int64_t wg = (int64_t)blockIdx.x * kWarps + warp;     // this warp's first item
-  const int64_t nw = (int64_t)gridDim.x * kWarps;             // item stride
+  if (blockIdx.x == 0) {
+    if (p.prefix_out != nullptr)
+      for (int b = tid; b < B; b += kThreads) p.prefix_out[b] = prefix[b];
+    if (p.range_out != nullptr && tid == 0) *p.range_out = wconst->R;
+    // sequences without tokens are in no range: their output is zero
+    const int row16 = p.Hq * D / 8;                  // 16-byte stores per sequence
+    for (int b = tid; b < B; b += kThreads)
+      if (lens[b] == 0) {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + (int64_t)b * p.Hq * D);
+        for (int i = 0; i < row16; ++i) o[i] = make_uint4(0, 0, 0, 0);
+      }
+  }
+  const int wg = blockIdx.x * kWarps + warp;                   // this warp's first unit
 
   const uint32_t tiles_u32 = smem_u32(smem + lay.tiles) + warp * S * C::kStageBytes;
   const uint32_t q_u32 = smem_u32(smem + lay.q) + warp * lay.q_bytes;
   uint2* qfrag = reinterpret_cast<uint2*>(smem + lay.qfrag + (size_t)warp * lay.q_bytes);
-  const uint32_t qfrag_lane_u32 = smem_u32(qfrag) + 8 * lane;   // + 32 * G * ks
+  // lanes of padded heads (g >= G) read a real head's fragment: their
+  // columns of the MMAs are never used, and finite values keep them quiet
+  const uint32_t qfrag_lane_u32 = smem_u32(qfrag) + 8 * (lane % (4 * G));   // + 32 * G * ks
   const uint32_t qks = 32u * (uint32_t)G;                        // bytes per k-step
   const uint32_t scales_u32 = smem_u32(smem + lay.scales) + warp * S * C::kScaleBytes;
   const uint16_t* scales_w =
@@ -333,25 +372,26 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   const uint32_t sc_dst = scales_u32 + (lane == kTensorCopies ? 0 : kBlockSize * 2);
 
   // ---------------------------------------------------------------- issuer
-  // Warp-uniform state; lane 0 performs the copies.  The block ids of the
+  // Warp-uniform state; lanes 0..5 perform the copies.  The block ids of the
   // current 32-page chunk live one per lane (blk_cur); the first chunk of the
-  // following item is prefetched into blk_nxt.
-  int64_t is_item = wg;
+  // following piece is prefetched into blk_nxt.
   int is_ord = 0, is_pg = 0, is_chunk = 0;
-  ItemInfo nx_it{};                      // the item after the issuer's (first chunk in blk_nxt)
-  int q_issued = -1, q_consumed = -1;   // ordinals: last item whose query was copied / read
-  ItemInfo is_it{};
+  int q_issued = -1, q_consumed = -1;   // ordinals: last piece whose query was copied / read
+  WarpWalk& ww = wwalk[warp];
+  // the issuer's piece (the fields the page issue needs); the following
+  // piece's descriptor is in ww.ring and its first block-id chunk in blk_nxt
+  int is_b = 0, is_j = 0, is_pg0 = 0, is_npg = 0;
   int blk_cur = -1, blk_nxt = -1;
   uint32_t n_issued = 0, n_done = 0;
   int is_slot = 0;                       // stage the next issued page goes to
   int cs_slot = 0;                       // stage the consumer reads next
   uint32_t cs_phase = 0;                 // parity of that wait (flips each pass over the ring)
 
-  auto load_chunk = [&](const ItemInfo& it, int base) -> int {
+  auto load_chunk = [&](int b, int pg0, int npg, int base) -> int {
     const int pg = base + lane;
     int blk = -1;
-    if (pg < it.npg) {
-      blk = __ldg(&p.block_tables[(int64_t)it.b * p.max_blocks + it.pg0 + pg]);
+    if (pg < npg) {
+      blk = __ldg(&p.block_tables[(int64_t)b * p.max_blocks + pg0 + pg]);
       if (blk < 0 || blk >= p.num_blocks) {
         atomicOr(p.err, 0x2u);
         blk = -1;
@@ -359,40 +399,58 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
     }
     return blk;
   };
-  auto next_item_chunk = [&](int64_t item) -> int {
-    if (item >= n_items) {
-      nx_it.npg = 0;
-      return -1;
+  // piece `ord` of the walk into ring[ord & 3] (cursor kept in shared
+  // memory); returns its first block-id chunk
+  auto walk_next = [&](int ord) -> int {
+    Cursor k = ww.cur;
+    const Piece pc = next_piece(*wconst, prefix, lens, k);
+    __syncwarp();
+    if (lane == 0) {
+      ww.cur = k;
+      ww.ring[ord & 3] = pc;
     }
-    nx_it = item_info(item, prefix, lens, B, Hkv, P);
-    return load_chunk(nx_it, 0);
+    __syncwarp();
+    return load_chunk(pc.b, pc.pg0, pc.npg, 0);
   };
-  if (is_item < n_items) {
-    is_it = item_info(is_item, prefix, lens, B, Hkv, P);
-    blk_cur = load_chunk(is_it, 0);
-    blk_nxt = next_item_chunk(is_item + nw);
+  {
+    const WalkConst& wc = *wconst;
+    Cursor k;
+    k.u = wg;
+    k.c = wg / Hkv;
+    k.j = wg - k.c * Hkv;
+    unit_window(wc, prefix, k);
+    if (lane == 0) ww.cur = k;
+    __syncwarp();
+    blk_cur = walk_next(0);
+    const Piece& p0 = ww.ring[0];
+    is_b = p0.b;
+    is_j = p0.j;
+    is_pg0 = p0.pg0;
+    is_npg = p0.npg;
+    if (is_npg > 0) blk_nxt = walk_next(1);
   }
 
-  // Issue pages while fewer than S are in flight; an item's first page (which
-  // also copies the item's query rows into the single raw query slot) waits
+  // Issue pages while fewer than S are in flight; a piece's first page (which
+  // also copies the piece's query rows into the single raw query slot) waits
   // until the previously copied query rows have been read by the consumer.
   auto refill = [&]() {
     while (n_issued - n_done < (uint32_t)S) {
-      while (is_item < n_items && is_pg >= is_it.npg) {   // next item with pages
-        is_item += nw;
+      if (is_npg > 0 && is_pg >= is_npg) {   // next piece (pieces have pages)
         ++is_ord;
+        const Piece& nx = ww.ring[is_ord & 3];
+        is_b = nx.b;
+        is_j = nx.j;
+        is_pg0 = nx.pg0;
+        is_npg = nx.npg;
         is_pg = 0;
         is_chunk = 0;
-        if (is_item < n_items) {
-          is_it = item_info(is_item, prefix, lens, B, Hkv, P);
-          blk_cur = blk_nxt;
-          blk_nxt = next_item_chunk(is_item + nw);
-        }
+        blk_cur = blk_nxt;
+        if (is_npg > 0) blk_nxt = walk_next(is_ord + 1);
       }
-      if (is_item >= n_items || (is_pg == 0 && q_issued > q_consumed)) return;
+      if (is_npg == 0 || (is_pg == 0 && q_issued > q_consumed)) return;
       if (is_pg >= is_chunk + 32) {
         is_chunk += 32;
-        blk_cur = load_chunk(is_it, is_chunk);
+        blk_cur = load_chunk(is_b, is_pg0, is_npg, is_chunk);
       }
       const int blk = __shfl_sync(0xFFFFFFFFu, blk_cur, is_pg - is_chunk);
       const int s = is_slot;
@@ -406,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
         else mbar_arrive(bar);
       }
       if (blk >= 0) {
-        const int row = blk * Hkv + is_it.j;          // (block, KV head) tile index
+        const int row = blk * Hkv + is_j;             // (block, KV head) tile index
         if (lane < kTensorCopies) {
           tma_load_2d(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * kBlockSize, bar);
         } else if (INT8 && lane < kTensorCopies + 2) {
@@ -416,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
       }
       if (qbytes && lane == 4) {
         const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) +
-                               ((int64_t)is_it.b * p.Hq + (int64_t)is_it.j * G) * D;
+                               ((int64_t)is_b * p.Hq + (int64_t)is_j * G) * D;
         bulk_load(q_u32, qsrc, qbytes, bar);
       }
       if (is_pg == 0) q_issued = is_ord;
@@ -429,8 +487,11 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   // -------------------------------------------------------------- consumer
   int ord = 0;
   bool aborted = false;
-  for (int64_t item = wg; item < n_items && !aborted; item += nw, ++ord) {
-    const ItemInfo it = item_info(item, prefix, lens, B, Hkv, P);
+  for (;; ++ord) {
+    // the issuer computed this piece's descriptor before issuing its pages
+    const int it_npg = ww.ring[ord & 3].npg;
+    if (it_npg == 0) break;
+    const int it_pg0 = ww.ring[ord & 3].pg0, it_L = ww.ring[ord & 3].L;
     // Running softmax state of the two query heads this thread's columns hold
     // (heads 2c and 2c+1 of the KV head's group), and the output accumulator
     // O^T[d][head]: o[4cb + e] for 16-wide head-dim block cb, e = (row, col)
@@ -442,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
     for (int i = 0; i < NOUT; ++i) o[i] = 0.f;
     const bool has_head = g < G;   // this lane provides a real query column
 
-    for (int pg = 0; pg < it.npg; ++pg) {
+    for (int pg = 0; pg < it_npg; ++pg) {
       const int s = cs_slot;
       const uint32_t par = cs_phase;
       if (++cs_slot == S) {
@@ -481,13 +542,14 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
             qfrag[ks * 4 * G + lane] = f;
           }
         }
+        __syncwarp();   // padded lanes read fragments written by other lanes
         q_consumed = ord;
       }
       const int blk = blk_w[s];
       if (blk >= 0) {
         const uint32_t kt = tiles_u32 + s * C::kStageBytes;
         const uint32_t vt = kt + C::kTile;
-        const int nvalid = min(kBlockSize, it.L - (it.pg0 + pg) * kBlockSize);
+        const int nvalid = min(kBlockSize, it_L - (it_pg0 + pg) * kBlockSize);
         // ldmatrix row address: matrices (tokens 0-7, chunk 2i), (8-15, 2i),
         // (0-7, 2i+1), (8-15, 2i+1) for lanes 0-7, 8-15, 16-23, 24-31
         const int lt = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -499,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
         for (int kk = 0; kk < (INT8 ? KSTEPS / 2 : 0); ++kk) {
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kt + tile_off<C>(lt, 2 * kk + (lane >> 4)), r0, r1, r2, r3);
-          const uint2 qa = lds_u2_if(has_head, qfrag_lane_u32 + qks * (2 * kk));
-          const uint2 qb = lds_u2_if(has_head, qfrag_lane_u32 + qks * (2 * kk + 1));
+          const uint2 qa = lds_u2(qfrag_lane_u32 + qks * (2 * kk));
+          const uint2 qb = lds_u2(qfrag_lane_u32 + qks * (2 * kk + 1));
           if constexpr (INT8) {
             // r0/r1: tokens g / g+8, head-dim 16(2kk)+4c+{0..3}; r2/r3: next chunk
             uint32_t a0, a2, a1, a3;
@@ -519,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
           for (int ks = 0; ks < KSTEPS; ++ks) {
             uint32_t r0, r1, r2, r3;
             ldsm_x4(kt + tile_off<C>(lt, 2 * ks + (lane >> 4)), r0, r1, r2, r3);
-            const uint2 qa = lds_u2_if(has_head, qfrag_lane_u32 + qks * ks);
+            const uint2 qa = lds_u2(qfrag_lane_u32 + qks * ks);
             // a0: token g, d 16ks+2c..; a1: token g+8; a2: token g, d 16ks+8+2c..; a3: g+8
             if (ks & 1) mma_16816_acc<MMA_BF16>(sb, r0, r1, r2, r3, qa.x, qa.y);
             else mma_16816_acc<MMA_BF16>(sa, r0, r1, r2, r3, qa.x, qa.y);
@@ -613,7 +675,8 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
     }
     if (aborted) break;
 
-    // ---- finalize the item: this warp holds the whole partition ----
+    // ---- finalize the piece: the whole sequence, or a partial for the combine ----
+    const Piece it = ww.ring[ord & 3];
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
@@ -627,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
       const float m = hh ? m1 : m0;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t hrow = (int64_t)it.b * p.Hq + (int64_t)it.j * G + head;
-      if (it.nparts == 1) {
+      if (it.flags & 1) {
         uint16_t* dst = static_cast<uint16_t*>(p.out) + hrow * D;
 #pragma unroll
         for (int cb = 0; cb < D / 16; ++cb) {
@@ -641,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
           }
         }
       } else {
-        const int64_t prow = ((int64_t)it.sp * Hkv + it.j) * G + head;
+        const int64_t prow = (2 * (int64_t)it.unit + (it.flags >> 1)) * G + head;
         float* dst = p.part_o + prow * D;
 #pragma unroll
         for (int cb = 0; cb < D / 16; ++cb) {

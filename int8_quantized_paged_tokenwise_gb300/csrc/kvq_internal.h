@@ -30,32 +30,47 @@ struct QuantParams {
   unsigned int* err;
 };
 
+// Work distribution of the decode: the pages of all sequences form one
+// column stream (sequence-major), cut into ranges of R columns; work unit
+// u = (range u / Hkv, KV head u % Hkv) goes to warp u mod (warps in the
+// grid).  The part of a range inside one sequence is a "piece": a piece
+// covering the whole sequence writes the output directly; otherwise it writes
+// a normalized partial and its log2-sum-exp into one of the unit's two
+// partial slots (slot 0: the piece continues a sequence begun in an earlier
+// range; slot 1: the piece begins a sequence that continues in a later
+// range), which the combine kernel merges.
+constexpr int kMinRangePages = 4;   // shortest range of the balanced split
+
 struct DecodeParams {
   const void* q;
   void* out;
-  const void* k_cache;      // payload base pointers (L2 prefetch addresses)
+  const void* k_cache;      // payload base pointers
   const void* v_cache;
   const uint16_t* k_scale;  // INT8 path only
   const uint16_t* v_scale;
   const int32_t* block_tables;
   const int32_t* context_lens;
-  float* part_o;            // [sp][Hkv][G][D]
-  float* part_lse;          // [sp][Hkv][G]   (log2 domain)
-  int32_t* prefix_out;      // [B] inclusive partition prefix, written by CTA 0
+  float* part_o;            // [2 * range_cap][G][D]   (unit u, slot k -> rows (2u + k) * G)
+  float* part_lse;          // [2 * range_cap][G]      (log2 domain)
+  int32_t* prefix_out;      // [B] inclusive page prefix over sequences, written by CTA 0
+  int64_t* range_out;       // the range length used, written by CTA 0
   unsigned int* err;
   int32_t B, Hq, Hkv, G;
   int32_t max_blocks;       // block-table row length
   int32_t max_ctx;          // host upper bound on context_lens
   int32_t num_blocks;
-  int32_t P;                // pages per partition (one warp's work item); 0 = kernel picks
-  int32_t sp_cap;           // sequence-partitions the workspace holds (>= B)
+  int32_t R;                // > 0: pages per range; 0: balanced (ceil(columns / groups), at
+                            // least kMinRangePages); < 0: one unit per (sequence, KV head)
+  int64_t groups;           // R == 0: ranges of the balanced split (>= 1)
+  int64_t range_cap;        // work units the partial slots hold (0 when R < 0)
   float scale_log2;         // sm_scale * log2(e)
 };
 
 struct CombineParams {
   const float* part_o;
   const float* part_lse;
-  const int32_t* prefix;
+  const int32_t* prefix;    // inclusive page prefix (from the decode kernel)
+  const int64_t* range;     // range length (from the decode kernel)
   void* out;
   int32_t B, Hq, Hkv, G;
 };

@@ -135,20 +135,6 @@ __device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
   return v;
 }
 
-// lds_u2 when `pred` holds, zeros otherwise (no access when it does not).
-__device__ __forceinline__ uint2 lds_u2_if(bool pred, uint32_t addr) {
-  uint2 v;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %3, 0;\n\t"
-      "mov.b32 %0, 0;\n\t"
-      "mov.b32 %1, 0;\n\t"
-      "@p ld.shared.v2.u32 {%0, %1}, [%2];\n\t}"
-      : "=r"(v.x), "=r"(v.y)
-      : "r"(addr), "r"((uint32_t)pred));
-  return v;
-}
-
 // ------------------------------------------------------------ ldmatrix ---
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {

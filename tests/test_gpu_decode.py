@@ -275,3 +275,26 @@ def test_decode_on_side_stream_and_graph_capture():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_decode_without_workspace_and_with_a_small_one():
+    """An empty workspace runs one warp per (sequence, KV head) with no split;
+    a workspace for only a few work ranges lowers the warp count (long
+    ranges, many pieces per range).  Both match the oracle."""
+    w = W.custom(len(RAGGED), 16, 4, 128, "bf16", RAGGED, seed=31)
+    case = Case(w)
+    case.write_prefix()
+    none = torch.empty(0, dtype=torch.uint8, device="cuda")
+    out = kvq.kvq_paged_decode(case.q, *case.int8, case.bt, case.cl, w.max_context_len,
+                               w.sm_scale, workspace=none)
+    _check_all(case, out, what="no workspace")
+    assert bool((out[0] == 0).all())
+    for ranges_pages in (w.max_context_len, 64):
+        # bytes for ceil(tiles / ranges_pages) ranges: a handful of ranges
+        nbytes = kvq.kvq_decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                w.head_dim, w.max_context_len, ranges_pages)
+        small = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        out = kvq.kvq_paged_decode(case.q, *case.int8, case.bt, case.cl, w.max_context_len,
+                                   w.sm_scale, workspace=small)
+        _check_all(case, out, what=f"small workspace ({nbytes} B)")
+    assert kvq.kvq_get_error() == (0, 0)
