@@ -94,22 +94,20 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // bound the host sizes everything for.
 int64_t columns_max(int32_t B, int32_t max_ctx) { return (int64_t)B * cdiv(max_ctx, kBlockSize); }
 
-// Workspace: the range length used (int64, written by the decode kernel),
-// the inclusive page prefix int32 [B], then per work unit (range, KV head)
-// two partial slots of G rows: log2-sum-exp float [2 * units][G] and
-// normalized partial output float [2 * units][G][D].
+// Workspace: per work unit (range, KV head) two partial slots of G rows:
+// log2-sum-exp float [2 * units][G], then normalized partial output float
+// [2 * units][G][D].
 struct WsLayout {
-  size_t range = 0, prefix = 0, lse = 0, o = 0, total = 0;
+  size_t lse = 0, o = 0, total = 0;
   int64_t ranges = 0;   // work units the slots hold
 };
 
 WsLayout layout_for(int32_t B, int32_t G, int32_t D, int64_t ranges) {
+  (void)B;
   WsLayout w;
   w.ranges = ranges;
-  w.range = 0;
-  w.prefix = 256;
-  w.lse = w.prefix + round_up((size_t)B * 4, 256);
-  w.o = w.lse + round_up((size_t)(2 * ranges * G) * 4, 256);
+  w.lse = 0;
+  w.o = round_up((size_t)(2 * ranges * G) * 4, 256);
   w.total = w.o + (size_t)(2 * ranges * G * D) * 4;
   return w;
 }
@@ -208,8 +206,9 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   kvq_status s = check_decode(q, dtype, B, Hq, Hkv, D, kc, vc, ks, vs, int8, num_blocks, bs, bt,
                               max_blocks, cl, max_ctx, sm_scale, out);
   if (s != KVQ_OK || B == 0) return s;
-  // the page prefix over sequences is counted in 32 bits
-  if ((int64_t)B * max_blocks > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+  // the page prefix over sequences and token counts are 32-bit in the kernels
+  if ((int64_t)B * max_blocks > INT32_MAX || max_blocks > INT32_MAX / kBlockSize)
+    return KVQ_ERR_UNSUPPORTED;
   if (R < 0 || R > kMaxRangePages) return KVQ_ERR_INVALID_ARGUMENT;
   DeviceState* st = device_state();
   if (!st) return cuda_fail();
@@ -282,8 +281,6 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   p.block_tables = bt;
   p.context_lens = cl;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  p.range_out = split ? reinterpret_cast<int64_t*>(w + wl.range) : nullptr;
-  p.prefix_out = split ? reinterpret_cast<int32_t*>(w + wl.prefix) : nullptr;
   p.part_lse = split ? reinterpret_cast<float*>(w + wl.lse) : nullptr;
   p.part_o = split ? reinterpret_cast<float*>(w + wl.o) : nullptr;
   p.err = st->err;
@@ -303,14 +300,19 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
     CombineParams cp{};
     cp.part_o = p.part_o;
     cp.part_lse = p.part_lse;
-    cp.prefix = p.prefix_out;
-    cp.range = p.range_out;
+    cp.context_lens = cl;
     cp.out = out;
     cp.B = B;
     cp.Hq = Hq;
     cp.Hkv = Hkv;
     cp.G = G;
-    if (combine_launch(D, bf16, cp, stream) != cudaSuccess) return cuda_fail();
+    cp.max_tok = max_blocks * kBlockSize < max_ctx ? max_blocks * kBlockSize : max_ctx;
+    cp.R = p.R;
+    cp.groups = p.groups;
+    // few pairs: their sequences are long and split into many pieces, so a
+    // whole CTA per pair shortens the dependent loads
+    cp.per_cta = (int64_t)B * Hq <= 2 * (int64_t)st->sms ? 1 : 0;
+    if (combine_launch(D, bf16, cp, st->sms, stream) != cudaSuccess) return cuda_fail();
   }
   return KVQ_OK;
 }

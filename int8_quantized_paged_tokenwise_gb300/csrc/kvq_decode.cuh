@@ -243,12 +243,13 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
     prefetch_tensormap(&tmV);
   }
   if (tid < kWarps * S) mbar_init(smem_u32(&bars[tid]), 1);
-  // Programmatic dependent launch: let the combine kernel be scheduled as this
-  // grid drains, and wait here until the previous kernel in the stream (e.g.
-  // the quantize-append that wrote the newest tokens) has completed and its
-  // writes are visible, before reading any input.
-  griddep_launch_dependents();
+  // Programmatic dependent launch: wait here until the previous kernel in the
+  // stream (e.g. the quantize-append that wrote the newest tokens) has
+  // completed and its writes are visible, before reading any input; then let
+  // the combine kernel be scheduled (it reads context_lens before waiting for
+  // this grid).
   griddep_wait();
+  griddep_launch_dependents();
   // Warm L2 with the small inputs every warp reads first (block tables and
   // query rows): CTA i prefetches the i-th 4 KB slice of each.
   if (tid == 0) {
@@ -331,9 +332,6 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
   __syncthreads();
 
   if (blockIdx.x == 0) {
-    if (p.prefix_out != nullptr)
-      for (int b = tid; b < B; b += kThreads) p.prefix_out[b] = prefix[b];
-    if (p.range_out != nullptr && tid == 0) *p.range_out = wconst->R;
     // sequences without tokens are in no range: their output is zero
     const int row16 = p.Hq * D / 8;                  // 16-byte stores per sequence
     for (int b = tid; b < B; b += kThreads)

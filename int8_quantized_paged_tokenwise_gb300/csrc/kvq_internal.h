@@ -52,8 +52,6 @@ struct DecodeParams {
   const int32_t* context_lens;
   float* part_o;            // [2 * range_cap][G][D]   (unit u, slot k -> rows (2u + k) * G)
   float* part_lse;          // [2 * range_cap][G]      (log2 domain)
-  int32_t* prefix_out;      // [B] inclusive page prefix over sequences, written by CTA 0
-  int64_t* range_out;       // the range length used, written by CTA 0
   unsigned int* err;
   int32_t B, Hq, Hkv, G;
   int32_t max_blocks;       // block-table row length
@@ -69,10 +67,13 @@ struct DecodeParams {
 struct CombineParams {
   const float* part_o;
   const float* part_lse;
-  const int32_t* prefix;    // inclusive page prefix (from the decode kernel)
-  const int64_t* range;     // range length (from the decode kernel)
+  const int32_t* context_lens;
   void* out;
   int32_t B, Hq, Hkv, G;
+  int32_t max_tok;          // the decode kernel's clamp of context_lens
+  int32_t R;                // as DecodeParams::R (>= 0)
+  int64_t groups;           // as DecodeParams::groups
+  int32_t per_cta;          // 1: one CTA per (sequence, query head), else one warp
 };
 
 // decode (kvq_decode_int8.cu / kvq_decode_kv16.cu); D = head_dim, smem in bytes; maps =
@@ -89,7 +90,7 @@ cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* maps,
                                const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
 
 // combine (kvq_combine.cu)
-cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, cudaStream_t s);
+cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, int sms, cudaStream_t s);
 
 // quantize-append and twin append (kvq_quant.cu)
 cudaError_t quantize_append_launch(int D, bool bf16, const QuantParams& p, cudaStream_t s);
