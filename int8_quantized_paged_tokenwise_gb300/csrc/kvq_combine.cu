@@ -15,7 +15,7 @@ namespace {
 
 constexpr int kCombineWarps = 8;
 constexpr int kCombineThreads = kCombineWarps * 32;
-constexpr int kCombineBatch = 8;   // pieces a lane loads before using any
+constexpr int kCombineBatch = 16;  // pieces a lane loads before using any
 
 // Every CTA first rebuilds, from context_lens, the page prefix and range
 // length the decode kernel used (this overlaps the decode's tail: the launch
