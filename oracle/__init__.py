@@ -69,6 +69,8 @@ def lib():
         L.orc_quantize_row.argtypes = [vp, i32, i32, u16, vp]; L.orc_quantize_row.restype = None
         L.orc_dequant.argtypes = [ctypes.c_int8, u16]; L.orc_dequant.restype = f64
         L.orc_quantize_rows.argtypes = [vp, i64, i32, i32, vp, vp]; L.orc_quantize_rows.restype = None
+        L.orc_dequantize_rows.argtypes = [vp, vp, i64, i32, i32, vp]
+        L.orc_dequantize_rows.restype = None
         L.orc_quantize_append.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp,
                                           vp, vp, vp, vp, i64, i32]
         L.orc_quantize_append.restype = i64
@@ -144,6 +146,19 @@ def quantize_rows(x_bits: np.ndarray, dtype: str):
     s = np.empty(x.shape[:-1], dtype=np.uint16)
     lib().orc_quantize_rows(_p(x), N, D, _is_bf16(dtype), _p(q), _p(s))
     return q, s
+
+
+def dequantize_rows(codes: np.ndarray, scales: np.ndarray, dtype: str) -> np.ndarray:
+    """Codes [..., D] int8 times their row's FP16 scale [...], rounded (RNE)
+    to ``dtype``: the dequantize-window baseline ("fix(cuda/kv): correct Int8
+    KV per-token scale ..." (mlxcel PR #717), "The Int8 bug and fix")."""
+    c = np.ascontiguousarray(codes, dtype=np.int8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint16).reshape(-1)
+    D = c.shape[-1]
+    assert c.size == sc.size * D
+    out = np.empty(c.shape, dtype=np.uint16)
+    lib().orc_dequantize_rows(_p(c), _p(sc), sc.size, D, _is_bf16(dtype), _p(out))
+    return out
 
 
 def quantize_append(k_bits, v_bits, dtype, slot_mapping, k_cache, v_cache, k_scale, v_scale,

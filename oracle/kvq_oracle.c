@@ -170,6 +170,17 @@ double orc_dequant(int8_t q, uint16_t scale_bits) {
   return orc_fp16_to_double(scale_bits) * (double)q;
 }
 
+/* Dequantize-window baseline ([ML] "The Int8 bug and fix": its CUDA path
+ * dequantizes the whole cached window to the activation dtype, then runs
+ * SDPA): every code times its row's scale, rounded once (round to nearest
+ * even) to the dtype.  codes [N][D], scales [N] -> out [N][D] dtype bits. */
+void orc_dequantize_rows(const int8_t* q, const uint16_t* scales, int64_t N, int D,
+                         int is_bf16, uint16_t* out) {
+  for (int64_t n = 0; n < N; ++n)
+    for (int d = 0; d < D; ++d)
+      out[n * D + d] = orc_from_double_rne(orc_dequant(q[n * D + d], scales[n]), is_bf16);
+}
+
 /* Quantize rows [N][D] into codes [N][D] and scales [N]. */
 void orc_quantize_rows(const uint16_t* x, int64_t N, int D, int is_bf16,
                        int8_t* q, uint16_t* scales) {

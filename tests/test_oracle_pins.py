@@ -320,3 +320,28 @@ def test_sampled_heads_match_full_decode():
     full, fb = oracle.decode_sequence(q, k, v, "bf16", w.sm_scale)
     part, pb = oracle.decode_sequence(q, k, v, "bf16", w.sm_scale, heads=[7, 0, 5])
     assert np.array_equal(part, full[[7, 0, 5]]) and np.array_equal(pb, fb[[7, 0, 5]])
+
+
+def test_dequantize_rows_vs_library_rounding():
+    """Dequantize-window baseline: code * scale rounded once to the dtype,
+    against numpy's float16 and torch's bfloat16 conversions of the exact
+    product (both round to nearest even), including overflow to inf and the
+    signs of zero."""
+    r = np.random.default_rng(11)
+    N, D = 64, 32
+    codes = r.integers(-127, 128, size=(N, D)).astype(np.int8)
+    codes[0, :4] = [0, 127, -127, 1]
+    scales = r.integers(0x0001, 0x7C00, size=N).astype(np.uint16)   # finite positive fp16
+    scales[:3] = [0x7BFF, 0x0001, 0x3C00]                          # 65504, min subnormal, 1
+    exact = codes.astype(np.float64) * np.array(
+        [oracle.fp16_to_double(int(s)) for s in scales])[:, None]
+    got16 = oracle.dequantize_rows(codes, scales, "fp16")
+    with np.errstate(over="ignore"):                              # 127 * 65504 overflows
+        want16 = exact.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got16, want16)
+    assert got16[0, 1] == 0x7C00 and got16[0, 2] == 0xFC00          # 127 * 65504 -> +-inf
+    gotbf = oracle.dequantize_rows(codes, scales, "bf16")
+    wantbf = torch.from_numpy(exact).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(gotbf, wantbf)
+    # a wrong row/scale pairing (transposed operand) must not pass: scales differ by row
+    assert not np.array_equal(oracle.dequantize_rows(codes, scales[::-1].copy(), "fp16"), want16)
