@@ -226,6 +226,33 @@ kvq_status kvq_cache_append_kv16(const void* k, const void* v, int64_t k_token_s
                                  int32_t num_blocks, int32_t block_size, kvq_stream_t stream);
 
 /*
+ * kvq_dequantize_window -- the dequantize-window baseline: for every page of
+ * every sequence (pages 0 .. ceil(context_lens[b]/16)-1 through the block
+ * table), write s[t] * code[t][d] rounded (nearest even) to `dtype` into a
+ * 16-bit cache of the same [num_blocks][num_kv_heads][16][D] layout, K and V.
+ * Defined by [ML] "The Int8 bug and fix" (its CUDA path dequantizes the
+ * whole window, then runs attention over FP16); followed by
+ * kvq_paged_decode_kv16 on k_out/v_out it is that path, the comparison the
+ * fused kvq_paged_decode is measured against.
+ *
+ *   k_cache, v_cache, k_scale, v_scale   the INT8 cache (as kvq_paged_decode).
+ *   k_out, v_out     device, 16-byte aligned, [num_blocks][num_kv_heads][16][D]
+ *                    of `dtype`; only the pages the sequences reach are
+ *                    written (all 16 rows of each).
+ *   block_tables, context_lens, max_context_len   as kvq_paged_decode.
+ * Device errors: block id out of range (page skipped, KVQ_DEVERR_BLOCK),
+ * context above max_context_len (clamped, KVQ_DEVERR_CONTEXT).
+ */
+kvq_status kvq_dequantize_window(const int8_t* k_cache, const int8_t* v_cache,
+                                 const uint16_t* k_scale, const uint16_t* v_scale,
+                                 int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                 int32_t head_dim, const int32_t* block_tables,
+                                 int32_t num_seqs, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, int32_t max_context_len,
+                                 kvq_dtype dtype, void* k_out, void* v_out,
+                                 kvq_stream_t stream);
+
+/*
  * kvq_paged_decode_noalloc -- kvq_paged_decode for callers that cannot
  * allocate device memory.  The pages have no counterpart of this call; it
  * exists for hosts that own all device memory through their own pool

@@ -28,7 +28,8 @@ from . import _build
 
 __all__ = [
     "KvqError", "load", "kvq_quantize_append", "kvq_paged_decode", "kvq_paged_decode_kv16",
-    "kvq_cache_append_kv16", "kvq_paged_decode_noalloc", "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
+    "kvq_cache_append_kv16", "kvq_paged_decode_noalloc", "kvq_dequantize_window",
+    "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
     "kvq_get_error", "kvq_status_string", "alloc_int8_cache", "alloc_kv16_cache",
     "HEADER_SYMBOLS", "BLOCK_SIZE", "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_CONTEXT",
     "DEVERR_TIMEOUT",
@@ -47,6 +48,7 @@ HEADER_SYMBOLS = (
     "kvq_decode_partition_pages", "kvq_paged_decode_split", "kvq_decode_workspace_bytes_split",
     "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split", "kvq_cache_append_kv16",
     "kvq_get_error", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
+    "kvq_dequantize_window",
 )
 
 _lib = None
@@ -84,8 +86,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     dec16 = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz]
     L.kvq_paged_decode_kv16.argtypes = dec16 + [vp]
     L.kvq_paged_decode_kv16_split.argtypes = dec16 + [i32, vp]
+    L.kvq_dequantize_window.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, i32, vp,
+                                        i32, i32, vp, vp, vp]
     for fn in ("kvq_quantize_append", "kvq_cache_append_kv16", "kvq_paged_decode",
-               "kvq_paged_decode_split", "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split"):
+               "kvq_paged_decode_split", "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split",
+               "kvq_dequantize_window"):
         getattr(L, fn).restype = ctypes.c_int
     L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.kvq_decode_workspace_bytes.restype = sz
@@ -310,6 +315,35 @@ def kvq_paged_decode_kv16(q, k_cache, v_cache, block_tables, context_lens, max_c
         st = L.kvq_paged_decode_kv16(*args, _stream(stream))
     _check(st, "kvq_paged_decode_kv16")
     return out
+
+
+def kvq_dequantize_window(k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                          max_context_len: int, dtype, k_out=None, v_out=None, stream=None):
+    """Dequantize-window baseline: writes s * code, rounded to ``dtype``
+    (torch.float16 / torch.bfloat16), for every page the sequences reach into
+    a 16-bit cache of the INT8 cache's layout; returns (k_out, v_out)."""
+    L = load()
+    NB, Hkv, bs, D = k_cache.shape
+    _check_cache(k_cache, v_cache, Hkv, D, (torch.int8,))
+    _check_scales(k_scale, v_scale, k_cache)
+    _need(dtype in (torch.float16, torch.bfloat16), "dtype must be float16 or bfloat16")
+    B = context_lens.shape[0]
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+          and block_tables.shape[0] == B and block_tables.is_contiguous(),
+          "block_tables must be contiguous int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous(),
+          "context_lens must be int32 [B]")
+    if k_out is None:
+        k_out, v_out = alloc_kv16_cache(NB, Hkv, D, dtype, k_cache.device)
+    _check_cache(k_out, v_out, Hkv, D, (dtype,))
+    _need(k_out.shape == k_cache.shape, "k_out/v_out must have the INT8 cache's shape")
+    st = L.kvq_dequantize_window(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), NB,
+                                 bs, Hkv, D, _ptr(block_tables), B, block_tables.shape[1],
+                                 _ptr(context_lens), int(max_context_len),
+                                 BF16 if dtype == torch.bfloat16 else FP16, _ptr(k_out),
+                                 _ptr(v_out), _stream(stream))
+    _check(st, "kvq_dequantize_window")
+    return k_out, v_out
 
 
 def kvq_get_error(stream=None):

@@ -463,6 +463,56 @@ kvq_status kvq_paged_decode_kv16(const void* q, kvq_dtype dtype, int32_t num_seq
                        workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
+kvq_status kvq_dequantize_window(const int8_t* k_cache, const int8_t* v_cache,
+                                 const uint16_t* k_scale, const uint16_t* v_scale,
+                                 int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                 int32_t head_dim, const int32_t* block_tables,
+                                 int32_t num_seqs, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, int32_t max_context_len,
+                                 kvq_dtype dtype, void* k_out, void* v_out,
+                                 kvq_stream_t stream) {
+  if (dtype != KVQ_FP16 && dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_context_len < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (block_size != kBlockSize) return KVQ_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (num_seqs > kMaxSeqs || (int64_t)num_blocks * num_kv_heads * kBlockSize > INT32_MAX)
+    return KVQ_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return KVQ_OK;
+  if (max_blocks_per_seq <= 0 || max_blocks_per_seq > INT32_MAX / kBlockSize ||
+      (int64_t)max_context_len > (int64_t)max_blocks_per_seq * kBlockSize)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !context_lens || !k_out ||
+      !v_out)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_out, 16) ||
+      !aligned(v_out, 16) || !aligned(k_scale, 2) || !aligned(v_scale, 2) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  DeviceState* st = device_state();
+  if (!st) return cuda_fail();
+  DequantParams p{};
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.k_out = k_out;
+  p.v_out = v_out;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.err = st->err;
+  p.B = num_seqs;
+  p.Hkv = num_kv_heads;
+  p.max_blocks = max_blocks_per_seq;
+  p.max_tok = max_context_len;
+  p.num_blocks = num_blocks;
+  const int max_pages = (int)cdiv(max_context_len, kBlockSize);
+  if (dequant_window_launch(head_dim, dtype == KVQ_BF16, p, max_pages,
+                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return KVQ_OK;
+}
+
 int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_context_len) {
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||

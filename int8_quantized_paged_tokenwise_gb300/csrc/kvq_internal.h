@@ -76,6 +76,19 @@ struct CombineParams {
   int32_t per_cta;          // 1: one CTA per (sequence, query head), else one warp
 };
 
+struct DequantParams {
+  const int8_t* k_cache;
+  const int8_t* v_cache;
+  const uint16_t* k_scale;
+  const uint16_t* v_scale;
+  void* k_out;              // 16-bit cache, same [NB][Hkv][16][D] layout
+  void* v_out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  unsigned int* err;
+  int32_t B, Hkv, max_blocks, max_tok, num_blocks;
+};
+
 // decode (kvq_decode_int8.cu / kvq_decode_kv16.cu); D = head_dim, smem in bytes; maps =
 // {K tiles, V tiles}.
 size_t decode_smem_bytes_int8(int D, int B, int G);
@@ -91,6 +104,10 @@ cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* maps,
 
 // combine (kvq_combine.cu)
 cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, int sms, cudaStream_t s);
+
+// dequantize-window baseline (kvq_dequant.cu)
+cudaError_t dequant_window_launch(int D, bool bf16, const DequantParams& p, int max_pages,
+                                  cudaStream_t s);
 
 // quantize-append and twin append (kvq_quant.cu)
 cudaError_t quantize_append_launch(int D, bool bf16, const QuantParams& p, cudaStream_t s);
