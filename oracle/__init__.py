@@ -69,6 +69,8 @@ def lib():
         L.orc_quantize_row.argtypes = [vp, i32, i32, u16, vp]; L.orc_quantize_row.restype = None
         L.orc_dequant.argtypes = [ctypes.c_int8, u16]; L.orc_dequant.restype = f64
         L.orc_quantize_rows.argtypes = [vp, i64, i32, i32, vp, vp]; L.orc_quantize_rows.restype = None
+        L.orc_quantize_rows_static.argtypes = [vp, i64, i32, i32, ctypes.c_float, vp]
+        L.orc_quantize_rows_static.restype = None
         L.orc_dequantize_rows.argtypes = [vp, vp, i64, i32, i32, vp]
         L.orc_dequantize_rows.restype = None
         L.orc_quantize_append.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp,
@@ -146,6 +148,19 @@ def quantize_rows(x_bits: np.ndarray, dtype: str):
     s = np.empty(x.shape[:-1], dtype=np.uint16)
     lib().orc_quantize_rows(_p(x), N, D, _is_bf16(dtype), _p(q), _p(s))
     return q, s
+
+
+def quantize_rows_static(x_bits: np.ndarray, dtype: str, scale: float) -> np.ndarray:
+    """Static per-tensor scale (binary32): codes = clamp(rne(fl32(x * fl32(1/s))),
+    +-127) ("fix: #552 int8 kv cache quantization cannot be enabled" (InfiniLM
+    PR #553); "Add calibrated INT8 KV cache to PyTorch backend" (TensorRT-LLM
+    PR #18953))."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    D = x.shape[-1]
+    q = np.empty(x.shape, dtype=np.int8)
+    lib().orc_quantize_rows_static(_p(x), x.size // D if D else 0, D, _is_bf16(dtype),
+                                   float(np.float32(scale)), _p(q))
+    return q
 
 
 def dequantize_rows(codes: np.ndarray, scales: np.ndarray, dtype: str) -> np.ndarray:

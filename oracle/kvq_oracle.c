@@ -181,6 +181,28 @@ void orc_dequantize_rows(const int8_t* q, const uint16_t* scales, int64_t N, int
       out[n * D + d] = orc_from_double_rne(orc_dequant(q[n * D + d], scales[n]), is_bf16);
 }
 
+/* Static (per-tensor) scale quantizer: "fix: #552 int8 kv cache quantization
+ * cannot be enabled" (InfiniLM PR #553) -- one static scale per tensor
+ * (default 1.0, or calibrated from max|K| / 127); "Add calibrated INT8 KV
+ * cache to PyTorch backend" (TensorRT-LLM PR #18953) -- a calibrated scalar
+ * (shared by K and V) applied through its reciprocal.  Reading: the scale s
+ * is binary32, inv = fl32(1 / s), and
+ *   q = clamp(round_half_even(fl32(x * inv)), -127, 127)
+ * (the code format of the tokenwise path, no -128).  x * inv is exact in
+ * double (at most 11 + 24 significant bits), so converting it to float is
+ * the single fp32 rounding of the definition. */
+void orc_quantize_rows_static(const uint16_t* x, int64_t N, int D, int is_bf16, float s,
+                              int8_t* q) {
+  const float inv = 1.0f / s;
+  for (int64_t i = 0; i < N * (int64_t)D; ++i) {
+    const float p = (float)(orc_bits_to_double(x[i], is_bf16) * (double)inv);
+    double r = rint((double)p);
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    q[i] = (int8_t)r;
+  }
+}
+
 /* Quantize rows [N][D] into codes [N][D] and scales [N]. */
 void orc_quantize_rows(const uint16_t* x, int64_t N, int D, int is_bf16,
                        int8_t* q, uint16_t* scales) {

@@ -345,3 +345,75 @@ def test_dequantize_rows_vs_library_rounding():
     assert np.array_equal(gotbf, wantbf)
     # a wrong row/scale pairing (transposed operand) must not pass: scales differ by row
     assert not np.array_equal(oracle.dequantize_rows(codes, scales[::-1].copy(), "fp16"), want16)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("scale", [1.0, 0.05, 0.0371, 3.5e-4])
+def test_static_quantizer_vs_float32_arithmetic(dtype, scale):
+    """Static per-tensor scale: against numpy's IEEE float32 reciprocal and
+    product, round half to even, clamp; plus the error bound inside the range,
+    odd symmetry and the default scale 1.0 (codes = rounded values)."""
+    r = np.random.default_rng(int(scale * 1e4) + len(dtype))
+    x = (r.standard_normal((200, 64)) * 127 * scale * 0.4).astype(np.float32)
+    x[0, :6] = [0.0, 127 * scale, -127 * scale, 300 * scale, -300 * scale, 2.5 * scale]
+    if dtype == "fp16":
+        bits = x.astype(np.float16).view(np.uint16)
+        xv = bits.view(np.float16).astype(np.float32)
+    else:
+        bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        xv = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    s32 = np.float32(scale)
+    inv = np.float32(1.0) / s32
+    want = np.clip(np.rint(xv * inv), -127, 127).astype(np.int8)      # float32 product, RNE
+    got = oracle.quantize_rows_static(bits, dtype, scale)
+    assert np.array_equal(got, want)
+    assert got.min() >= -127
+    inside = np.abs(xv.astype(np.float64)) <= 126 * float(s32)
+    err = np.abs(xv.astype(np.float64) - got.astype(np.float64) * float(s32))
+    # the fp32 reciprocal and product move x/s by at most ~2^-23 relative, so a
+    # value within that of a half step may round across it: s/2 (1 + 1e-4)
+    assert np.all(err[inside] <= float(s32) / 2 * (1 + 1e-4))
+    neg = bits ^ np.uint16(0x8000)
+    assert np.array_equal(oracle.quantize_rows_static(neg, dtype, scale), -got)
+    if scale == 1.0:
+        assert np.array_equal(got, np.clip(np.rint(xv), -127, 127).astype(np.int8))
+
+
+def test_static_scale_quality_below_tokenwise_when_token_norms_vary():
+    """The comparison the static variant exists for: when token magnitudes
+    vary (log-normal norms, sigma 1 -- large tokens such as attention sinks
+    next to many small ones), one calibrated per-tensor scale (max|x| / 127
+    over the tensor, as the static-scale pages calibrate) resolves the small
+    tokens far more coarsely than one scale per token: the dequantized K/V
+    error is several times larger, and so is the attention error against the
+    unquantized values (seeded case)."""
+    r = np.random.default_rng(17)
+    L, Hkv, G, D = 512, 2, 4, 128
+    sm = 1.0 / np.sqrt(D)
+
+    def bf16(x):
+        return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(
+            torch.int16).numpy().view(np.uint16)
+    norms = np.exp(1.0 * r.standard_normal((L, Hkv, 1)))
+    k = bf16(r.standard_normal((L, Hkv, D)) * norms)
+    v = bf16(r.standard_normal((L, Hkv, D)) * norms)
+    q = bf16(r.standard_normal((Hkv * G, D)))
+    kf, vf, qf = (oracle.bits_to_double(a, "bf16") for a in (k, v, q))
+    # element level: relative RMS error of the dequantized tensors
+    def rel_rms(xf, xh):
+        return np.sqrt(np.mean((xh - xf) ** 2) / np.mean(xf ** 2))
+    ck, sck = oracle.quantize_rows(k, "bf16")
+    kt = ck.astype(np.float64) * oracle.bits_to_double(sck, "fp16")[..., None]
+    sk = float(np.float32(np.abs(kf).max() / 127))
+    sv = float(np.float32(np.abs(vf).max() / 127))
+    kh = oracle.quantize_rows_static(k, "bf16", sk).astype(np.float64) * sk
+    vh = oracle.quantize_rows_static(v, "bf16", sv).astype(np.float64) * sv
+    assert rel_rms(kf, kh) > 3 * rel_rms(kf, kt)
+    # attention level
+    exact, _ = oracle.decode_sequence(q, k, v, "bf16", sm, quantized=False)
+    tok, _ = oracle.decode_sequence(q, k, v, "bf16", sm, quantized=True)
+    st = np.stack([oracle.attend_one(qf[h], kh[:, h // G], vh[:, h // G], sm)
+                   for h in range(Hkv * G)])
+    err_tok = np.abs(tok - exact).max()
+    err_static = np.abs(st - exact).max()
+    assert err_static > 2 * err_tok, (err_static, err_tok)
