@@ -216,6 +216,41 @@ kvq_status kvq_paged_decode_kv16_split(const void* q, kvq_dtype dtype, int32_t n
                                        void* workspace, size_t workspace_bytes,
                                        int32_t partition_pages, kvq_stream_t stream);
 
+/*
+ * Static-scale variant (one binary32 scale per tensor, no scale planes):
+ * "fix: #552 int8 kv cache quantization cannot be enabled" (InfiniLM PR #553)
+ * -- a static per-tensor scale (default 1.0, or calibrated from max|K|/127);
+ * "Add calibrated INT8 KV cache to PyTorch backend" (TensorRT-LLM PR #18953)
+ * -- a calibrated scalar applied through its reciprocal (K and V may share
+ * it: pass the same value twice).
+ *
+ * kvq_quantize_append_static: as kvq_quantize_append, with
+ *     inv = fl32(1 / scale),  code = clamp(rne(fl32(x * inv)), -127, 127)
+ * (binary32 reciprocal and product, round half to even); no scale planes.
+ * k_scale, v_scale must be finite and > 0 (KVQ_ERR_INVALID_ARGUMENT).
+ *
+ * kvq_paged_decode_static: as kvq_paged_decode over such a cache:
+ *     k_hat = k_scale * code_k,  v_hat = v_scale * code_v
+ * (the K scale is folded into the score scale, the V scale applied to the
+ * output).  Same workspace (kvq_decode_workspace_bytes) and errors.
+ */
+kvq_status kvq_quantize_append_static(const void* k, const void* v, int64_t k_token_stride,
+                                      int64_t v_token_stride, int32_t num_tokens,
+                                      int32_t num_kv_heads, int32_t head_dim, kvq_dtype dtype,
+                                      const int64_t* slot_mapping, int8_t* k_cache,
+                                      int8_t* v_cache, float k_scale, float v_scale,
+                                      int32_t num_blocks, int32_t block_size,
+                                      kvq_stream_t stream);
+
+kvq_status kvq_paged_decode_static(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   const int8_t* k_cache, const int8_t* v_cache, float k_scale,
+                                   float v_scale, int32_t num_blocks, int32_t block_size,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t max_context_len,
+                                   float sm_scale, void* out, void* workspace,
+                                   size_t workspace_bytes, kvq_stream_t stream);
+
 /* Scatter copy of new 16-bit K/V rows into the twin's cache (no
  * quantization): the write half of the 16-bit A/B path.  Arguments as
  * kvq_quantize_append; caches are [num_blocks][num_kv_heads][16][D] of dtype. */

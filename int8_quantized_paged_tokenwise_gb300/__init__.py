@@ -29,6 +29,7 @@ from . import _build
 __all__ = [
     "KvqError", "load", "kvq_quantize_append", "kvq_paged_decode", "kvq_paged_decode_kv16",
     "kvq_cache_append_kv16", "kvq_paged_decode_noalloc", "kvq_dequantize_window",
+    "kvq_quantize_append_static", "kvq_paged_decode_static",
     "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
     "kvq_get_error", "kvq_status_string", "alloc_int8_cache", "alloc_kv16_cache",
     "HEADER_SYMBOLS", "BLOCK_SIZE", "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_CONTEXT",
@@ -48,7 +49,7 @@ HEADER_SYMBOLS = (
     "kvq_decode_partition_pages", "kvq_paged_decode_split", "kvq_decode_workspace_bytes_split",
     "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split", "kvq_cache_append_kv16",
     "kvq_get_error", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
-    "kvq_dequantize_window",
+    "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static",
 )
 
 _lib = None
@@ -88,9 +89,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.kvq_paged_decode_kv16_split.argtypes = dec16 + [i32, vp]
     L.kvq_dequantize_window.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, i32, vp,
                                         i32, i32, vp, vp, vp]
+    f32s = ctypes.c_float
+    L.kvq_quantize_append_static.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp, vp, vp,
+                                             f32s, f32s, i32, i32, vp]
+    L.kvq_paged_decode_static.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, f32s, f32s, i32,
+                                          i32, vp, i32, vp, i32, f32s, vp, vp, sz, vp]
     for fn in ("kvq_quantize_append", "kvq_cache_append_kv16", "kvq_paged_decode",
                "kvq_paged_decode_split", "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split",
-               "kvq_dequantize_window"):
+               "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static"):
         getattr(L, fn).restype = ctypes.c_int
     L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.kvq_decode_workspace_bytes.restype = sz
@@ -194,6 +200,41 @@ def kvq_quantize_append(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, 
                                _ptr(k_scale), _ptr(v_scale), k_cache.shape[0], k_cache.shape[2],
                                _stream(stream))
     _check(st, "kvq_quantize_append")
+
+
+def kvq_quantize_append_static(k, v, slot_mapping, k_cache, v_cache, k_scale: float,
+                               v_scale: float, stream=None):
+    """Quantize-on-write with static per-tensor scales (binary32): codes only,
+    code = clamp(rne(fl32(x * fl32(1/scale))), +-127)."""
+    L = load()
+    _check_cache(k_cache, v_cache, k_cache.shape[1], k_cache.shape[3], (torch.int8,))
+    _check_rows(k, v, slot_mapping)
+    st = L.kvq_quantize_append_static(_ptr(k), _ptr(v), _rows(k, "k"), _rows(v, "v"), k.shape[0],
+                                      k.shape[1], k.shape[2], _dtype_code(k), _ptr(slot_mapping),
+                                      _ptr(k_cache), _ptr(v_cache), float(k_scale),
+                                      float(v_scale), k_cache.shape[0], k_cache.shape[2],
+                                      _stream(stream))
+    _check(st, "kvq_quantize_append_static")
+
+
+def kvq_paged_decode_static(q, k_cache, v_cache, k_scale: float, v_scale: float, block_tables,
+                            context_lens, max_context_len: int, sm_scale: float, out=None,
+                            workspace=None, stream=None):
+    """Paged decode over an INT8 cache with static per-tensor scales."""
+    L = load()
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_decode(q, k_cache, v_cache, block_tables, context_lens, out, (torch.int8,))
+    ws, nbytes = _workspace(q, Hkv, max_context_len, 0, workspace)
+    st = L.kvq_paged_decode_static(_ptr(q), _dtype_code(q), B, Hq, Hkv, D, _ptr(k_cache),
+                                   _ptr(v_cache), float(k_scale), float(v_scale), NB, bs,
+                                   _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                   int(max_context_len), float(sm_scale), _ptr(out), _ptr(ws),
+                                   nbytes, _stream(stream))
+    _check(st, "kvq_paged_decode_static")
+    return out
 
 
 def kvq_cache_append_kv16(k, v, slot_mapping, k_cache, v_cache, stream=None):

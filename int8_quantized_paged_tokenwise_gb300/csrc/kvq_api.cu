@@ -25,8 +25,8 @@ struct DeviceState {
   int sms = 0;
   unsigned int* err = nullptr;
   // occupancy cache: [variant][last smem] -> ctas per SM
-  size_t occ_smem[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  int occ_ctas[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  size_t occ_smem[12] = {};
+  int occ_ctas[12] = {};
 };
 
 std::mutex g_mu;
@@ -60,6 +60,8 @@ DeviceState* device_state() {
     for (bool bf : {false, true}) {
       if (decode_configure_int8(D, bf, decode_smem_bytes_int8(D, kMaxSeqs, kMaxGroup)) !=
               cudaSuccess ||
+          decode_configure_static(D, bf, decode_smem_bytes_static(D, kMaxSeqs, kMaxGroup)) !=
+              cudaSuccess ||
           decode_configure_kv16(D, bf, decode_smem_bytes_kv16(D, kMaxSeqs, kMaxGroup)) !=
               cudaSuccess)
         return nullptr;
@@ -69,14 +71,25 @@ DeviceState* device_state() {
   return &st;
 }
 
-int ctas_per_sm(DeviceState* st, bool int8, int D, bool bf16, size_t smem) {
-  // variants: {int8, kv16} x {D128, D64} x {fp16, bf16}
-  const int v = (int8 ? 0 : 4) + (D == 128 ? 0 : 2) + (bf16 ? 1 : 0);
+// The decode kernel variants: INT8 with per-token scale planes, INT8 with
+// static (per-tensor) scales, and the 16-bit twin.
+enum class Dec { kInt8 = 0, kStatic = 1, kKv16 = 2 };
+
+size_t dec_smem(Dec v, int D, int B, int G) {
+  return v == Dec::kInt8     ? decode_smem_bytes_int8(D, B, G)
+         : v == Dec::kStatic ? decode_smem_bytes_static(D, B, G)
+                             : decode_smem_bytes_kv16(D, B, G);
+}
+
+int ctas_per_sm(DeviceState* st, Dec var, int D, bool bf16, size_t smem) {
+  // cache slots: {int8, static, kv16} x {D128, D64} x {fp16, bf16}
+  const int v = (int)var * 4 + (D == 128 ? 0 : 2) + (bf16 ? 1 : 0);
   std::lock_guard<std::mutex> lk(g_mu);
   if (st->occ_smem[v] != smem || st->occ_ctas[v] == 0) {
     int n = 0;
-    cudaError_t e = int8 ? decode_occupancy_int8(D, bf16, smem, &n)
-                         : decode_occupancy_kv16(D, bf16, smem, &n);
+    cudaError_t e = var == Dec::kInt8     ? decode_occupancy_int8(D, bf16, smem, &n)
+                    : var == Dec::kStatic ? decode_occupancy_static(D, bf16, smem, &n)
+                                          : decode_occupancy_kv16(D, bf16, smem, &n);
     if (e != cudaSuccess || n <= 0) return 0;
     st->occ_smem[v] = smem;
     st->occ_ctas[v] = n;
@@ -125,9 +138,8 @@ int64_t ranges_for_bytes(int32_t B, int32_t G, int32_t D, size_t bytes) {
 
 // Warps of a full persistent grid of one decode variant on this device (0
 // on failure).
-int64_t resident_warps(DeviceState* st, bool int8, int D, bool bf16, int32_t B, int32_t G) {
-  const size_t smem = int8 ? decode_smem_bytes_int8(D, B, G) : decode_smem_bytes_kv16(D, B, G);
-  return (int64_t)st->sms * ctas_per_sm(st, int8, D, bf16, smem) * kWarps;
+int64_t resident_warps(DeviceState* st, Dec var, int D, bool bf16, int32_t B, int32_t G) {
+  return (int64_t)st->sms * ctas_per_sm(st, var, D, bf16, dec_smem(var, D, B, G)) * kWarps;
 }
 
 // Work units of the balanced split for a grid of `warps` warps: one range
@@ -144,9 +156,9 @@ int64_t balanced_units(int64_t warps, int32_t Hkv, int64_t cols_max) {
 int64_t balanced_units_max(DeviceState* st, int32_t B, int32_t Hkv, int32_t G, int32_t D,
                            int32_t max_ctx) {
   int64_t w = 0;
-  for (bool int8 : {true, false})
+  for (Dec var : {Dec::kInt8, Dec::kStatic, Dec::kKv16})
     for (bool bf : {false, true}) {
-      const int64_t x = resident_warps(st, int8, D, bf, B, G);
+      const int64_t x = resident_warps(st, var, D, bf, B, G);
       w = x > w ? x : w;
     }
   return balanced_units(w, Hkv, columns_max(B, max_ctx));
@@ -170,7 +182,7 @@ bool make_map(CUtensorMap* m, const void* base, int elem_bytes, int D, int64_t r
 // Shared validation of the decode arguments (both caches).
 kvq_status check_decode(const void* q, kvq_dtype dtype, int32_t B, int32_t Hq, int32_t Hkv,
                         int32_t D, const void* kc, const void* vc, const void* ks,
-                        const void* vs, bool int8, int32_t num_blocks, int32_t bs,
+                        const void* vs, bool planes, int32_t num_blocks, int32_t bs,
                         const int32_t* bt, int32_t max_blocks, const int32_t* cl,
                         int32_t max_ctx, float sm_scale, const void* out) {
   if (dtype != KVQ_FP16 && dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARGUMENT;
@@ -187,24 +199,25 @@ kvq_status check_decode(const void* q, kvq_dtype dtype, int32_t B, int32_t Hq, i
   if (max_blocks <= 0) return KVQ_ERR_INVALID_ARGUMENT;
   if ((int64_t)max_ctx > (int64_t)max_blocks * kBlockSize) return KVQ_ERR_INVALID_ARGUMENT;
   if (!q || !kc || !vc || !bt || !cl || !out) return KVQ_ERR_INVALID_ARGUMENT;
-  if (int8 && (!ks || !vs)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (planes && (!ks || !vs)) return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(kc, 16) || !aligned(vc, 16) ||
       !aligned(bt, 4) || !aligned(cl, 4))
     return KVQ_ERR_INVALID_ARGUMENT;
-  if (int8 && (!aligned(ks, 16) || !aligned(vs, 16))) return KVQ_ERR_INVALID_ARGUMENT;
+  if (planes && (!aligned(ks, 16) || !aligned(vs, 16))) return KVQ_ERR_INVALID_ARGUMENT;
   return KVQ_OK;
 }
 
 // R == 0: balanced split (or one range per segment without a workspace, or
 // when no sequence can span two pages); R >= 1: ranges of R pages.
-kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, int32_t Hq,
+kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int32_t Hq,
                          int32_t Hkv, int32_t D, const void* kc, const void* vc,
                          const uint16_t* ks, const uint16_t* vs, int32_t num_blocks,
                          int32_t bs, const int32_t* bt, int32_t max_blocks, const int32_t* cl,
                          int32_t max_ctx, float sm_scale, void* out, void* ws, size_t ws_bytes,
-                         int32_t R, cudaStream_t stream) {
-  kvq_status s = check_decode(q, dtype, B, Hq, Hkv, D, kc, vc, ks, vs, int8, num_blocks, bs, bt,
-                              max_blocks, cl, max_ctx, sm_scale, out);
+                         int32_t R, cudaStream_t stream, float k_static = 1.f,
+                         float v_static = 1.f) {
+  kvq_status s = check_decode(q, dtype, B, Hq, Hkv, D, kc, vc, ks, vs, var == Dec::kInt8,
+                              num_blocks, bs, bt, max_blocks, cl, max_ctx, sm_scale, out);
   if (s != KVQ_OK || B == 0) return s;
   // the page prefix over sequences and token counts are 32-bit in the kernels
   if ((int64_t)B * max_blocks > INT32_MAX || max_blocks > INT32_MAX / kBlockSize)
@@ -214,9 +227,8 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   if (!st) return cuda_fail();
   const bool bf16 = dtype == KVQ_BF16;
   const int32_t G = Hq / Hkv;
-  const size_t smem =
-      int8 ? decode_smem_bytes_int8(D, B, G) : decode_smem_bytes_kv16(D, B, G);
-  const int occ = ctas_per_sm(st, int8, D, bf16, smem);
+  const size_t smem = dec_smem(var, D, B, G);
+  const int occ = ctas_per_sm(st, var, D, bf16, smem);
   if (occ <= 0) return cuda_fail();
   const int64_t slots = (int64_t)st->sms * occ;      // CTAs of a full persistent grid
   const int64_t cols = columns_max(B, max_ctx);
@@ -268,7 +280,7 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
 
   CUtensorMap maps[2];
   const int64_t rows = (int64_t)num_blocks * Hkv * kBlockSize;
-  const int eb = int8 ? 1 : 2;
+  const int eb = var == Dec::kKv16 ? 2 : 1;
   if (!make_map(&maps[0], kc, eb, D, rows) || !make_map(&maps[1], vc, eb, D, rows))
     return cuda_fail();
 
@@ -291,10 +303,14 @@ kvq_status decode_common(bool int8, const void* q, kvq_dtype dtype, int32_t B, i
   p.max_blocks = max_blocks;
   p.max_ctx = max_ctx;
   p.num_blocks = num_blocks;
-  p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
+  p.scale_log2 = (float)((double)sm_scale * (double)k_static * 1.4426950408889634);
+  p.v_static = v_static;
 
-  cudaError_t e = int8 ? decode_launch_int8(D, bf16, maps, p, (int)grid, smem, stream)
-                       : decode_launch_kv16(D, bf16, maps, p, (int)grid, smem, stream);
+  cudaError_t e = var == Dec::kInt8
+                      ? decode_launch_int8(D, bf16, maps, p, (int)grid, smem, stream)
+                  : var == Dec::kStatic
+                      ? decode_launch_static(D, bf16, maps, p, (int)grid, smem, stream)
+                      : decode_launch_kv16(D, bf16, maps, p, (int)grid, smem, stream);
   if (e != cudaSuccess) return cuda_fail();
   if (split) {
     CombineParams cp{};
@@ -372,6 +388,63 @@ kvq_status kvq_quantize_append(const void* k, const void* v, int64_t k_token_str
   return KVQ_OK;
 }
 
+kvq_status kvq_quantize_append_static(const void* k, const void* v, int64_t k_token_stride,
+                                      int64_t v_token_stride, int32_t num_tokens,
+                                      int32_t num_kv_heads, int32_t head_dim, kvq_dtype dtype,
+                                      const int64_t* slot_mapping, int8_t* k_cache,
+                                      int8_t* v_cache, float k_scale, float v_scale,
+                                      int32_t num_blocks, int32_t block_size,
+                                      kvq_stream_t stream) {
+  kvq_status s = check_append(k, v, k_token_stride, v_token_stride, num_tokens, num_kv_heads,
+                              head_dim, dtype, slot_mapping, k_cache, v_cache, num_blocks,
+                              block_size);
+  if (s != KVQ_OK) return s;
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  // the reciprocal each code is computed with: one IEEE binary32 division
+  const volatile float one = 1.0f;
+  const float inv_k = one / k_scale, inv_v = one / v_scale;
+  if (!std::isfinite(inv_k) || !std::isfinite(inv_v)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return KVQ_OK;
+  DeviceState* st = device_state();
+  if (!st) return cuda_fail();
+  QuantParams p{};
+  p.k = k;
+  p.v = v;
+  p.k_stride = k_token_stride;
+  p.v_stride = v_token_stride;
+  p.slots = slot_mapping;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.num_rows = (int64_t)num_tokens * num_kv_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_slots = (int64_t)num_blocks * kBlockSize;
+  p.err = st->err;
+  if (quantize_static_launch(head_dim, dtype == KVQ_BF16, p, inv_k, inv_v,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return KVQ_OK;
+}
+
+kvq_status kvq_paged_decode_static(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   const int8_t* k_cache, const int8_t* v_cache, float k_scale,
+                                   float v_scale, int32_t num_blocks, int32_t block_size,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t max_context_len,
+                                   float sm_scale, void* out, void* workspace,
+                                   size_t workspace_bytes, kvq_stream_t stream) {
+  if (!(std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite((double)sm_scale * (double)k_scale * 1.4426950408889634))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  return decode_common(Dec::kStatic, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       k_cache, v_cache, nullptr, nullptr, num_blocks, block_size, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
+                       workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream),
+                       k_scale, v_scale);
+}
+
 kvq_status kvq_cache_append_kv16(const void* k, const void* v, int64_t k_token_stride,
                                  int64_t v_token_stride, int32_t num_tokens,
                                  int32_t num_kv_heads, int32_t head_dim, kvq_dtype dtype,
@@ -411,7 +484,7 @@ kvq_status kvq_paged_decode_split(const void* q, kvq_dtype dtype, int32_t num_se
                                   size_t workspace_bytes, int32_t partition_pages,
                                   kvq_stream_t stream) {
   if (partition_pages <= 0) return KVQ_ERR_INVALID_ARGUMENT;
-  return decode_common(true, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+  return decode_common(Dec::kInt8, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
                        v_cache, k_scale, v_scale, num_blocks, block_size, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
                        workspace, workspace_bytes, partition_pages,
@@ -427,7 +500,7 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
                             const int32_t* context_lens, int32_t max_context_len,
                             float sm_scale, void* out, void* workspace, size_t workspace_bytes,
                             kvq_stream_t stream) {
-  return decode_common(true, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+  return decode_common(Dec::kInt8, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
                        v_cache, k_scale, v_scale, num_blocks, block_size, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
                        workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
@@ -443,7 +516,7 @@ kvq_status kvq_paged_decode_kv16_split(const void* q, kvq_dtype dtype, int32_t n
                                        void* workspace, size_t workspace_bytes,
                                        int32_t partition_pages, kvq_stream_t stream) {
   if (partition_pages <= 0) return KVQ_ERR_INVALID_ARGUMENT;
-  return decode_common(false, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+  return decode_common(Dec::kKv16, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
                        v_cache, nullptr, nullptr, num_blocks, block_size, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
                        workspace, workspace_bytes, partition_pages,
@@ -457,7 +530,7 @@ kvq_status kvq_paged_decode_kv16(const void* q, kvq_dtype dtype, int32_t num_seq
                                  int32_t max_blocks_per_seq, const int32_t* context_lens,
                                  int32_t max_context_len, float sm_scale, void* out,
                                  void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
-  return decode_common(false, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+  return decode_common(Dec::kKv16, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
                        v_cache, nullptr, nullptr, num_blocks, block_size, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
                        workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
@@ -522,7 +595,7 @@ int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_q_heads, int32_
   DeviceState* st = device_state();
   if (!st) return 0;
   const int32_t G = num_q_heads / num_kv_heads;
-  const int64_t w = resident_warps(st, true, head_dim, true, num_seqs, G);
+  const int64_t w = resident_warps(st, Dec::kInt8, head_dim, true, num_seqs, G);
   if (w <= 0) return 0;
   const int64_t groups = w / num_kv_heads > 0 ? w / num_kv_heads : 1;
   const int64_t r = cdiv(columns_max(num_seqs, max_context_len), groups);

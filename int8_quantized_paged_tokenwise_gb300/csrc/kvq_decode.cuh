@@ -52,7 +52,8 @@
 
 namespace kvq {
 
-template <int D, bool INT8>
+// STATIC: INT8 codes with one binary32 scale per tensor (no scale planes).
+template <int D, bool INT8, bool STATIC = false>
 struct TileCfg {
   static constexpr int kElem = INT8 ? 1 : 2;                 // bytes per cache element
   static constexpr int kRowBytes = D * kElem;                // bytes per token row
@@ -62,7 +63,7 @@ struct TileCfg {
   static constexpr int kTile = kBlockSize * kRowBytes;        // bytes of one K (or V) tile
   static constexpr int kStages = INT8 ? KVQ_INT8_STAGES : 2;  // pages in flight per warp
   static constexpr int kStageBytes = 2 * kTile;               // K tile then V tile
-  static constexpr int kScaleBytes = INT8 ? 2 * kBlockSize * 2 : 0;  // K then V scale rows
+  static constexpr int kScaleBytes = INT8 && !STATIC ? 2 * kBlockSize * 2 : 0;  // K, V scale rows
   static constexpr uint32_t kTxBytes = 2 * kTile + kScaleBytes;
   static constexpr uint32_t kSwzMask = kSubRow == 128 ? 0x70u : 0x30u;
   static constexpr int kMinCtas = INT8 ? KVQ_INT8_MIN_CTAS : 3;
@@ -180,9 +181,9 @@ __device__ __forceinline__ Piece next_piece(const WalkConst& w, const int* prefi
 // S page stages, one raw query slot (the TMA target, G*D*2 bytes) and a query
 // fragment buffer ([k-step][lane] pairs of the MMA B operand for the lanes
 // 0..4G-1 of real heads, also G*D*2 bytes; the padded heads read as zeros).
-template <int D, bool INT8>
+template <int D, bool INT8, bool STATIC = false>
 struct SmemLayout {
-  using C = TileCfg<D, INT8>;
+  using C = TileCfg<D, INT8, STATIC>;
   size_t tiles, q, qfrag, scales, bars, stage_blk, misc, walk, seq, total_bytes;
   uint32_t q_bytes;  // one piece's query rows: G * D * 2
   __host__ __device__ SmemLayout(int B, int G) {
@@ -208,12 +209,12 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 // INT8: QBF16 = activations are bf16 (converted to FP16 for the tensor cores);
 // twin: QBF16 selects the bf16 MMA, otherwise FP16.
-template <int D, bool INT8, bool QBF16>
-__global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
+template <int D, bool INT8, bool QBF16, bool STATIC = false>
+__global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
-  using C = TileCfg<D, INT8>;
-  const SmemLayout<D, INT8> lay(p.B, p.G);
+  using C = TileCfg<D, INT8, STATIC>;
+  const SmemLayout<D, INT8, STATIC> lay(p.B, p.G);
   constexpr bool MMA_BF16 = (!INT8) && QBF16;
   constexpr int S = C::kStages;
   constexpr int KSTEPS = D / 16;       // MMA k-steps over the head dim
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
         const int row = blk * Hkv + is_j;             // (block, KV head) tile index
         if (lane < kTensorCopies) {
           tma_load_2d(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * kBlockSize, bar);
-        } else if (INT8 && lane < kTensorCopies + 2) {
+        } else if (INT8 && !STATIC && lane < kTensorCopies + 2) {
           bulk_load(sc_dst + s * C::kScaleBytes, sc_src + (int64_t)row * kBlockSize,
                     kBlockSize * 2, bar);
         }
@@ -587,8 +588,9 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
         }
 
         // scores in log2 units: z0 (token g, head 2c), z1 (g, 2c+1), z2 (g+8, 2c), z3
+        // (static scales: the K scale is folded into scale_log2)
         float ksg = p.scale_log2, ksg8 = p.scale_log2;
-        if constexpr (INT8) {
+        if constexpr (INT8 && !STATIC) {
           const uint16_t* ksc = scales_w + s * (C::kScaleBytes / 2);
           ksg *= __half2float(__ushort_as_half(ksc[g]));
           ksg8 *= __half2float(__ushort_as_half(ksc[g + 8]));
@@ -631,9 +633,14 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
 
         // ---------- O^T[d][head] += V^T P^T: M = 16 head-dims, N = 8 heads ----------
         if constexpr (INT8) {
-          const uint16_t* vsc = scales_w + s * (C::kScaleBytes / 2) + kBlockSize;
-          const __half2 vs01 = u32_as_h2(reinterpret_cast<const uint32_t*>(vsc)[c]);
-          const __half2 vs89 = u32_as_h2(reinterpret_cast<const uint32_t*>(vsc)[4 + c]);
+          // per-token V scales multiply the converted pairs; a static V scale
+          // is applied once to the output instead
+          __half2 vs01 = __float2half2_rn(1.f), vs89 = vs01;
+          if constexpr (!STATIC) {
+            const uint16_t* vsc = scales_w + s * (C::kScaleBytes / 2) + kBlockSize;
+            vs01 = u32_as_h2(reinterpret_cast<const uint32_t*>(vsc)[c]);
+            vs89 = u32_as_h2(reinterpret_cast<const uint32_t*>(vsc)[4 + c]);
+          }
 #pragma unroll
           for (int kk = 0; kk < KSTEPS / 2; ++kk) {
             uint32_t r[4];
@@ -645,10 +652,12 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
               uint32_t ev0, od0, ev1, od1;
               i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h], ev0, od0);
               i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h + 1], ev1, od1);
-              ev0 = h2_as_u32(__hmul2(u32_as_h2(ev0), vs01));
-              od0 = h2_as_u32(__hmul2(u32_as_h2(od0), vs01));
-              ev1 = h2_as_u32(__hmul2(u32_as_h2(ev1), vs89));
-              od1 = h2_as_u32(__hmul2(u32_as_h2(od1), vs89));
+              if constexpr (!STATIC) {
+                ev0 = h2_as_u32(__hmul2(u32_as_h2(ev0), vs01));
+                od0 = h2_as_u32(__hmul2(u32_as_h2(od0), vs01));
+                ev1 = h2_as_u32(__hmul2(u32_as_h2(ev1), vs89));
+                od1 = h2_as_u32(__hmul2(u32_as_h2(od1), vs89));
+              }
               const int cb = 2 * kk + h;
               float* oq = o + 4 * cb;
               mma_16816_acc<false>(*reinterpret_cast<float(*)[4]>(oq), ev0, od0, ev1, od1, pb0, pb1);
@@ -686,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8>::kMinCtas)
       if (head >= G) continue;
       const float l = hh ? l1 : l0;
       const float m = hh ? m1 : m0;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (STATIC ? p.v_static : 1.f) / l : 0.f;
       const int64_t hrow = (int64_t)it.b * p.Hq + (int64_t)it.j * G + head;
       if (it.flags & 1) {
         uint16_t* dst = static_cast<uint16_t*>(p.out) + hrow * D;

@@ -61,7 +61,8 @@ struct DecodeParams {
                             // least kMinRangePages); < 0: one unit per (sequence, KV head)
   int64_t groups;           // R == 0: ranges of the balanced split (>= 1)
   int64_t range_cap;        // work units the partial slots hold (0 when R < 0)
-  float scale_log2;         // sm_scale * log2(e)
+  float scale_log2;         // sm_scale * log2(e) (static scales: times the K scale)
+  float v_static;           // static scales: the V scale (applied to the output)
 };
 
 struct CombineParams {
@@ -96,6 +97,11 @@ cudaError_t decode_configure_int8(int D, bool bf16, size_t smem);
 cudaError_t decode_occupancy_int8(int D, bool bf16, size_t smem, int* n);
 cudaError_t decode_launch_int8(int D, bool bf16, const CUtensorMap* maps,
                                const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
+size_t decode_smem_bytes_static(int D, int B, int G);
+cudaError_t decode_configure_static(int D, bool bf16, size_t smem);
+cudaError_t decode_occupancy_static(int D, bool bf16, size_t smem, int* n);
+cudaError_t decode_launch_static(int D, bool bf16, const CUtensorMap* maps,
+                                 const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
 size_t decode_smem_bytes_kv16(int D, int B, int G);
 cudaError_t decode_configure_kv16(int D, bool bf16, size_t smem);
 cudaError_t decode_occupancy_kv16(int D, bool bf16, size_t smem, int* n);
@@ -111,6 +117,9 @@ cudaError_t dequant_window_launch(int D, bool bf16, const DequantParams& p, int 
 
 // quantize-append and twin append (kvq_quant.cu)
 cudaError_t quantize_append_launch(int D, bool bf16, const QuantParams& p, cudaStream_t s);
+// static scales: p.k_scale/v_scale unused, inv_k/inv_v = fl32(1 / scale)
+cudaError_t quantize_static_launch(int D, bool bf16, const QuantParams& p, float inv_k,
+                                   float inv_v, cudaStream_t s);
 cudaError_t append_kv16_launch(int D, const QuantParams& p, cudaStream_t s);
 
 }  // namespace kvq

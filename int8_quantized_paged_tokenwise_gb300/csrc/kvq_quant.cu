@@ -127,6 +127,51 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Qu
   }
 }
 
+// Static (per-tensor, binary32) scales: "fix: #552 int8 kv cache quantization
+// cannot be enabled" (InfiniLM PR #553) and "Add calibrated INT8 KV cache to
+// PyTorch backend" (TensorRT-LLM PR #18953) -- one scale per tensor applied
+// through its reciprocal: code = clamp(rint(fl32(x * inv)), -127, 127) with
+// inv = fl32(1 / scale) from the host.  __fmul_rn keeps the product one IEEE
+// rounding (no contraction); no scale planes are written.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kQuantThreads) quantize_static_kernel(const QuantParams p,
+                                                                         float inv_k,
+                                                                         float inv_v) {
+  constexpr int LPR = D / 4;  // lanes per row
+  const int64_t gthread = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
+  const int64_t row = gthread / LPR;
+  const int sub = (threadIdx.x & 31) % LPR;
+  griddep_launch_dependents();
+  if (row >= p.num_rows) return;
+  const int64_t t = row / p.num_kv_heads;
+  const int j = (int)(row - t * p.num_kv_heads);
+  const int64_t slot = p.slots[t];
+  if (slot < 0) return;
+  if (slot >= p.num_slots) {
+    if (sub == 0) atomicOr(p.err, 0x1u);
+    return;
+  }
+  const uint16_t* kr = static_cast<const uint16_t*>(p.k) + t * p.k_stride + (int64_t)j * D;
+  const uint16_t* vr = static_cast<const uint16_t*>(p.v) + t * p.v_stride + (int64_t)j * D;
+  const uint2 kx = __ldg(reinterpret_cast<const uint2*>(kr) + sub);
+  const uint2 vx = __ldg(reinterpret_cast<const uint2*>(vr) + sub);
+  const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
+  const int64_t crow = (blk * p.num_kv_heads + j) * kBlockSize + off;
+  uint32_t kq = 0, vq = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t kw = (e < 2) ? kx.x : kx.y, vw = (e < 2) ? vx.x : vx.y;
+    const uint32_t kb = (e & 1) ? (kw >> 16) : (kw & 0xFFFFu);
+    const uint32_t vb = (e & 1) ? (vw >> 16) : (vw & 0xFFFFu);
+    const float kr8 = fminf(fmaxf(rintf(__fmul_rn(bits_to_float<BF16>(kb), inv_k)), -127.f), 127.f);
+    const float vr8 = fminf(fmaxf(rintf(__fmul_rn(bits_to_float<BF16>(vb), inv_v)), -127.f), 127.f);
+    kq |= (uint32_t)((int)kr8 & 0xFF) << (8 * e);
+    vq |= (uint32_t)((int)vr8 & 0xFF) << (8 * e);
+  }
+  reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.k_cache) + crow * D)[sub] = kq;
+  reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.v_cache) + crow * D)[sub] = vq;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) append_kv16_kernel(const QuantParams p) {
   constexpr int LPR = D / 4;
@@ -168,6 +213,20 @@ cudaError_t quantize_append_launch(int D, bool bf16, const QuantParams& p, cudaS
   } else {
     if (bf16) quantize_append_kernel<64, true><<<grid, kQuantThreads, 0, s>>>(p);
     else quantize_append_kernel<64, false><<<grid, kQuantThreads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t quantize_static_launch(int D, bool bf16, const QuantParams& p, float inv_k,
+                                   float inv_v, cudaStream_t s) {
+  if (p.num_rows == 0) return cudaSuccess;
+  const int grid = grid_for(p.num_rows, D);
+  if (D == 128) {
+    if (bf16) quantize_static_kernel<128, true><<<grid, kQuantThreads, 0, s>>>(p, inv_k, inv_v);
+    else quantize_static_kernel<128, false><<<grid, kQuantThreads, 0, s>>>(p, inv_k, inv_v);
+  } else {
+    if (bf16) quantize_static_kernel<64, true><<<grid, kQuantThreads, 0, s>>>(p, inv_k, inv_v);
+    else quantize_static_kernel<64, false><<<grid, kQuantThreads, 0, s>>>(p, inv_k, inv_v);
   }
   return cudaGetLastError();
 }
