@@ -404,15 +404,22 @@ def sweep(torch, kvq, dev, flush, steps):
             # the dequantize-window baseline: 16-bit window, then the 16-bit decode
             kvq.kvq_dequantize_window(kc, vc, ksc, vsc, btd, cl, ctx, torch.bfloat16, kw, vw)
             kvq.kvq_paged_decode_kv16(q, kw, vw, btd, cl, ctx, w.sm_scale, out=out, workspace=ws)
+        # static per-tensor scales over the same codes (timing only: the codes
+        # were written with per-token scales)
+        dst = lambda: kvq.kvq_paged_decode_static(q, kc, vc, 0.05, 0.05, btd, cl, ctx,  # noqa
+                                                  w.sm_scale, out=out, workspace=ws)
         nop = lambda: None  # noqa: E731
         _, t8 = time_arm(torch, flush, nop, d8, steps, 3)
         _, t16 = time_arm(torch, flush, nop, d16, steps, 3)
         _, tw = time_arm(torch, flush, nop, dwin, steps, 3)
+        _, tst = time_arm(torch, flush, nop, dst, steps, 3)
         m8, m16, mw = statistics.mean(t8), statistics.mean(t16), statistics.mean(tw)
+        mst = statistics.mean(tst)
         res.append({"context": ctx, "num_seqs": B, "int8_us": round(1e3 * m8, 2),
                     "bf16_us": round(1e3 * m16, 2),
                     "dequant_window_us": round(1e3 * mw, 2),
                     "dequant_window_speedup_vs_bf16": round(m16 / mw, 3),
+                    "int8_static_us": round(1e3 * mst, 2),
                     "int8_gbs": round(w.decode_bytes_int8() / (m8 * 1e-3) / 1e9, 1),
                     "bf16_gbs": round(w.decode_bytes_kv16() / (m16 * 1e-3) / 1e9, 1),
                     "int8_speedup_vs_bf16": round(m16 / m8, 3)})

@@ -71,6 +71,8 @@ def lib():
         L.orc_quantize_rows.argtypes = [vp, i64, i32, i32, vp, vp]; L.orc_quantize_rows.restype = None
         L.orc_quantize_rows_static.argtypes = [vp, i64, i32, i32, ctypes.c_float, vp]
         L.orc_quantize_rows_static.restype = None
+        L.orc_trim_keep_sink.argtypes = [vp, i64, i64, i64, i64, vp]
+        L.orc_trim_keep_sink.restype = i64
         L.orc_dequantize_rows.argtypes = [vp, vp, i64, i32, i32, vp]
         L.orc_dequantize_rows.restype = None
         L.orc_quantize_append.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp,
@@ -161,6 +163,18 @@ def quantize_rows_static(x_bits: np.ndarray, dtype: str, scale: float) -> np.nda
     lib().orc_quantize_rows_static(_p(x), x.size // D if D else 0, D, _is_bf16(dtype),
                                    float(np.float32(scale)), _p(q))
     return q
+
+
+def trim_keep_sink(rows: np.ndarray, keep: int, n: int) -> np.ndarray:
+    """Front trim keeping the first ``keep`` tokens: rows [L, ...] -> [L', ...]
+    without the n tokens after the sink ("fix(cuda/kv): correct Int8 KV
+    per-token scale ..." (mlxcel PR #717) follow-up, "The fix")."""
+    a = np.ascontiguousarray(rows)
+    L = a.shape[0]
+    rb = a.nbytes // L if L else 0
+    out = np.empty_like(a)
+    m = lib().orc_trim_keep_sink(_p(a), L, rb, int(keep), int(n), _p(out))
+    return out[:m]
 
 
 def dequantize_rows(codes: np.ndarray, scales: np.ndarray, dtype: str) -> np.ndarray:

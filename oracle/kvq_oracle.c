@@ -203,6 +203,29 @@ void orc_quantize_rows_static(const uint16_t* x, int64_t N, int D, int is_bf16, 
   }
 }
 
+/* Front trim that keeps the attention sink: "fix(cuda/kv): correct Int8 KV
+ * per-token scale ..." (mlxcel PR #717) follow-up commit, "The fix" -- with
+ * keep > 0 the sequence becomes [first keep tokens] ++ [the rest after the
+ * next n], exactly n tokens removed, the INT8 payload and its scales sliced
+ * in lockstep; keep = 0 is the plain front trim.  Reading: keep and n are
+ * clamped to the sequence (keep <= L, n <= L - keep).  Rows are `row_bytes`
+ * bytes (one token's payload, or its scale row); in [L] -> out [L'] with
+ * L' = L - n returned. */
+int64_t orc_trim_keep_sink(const uint8_t* in, int64_t L, int64_t row_bytes, int64_t keep,
+                           int64_t n, uint8_t* out) {
+  if (keep < 0) keep = 0;
+  if (keep > L) keep = L;
+  if (n < 0) n = 0;
+  if (n > L - keep) n = L - keep;
+  int64_t o = 0;
+  for (int64_t t = 0; t < L; ++t) {
+    if (t >= keep && t < keep + n) continue;             /* the n tokens after the sink */
+    memcpy(out + o * row_bytes, in + t * row_bytes, (size_t)row_bytes);
+    ++o;
+  }
+  return o;
+}
+
 /* Quantize rows [N][D] into codes [N][D] and scales [N]. */
 void orc_quantize_rows(const uint16_t* x, int64_t N, int D, int is_bf16,
                        int8_t* q, uint16_t* scales) {

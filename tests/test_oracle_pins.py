@@ -417,3 +417,28 @@ def test_static_scale_quality_below_tokenwise_when_token_norms_vary():
     err_tok = np.abs(tok - exact).max()
     err_static = np.abs(st - exact).max()
     assert err_static > 2 * err_tok, (err_static, err_tok)
+
+
+def test_trim_keep_sink_matches_page_examples_and_composes():
+    """Front trim keeping the sink: the kept positions of the worked cases in
+    tests/golden/trim_keep_sink.txt (from the page's rule: [first keep] ++
+    [the rest after the next n], exactly n removed, keep = 0 the old front
+    trim, clamped to the sequence); trimming n1 then n2 equals trimming
+    n1 + n2 with the same keep; rows (payload or scale rows) move intact."""
+    with open(os.path.join(GOLDEN, "trim_keep_sink.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            L, keep, n, kept = [x.strip() for x in line.split("|")]
+            L, keep, n = int(L), int(keep), int(n)
+            pos = np.arange(L, dtype=np.int64)
+            got = oracle.trim_keep_sink(pos, keep, n)
+            assert got.tolist() == [int(x) for x in kept.split()], (L, keep, n)
+    r = np.random.default_rng(3)
+    rows = r.integers(-127, 128, size=(300, 8, 16)).astype(np.int8)
+    for keep in (0, 4, 17):
+        for n1, n2 in ((5, 9), (1, 1), (100, 150)):
+            two = oracle.trim_keep_sink(oracle.trim_keep_sink(rows, keep, n1), keep, n2)
+            one = oracle.trim_keep_sink(rows, keep, n1 + n2)
+            assert np.array_equal(two, one)
+            assert len(one) == 300 - (n1 + n2)
