@@ -288,6 +288,35 @@ kvq_status kvq_dequantize_window(const int8_t* k_cache, const int8_t* v_cache,
                                  kvq_stream_t stream);
 
 /*
+ * kvq_trim_front_keep_sink -- front trim of each sequence that keeps the
+ * attention sink.  Defined by "fix(cuda/kv): correct Int8 KV per-token scale
+ * ..." (mlxcel PR #717), follow-up commit, "The fix": a sequence of L tokens
+ * becomes [its first keep tokens] ++ [the tokens after the next n], exactly n
+ * removed, the INT8 payload and its scale rows moved in lockstep; keep = 0 is
+ * the plain front trim (drop the n oldest).  Per sequence b:
+ *     keep_b = min(keep, L),  n = clamp(trim[b], 0, L - keep_b)
+ *     token keep_b + n + i moves to keep_b + i,  context_lens[b] = L - n.
+ *
+ *   k_cache, v_cache   INT8 payload [num_blocks][num_kv_heads][16][D], moved
+ *                      in place through the block table.
+ *   k_scale, v_scale   FP16 scale planes, moved with the payload; both NULL
+ *                      for a static-scale cache (codes only).
+ *   context_lens       device int32 [B], read, then updated in place.
+ *   trim               device int32 [B], tokens to drop after the sink.
+ *   keep               sink tokens kept at the front (>= 0; 4 in the page's
+ *                      scheduler).
+ * The pages of a trimmed sequence must not be shared with another sequence.
+ * Rows past the new length are left as they were.  Device errors: block id
+ * out of range (that token skipped, KVQ_DEVERR_BLOCK).
+ */
+kvq_status kvq_trim_front_keep_sink(int8_t* k_cache, int8_t* v_cache, uint16_t* k_scale,
+                                    uint16_t* v_scale, int32_t num_blocks, int32_t block_size,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    const int32_t* block_tables, int32_t num_seqs,
+                                    int32_t max_blocks_per_seq, int32_t* context_lens,
+                                    const int32_t* trim, int32_t keep, kvq_stream_t stream);
+
+/*
  * kvq_paged_decode_noalloc -- kvq_paged_decode for callers that cannot
  * allocate device memory.  The pages have no counterpart of this call; it
  * exists for hosts that own all device memory through their own pool

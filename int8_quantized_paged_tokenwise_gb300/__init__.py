@@ -29,7 +29,7 @@ from . import _build
 __all__ = [
     "KvqError", "load", "kvq_quantize_append", "kvq_paged_decode", "kvq_paged_decode_kv16",
     "kvq_cache_append_kv16", "kvq_paged_decode_noalloc", "kvq_dequantize_window",
-    "kvq_quantize_append_static", "kvq_paged_decode_static",
+    "kvq_quantize_append_static", "kvq_paged_decode_static", "kvq_trim_front_keep_sink",
     "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
     "kvq_get_error", "kvq_status_string", "alloc_int8_cache", "alloc_kv16_cache",
     "HEADER_SYMBOLS", "BLOCK_SIZE", "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_CONTEXT",
@@ -50,6 +50,7 @@ HEADER_SYMBOLS = (
     "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split", "kvq_cache_append_kv16",
     "kvq_get_error", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
     "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static",
+    "kvq_trim_front_keep_sink",
 )
 
 _lib = None
@@ -90,13 +91,16 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.kvq_dequantize_window.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, i32, vp,
                                         i32, i32, vp, vp, vp]
     f32s = ctypes.c_float
+    L.kvq_trim_front_keep_sink.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, i32, vp,
+                                           vp, i32, vp]
     L.kvq_quantize_append_static.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp, vp, vp,
                                              f32s, f32s, i32, i32, vp]
     L.kvq_paged_decode_static.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, f32s, f32s, i32,
                                           i32, vp, i32, vp, i32, f32s, vp, vp, sz, vp]
     for fn in ("kvq_quantize_append", "kvq_cache_append_kv16", "kvq_paged_decode",
                "kvq_paged_decode_split", "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split",
-               "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static"):
+               "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static",
+               "kvq_trim_front_keep_sink"):
         getattr(L, fn).restype = ctypes.c_int
     L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.kvq_decode_workspace_bytes.restype = sz
@@ -385,6 +389,30 @@ def kvq_dequantize_window(k_cache, v_cache, k_scale, v_scale, block_tables, cont
                                  _ptr(v_out), _stream(stream))
     _check(st, "kvq_dequantize_window")
     return k_out, v_out
+
+
+def kvq_trim_front_keep_sink(k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                             trim, keep: int, stream=None):
+    """Front trim keeping the first ``keep`` tokens of each sequence: drops
+    trim[b] tokens after them (payload and scales in lockstep) and updates
+    context_lens in place.  k_scale/v_scale None for a static-scale cache."""
+    L = load()
+    NB, Hkv, bs, D = k_cache.shape
+    _check_cache(k_cache, v_cache, Hkv, D, (torch.int8,))
+    if k_scale is not None:
+        _check_scales(k_scale, v_scale, k_cache)
+    B = context_lens.shape[0]
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+          and block_tables.shape[0] == B and block_tables.is_contiguous(),
+          "block_tables must be contiguous int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous(),
+          "context_lens must be int32 [B]")
+    _need(trim.dtype == torch.int32 and trim.shape == (B,) and trim.is_contiguous(),
+          "trim must be int32 [B]")
+    st = L.kvq_trim_front_keep_sink(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                    NB, bs, Hkv, D, _ptr(block_tables), B, block_tables.shape[1],
+                                    _ptr(context_lens), _ptr(trim), int(keep), _stream(stream))
+    _check(st, "kvq_trim_front_keep_sink")
 
 
 def kvq_get_error(stream=None):

@@ -586,6 +586,52 @@ kvq_status kvq_dequantize_window(const int8_t* k_cache, const int8_t* v_cache,
   return KVQ_OK;
 }
 
+kvq_status kvq_trim_front_keep_sink(int8_t* k_cache, int8_t* v_cache, uint16_t* k_scale,
+                                    uint16_t* v_scale, int32_t num_blocks, int32_t block_size,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    const int32_t* block_tables, int32_t num_seqs,
+                                    int32_t max_blocks_per_seq, int32_t* context_lens,
+                                    const int32_t* trim, int32_t keep, kvq_stream_t stream) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_blocks <= 0 || keep < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (block_size != kBlockSize) return KVQ_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (num_kv_heads > 65535 || num_seqs > 65535 ||
+      (int64_t)num_blocks * num_kv_heads * kBlockSize > INT32_MAX)
+    return KVQ_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return KVQ_OK;
+  if (max_blocks_per_seq <= 0 || max_blocks_per_seq > INT32_MAX / kBlockSize)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!k_cache || !v_cache || !block_tables || !context_lens || !trim)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if ((k_scale == nullptr) != (v_scale == nullptr)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_tables, 4) ||
+      !aligned(context_lens, 4) || !aligned(trim, 4) || (k_scale && !aligned(k_scale, 2)) ||
+      (v_scale && !aligned(v_scale, 2)))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  DeviceState* st = device_state();
+  if (!st) return cuda_fail();
+  TrimParams p{};
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.trim = trim;
+  p.err = st->err;
+  p.B = num_seqs;
+  p.Hkv = num_kv_heads;
+  p.max_blocks = max_blocks_per_seq;
+  p.max_tok = max_blocks_per_seq * kBlockSize;
+  p.num_blocks = num_blocks;
+  p.keep = keep;
+  if (trim_launch(head_dim, p, context_lens, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return cuda_fail();
+  return KVQ_OK;
+}
+
 int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_context_len) {
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||

@@ -90,6 +90,18 @@ struct DequantParams {
   int32_t B, Hkv, max_blocks, max_tok, num_blocks;
 };
 
+struct TrimParams {
+  int8_t* k_cache;
+  int8_t* v_cache;
+  uint16_t* k_scale;        // nullptr: a cache without scale planes (static scales)
+  uint16_t* v_scale;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* trim;      // [B] tokens to drop after the sink
+  unsigned int* err;
+  int32_t B, Hkv, max_blocks, max_tok, num_blocks, keep;
+};
+
 // decode (kvq_decode_int8.cu / kvq_decode_kv16.cu); D = head_dim, smem in bytes; maps =
 // {K tiles, V tiles}.
 size_t decode_smem_bytes_int8(int D, int B, int G);
@@ -114,6 +126,10 @@ cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, int sms, cu
 // dequantize-window baseline (kvq_dequant.cu)
 cudaError_t dequant_window_launch(int D, bool bf16, const DequantParams& p, int max_pages,
                                   cudaStream_t s);
+
+// front trim keeping the sink (kvq_trim.cu): moves the rows, then updates
+// context_lens (the same array as p.context_lens)
+cudaError_t trim_launch(int D, const TrimParams& p, int32_t* context_lens, cudaStream_t s);
 
 // quantize-append and twin append (kvq_quant.cu)
 cudaError_t quantize_append_launch(int D, bool bf16, const QuantParams& p, cudaStream_t s);
