@@ -71,6 +71,9 @@ def lib():
         L.orc_quantize_rows.argtypes = [vp, i64, i32, i32, vp, vp]; L.orc_quantize_rows.restype = None
         L.orc_quantize_rows_static.argtypes = [vp, i64, i32, i32, ctypes.c_float, vp]
         L.orc_quantize_rows_static.restype = None
+        L.orc_prefill_sequence.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, i32, f64,
+                                           vp, vp, vp, vp]
+        L.orc_prefill_sequence.restype = None
         L.orc_trim_keep_sink.argtypes = [vp, i64, i64, i64, i64, vp]
         L.orc_trim_keep_sink.restype = i64
         L.orc_dequantize_rows.argtypes = [vp, vp, i64, i32, i32, vp]
@@ -163,6 +166,29 @@ def quantize_rows_static(x_bits: np.ndarray, dtype: str, scale: float) -> np.nda
     lib().orc_quantize_rows_static(_p(x), x.size // D if D else 0, D, _is_bf16(dtype),
                                    float(np.float32(scale)), _p(q))
     return q
+
+
+def prefill_sequence(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, dtype: str,
+                     sm_scale: float, quantized: bool = True):
+    """Causal attention of a chunk's n query tokens [n, Hq, D] (the last n of
+    the sequence's L tokens k/v [L, Hkv, D]) over tokens 0..L-n+i ("fix(cuda/kv):
+    correct Int8 KV per-token scale ..." (mlxcel PR #717), "Server integration":
+    Int8 chunked prefill).  Returns (out float64 [n, Hq, D], out_bits)."""
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    n, Hq, D = q.shape
+    L, Hkv, _ = k.shape
+    if n > L or Hq % Hkv:
+        raise ValueError("need n <= L and Hq a multiple of Hkv")
+    out = np.empty((n, Hq, D), dtype=np.float64)
+    out_bits = np.empty((n, Hq, D), dtype=np.uint16)
+    work = np.empty(2 * max(L, 1) * D, dtype=np.float64)
+    qwork = np.empty(D, dtype=np.int8)
+    lib().orc_prefill_sequence(_p(q), _p(k), _p(v), L, n, Hq, Hkv, D, _is_bf16(dtype),
+                               int(bool(quantized)), float(sm_scale), _p(out), _p(out_bits),
+                               _p(work), _p(qwork))
+    return out, out_bits
 
 
 def trim_keep_sink(rows: np.ndarray, keep: int, n: int) -> np.ndarray:

@@ -396,6 +396,54 @@ void orc_decode_sequence(const uint16_t* q, const uint16_t* k,
   }
 }
 
+/* Chunked prefill over the same cache: "fix(cuda/kv): correct Int8 KV
+ * per-token scale ..." (mlxcel PR #717), "Server integration" -- Int8
+ * chunked prefill + decode.  Reading: the n query tokens of the chunk are the
+ * last n of the sequence's L tokens (already written), and query i (position
+ * p = L - n + i) attends causally to tokens 0..p:
+ *   out[i][h] = softmax_t<=p(sm_scale * q[i][h] . k_hat_t) . v_hat
+ * q: [n][Hq][D]; k, v: [L][Hkv][D]; out, out_bits: [n][Hq][D].  work holds
+ * 2 * L * D doubles (dequantized rows of one KV head at a time). */
+void orc_prefill_sequence(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t L,
+                          int64_t n, int Hq, int Hkv, int D, int is_bf16, int quantized,
+                          double sm_scale, double* out, uint16_t* out_bits, double* work,
+                          int8_t* qwork) {
+  int G = Hq / Hkv;
+  double* k_hat = work;
+  double* v_hat = work + L * (int64_t)D;
+  for (int j = 0; j < Hkv; ++j) {
+    for (int64_t t = 0; t < L; ++t) {
+      const uint16_t* kr = k + (t * Hkv + j) * (int64_t)D;
+      const uint16_t* vr = v + (t * Hkv + j) * (int64_t)D;
+      if (quantized) {
+        uint16_t sk = orc_token_scale(kr, D, is_bf16);
+        uint16_t sv = orc_token_scale(vr, D, is_bf16);
+        orc_quantize_row(kr, D, is_bf16, sk, qwork);
+        for (int d = 0; d < D; ++d) k_hat[t * D + d] = orc_dequant(qwork[d], sk);
+        orc_quantize_row(vr, D, is_bf16, sv, qwork);
+        for (int d = 0; d < D; ++d) v_hat[t * D + d] = orc_dequant(qwork[d], sv);
+      } else {
+        for (int d = 0; d < D; ++d) {
+          k_hat[t * D + d] = orc_bits_to_double(kr[d], is_bf16);
+          v_hat[t * D + d] = orc_bits_to_double(vr[d], is_bf16);
+        }
+      }
+    }
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t len = L - n + i + 1;              /* tokens 0..p */
+      for (int g = 0; g < G; ++g) {
+        const int h = j * G + g;
+        double qd[256];
+        const int64_t row = (i * Hq + h) * (int64_t)D;
+        for (int d = 0; d < D; ++d) qd[d] = orc_bits_to_double(q[row + d], is_bf16);
+        orc_attend_one(qd, k_hat, v_hat, len, D, D, sm_scale, out + row);
+        if (out_bits)
+          for (int d = 0; d < D; ++d) out_bits[row + d] = orc_from_double_rne(out[row + d], is_bf16);
+      }
+    }
+  }
+}
+
 /* Bytes of one cache page in the two layouts ([MI] "Precision & memory"):
  *   INT8: K and V payload (1 byte per element) + one FP16 scale per
  *         (KV head, token) for K and for V;

@@ -442,3 +442,35 @@ def test_trim_keep_sink_matches_page_examples_and_composes():
             one = oracle.trim_keep_sink(rows, keep, n1 + n2)
             assert np.array_equal(two, one)
             assert len(one) == 300 - (n1 + n2)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_prefill_matches_causal_torch_sdpa_and_decode(dtype):
+    """Chunked prefill: against torch's float64 scaled_dot_product_attention
+    with a causal mask offset by the cached prefix (GQA by repeat), over the
+    native values; its last query row equals the decode of the whole
+    sequence; a chunk of one query is the decode."""
+    r = np.random.default_rng(23)
+    L, n, Hkv, G, D = 70, 19, 2, 3, 64
+    Hq = Hkv * G
+    if dtype == "fp16":
+        mk = lambda *s: r.standard_normal(s).astype(np.float16).view(np.uint16)  # noqa: E731
+    else:
+        mk = lambda *s: torch.from_numpy(r.standard_normal(s).astype(np.float32)).to(  # noqa: E731
+            torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    k, v, q = mk(L, Hkv, D), mk(L, Hkv, D), mk(n, Hq, D)
+    sm = 0.11
+    out, _ = oracle.prefill_sequence(q, k, v, dtype, sm, quantized=False)
+    qt = torch.from_numpy(oracle.bits_to_double(q, dtype)).permute(1, 0, 2)       # [Hq, n, D]
+    kt = torch.from_numpy(oracle.bits_to_double(k, dtype)).permute(1, 0, 2).repeat_interleave(G, 0)
+    vt = torch.from_numpy(oracle.bits_to_double(v, dtype)).permute(1, 0, 2).repeat_interleave(G, 0)
+    pos = torch.arange(L - n, L)[:, None]
+    mask = torch.arange(L)[None, :] <= pos                                         # [n, L]
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=sm)
+    assert np.allclose(out, ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+    outq, _ = oracle.prefill_sequence(q, k, v, dtype, sm, quantized=True)
+    dec, _ = oracle.decode_sequence(q[-1], k, v, dtype, sm, quantized=True)
+    assert np.allclose(outq[-1], dec, rtol=0, atol=1e-13)
+    one, _ = oracle.prefill_sequence(q[:1], k[:L - n + 1], v[:L - n + 1], dtype, sm)
+    dec1, _ = oracle.decode_sequence(q[0], k[:L - n + 1], v[:L - n + 1], dtype, sm)
+    assert np.allclose(one[0], dec1, rtol=0, atol=1e-13)
