@@ -192,6 +192,40 @@ size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
                                         int32_t max_context_len, int32_t partition_pages);
 
 /*
+ * kvq_paged_prefill -- chunked-prefill attention over the INT8 cache: the
+ * queries of a chunk of new tokens per sequence, written into the cache
+ * before the call (kvq_quantize_append), attend causally to the sequence's
+ * cached tokens.  Defined by [ML] "Server integration" (Int8 chunked prefill
+ * + decode over the same cache) with [MI]'s dequantized attention:
+ *     n_b = query_start[b+1] - query_start[b] queries, the last n_b of the
+ *     sequence's L_b = context_lens[b] tokens; query i sits at position
+ *     p = L_b - n_b + i and attends to tokens 0..p:
+ *     out[query_start[b] + i][h] = softmax_{t<=p}(sm_scale q . k_hat_t) . v_hat
+ * Arithmetic: q and codes in FP16 on the tensor cores, FP32 accumulation and
+ * softmax, output rounded to `dtype`.
+ *
+ *   q, out          [total_q][num_q_heads][head_dim] of `dtype`, 16-byte aligned.
+ *   query_start     device int32 [num_seqs + 1], non-decreasing, from 0.
+ *   total_q         rows of q and out; a sequence whose queries fall outside
+ *                   them is flagged (KVQ_DEVERR_CONTEXT) and skipped.
+ *   max_query_len   host upper bound on every n_b (sizes the grid; a larger
+ *                   n_b is flagged and skipped).
+ *   other arguments as kvq_paged_decode (no workspace).
+ * Device errors: n_b > L_b or L_b above the table / max_context_len
+ * (KVQ_DEVERR_CONTEXT, that sequence's output unspecified), block id out of
+ * range (KVQ_DEVERR_BLOCK).
+ */
+kvq_status kvq_paged_prefill(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             const int8_t* k_cache, const int8_t* v_cache,
+                             const uint16_t* k_scale, const uint16_t* v_scale,
+                             int32_t num_blocks, int32_t block_size,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t max_context_len,
+                             const int32_t* query_start, int32_t total_q, int32_t max_query_len,
+                             float sm_scale, void* out, kvq_stream_t stream);
+
+/*
  * kvq_paged_decode_kv16 -- the same decode over a native 16-bit cache (K and
  * V in `dtype`, no scales); the A/B twin of kvq_paged_decode.  Arguments as
  * kvq_paged_decode; k_cache/v_cache are [num_blocks][num_kv_heads][16][D] of

@@ -30,6 +30,7 @@ __all__ = [
     "KvqError", "load", "kvq_quantize_append", "kvq_paged_decode", "kvq_paged_decode_kv16",
     "kvq_cache_append_kv16", "kvq_paged_decode_noalloc", "kvq_dequantize_window",
     "kvq_quantize_append_static", "kvq_paged_decode_static", "kvq_trim_front_keep_sink",
+    "kvq_paged_prefill",
     "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
     "kvq_get_error", "kvq_status_string", "alloc_int8_cache", "alloc_kv16_cache",
     "HEADER_SYMBOLS", "BLOCK_SIZE", "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_CONTEXT",
@@ -50,7 +51,7 @@ HEADER_SYMBOLS = (
     "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split", "kvq_cache_append_kv16",
     "kvq_get_error", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
     "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static",
-    "kvq_trim_front_keep_sink",
+    "kvq_trim_front_keep_sink", "kvq_paged_prefill",
 )
 
 _lib = None
@@ -91,6 +92,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.kvq_dequantize_window.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, i32, vp,
                                         i32, i32, vp, vp, vp]
     f32s = ctypes.c_float
+    L.kvq_paged_prefill.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32, vp,
+                                    i32, vp, i32, vp, i32, i32, f32s, vp, vp]
     L.kvq_trim_front_keep_sink.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, i32, vp,
                                            vp, i32, vp]
     L.kvq_quantize_append_static.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp, vp, vp,
@@ -100,7 +103,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     for fn in ("kvq_quantize_append", "kvq_cache_append_kv16", "kvq_paged_decode",
                "kvq_paged_decode_split", "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split",
                "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static",
-               "kvq_trim_front_keep_sink"):
+               "kvq_trim_front_keep_sink", "kvq_paged_prefill"):
         getattr(L, fn).restype = ctypes.c_int
     L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.kvq_decode_workspace_bytes.restype = sz
@@ -413,6 +416,38 @@ def kvq_trim_front_keep_sink(k_cache, v_cache, k_scale, v_scale, block_tables, c
                                     NB, bs, Hkv, D, _ptr(block_tables), B, block_tables.shape[1],
                                     _ptr(context_lens), _ptr(trim), int(keep), _stream(stream))
     _check(st, "kvq_trim_front_keep_sink")
+
+
+def kvq_paged_prefill(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                      query_start, max_context_len: int, max_query_len: int, sm_scale: float,
+                      out=None, stream=None):
+    """Chunked-prefill attention over the INT8 cache.  q [total_q, Hq, D]: the
+    queries of each sequence's last n_b = query_start[b+1] - query_start[b]
+    tokens (already in the cache), attending causally; returns out like q."""
+    L = load()
+    _need(q.is_cuda and q.dim() == 3 and q.is_contiguous(), "q must be contiguous [T, Hq, D]")
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    _check_cache(k_cache, v_cache, Hkv, D, (torch.int8,))
+    _check_scales(k_scale, v_scale, k_cache)
+    B = context_lens.shape[0]
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+          and block_tables.shape[0] == B and block_tables.is_contiguous(),
+          "block_tables must be contiguous int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.is_contiguous(),
+          "context_lens must be int32 [B]")
+    _need(query_start.dtype == torch.int32 and query_start.shape == (B + 1,)
+          and query_start.is_contiguous(), "query_start must be int32 [B + 1]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(), "out must match q")
+    st = L.kvq_paged_prefill(_ptr(q), _dtype_code(q), B, Hq, Hkv, D, _ptr(k_cache), _ptr(v_cache),
+                             _ptr(k_scale), _ptr(v_scale), NB, bs, _ptr(block_tables),
+                             block_tables.shape[1], _ptr(context_lens), int(max_context_len),
+                             _ptr(query_start), T, int(max_query_len), float(sm_scale),
+                             _ptr(out), _stream(stream))
+    _check(st, "kvq_paged_prefill")
+    return out
 
 
 def kvq_get_error(stream=None):

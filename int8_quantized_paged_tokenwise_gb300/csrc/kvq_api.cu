@@ -67,6 +67,9 @@ DeviceState* device_state() {
         return nullptr;
     }
   }
+  for (int D : {64, 128})
+    for (bool bf : {false, true})
+      if (prefill_configure(D, bf) != cudaSuccess) return nullptr;
   st.ready = true;
   return &st;
 }
@@ -628,6 +631,61 @@ kvq_status kvq_trim_front_keep_sink(int8_t* k_cache, int8_t* v_cache, uint16_t* 
   p.keep = keep;
   if (trim_launch(head_dim, p, context_lens, reinterpret_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
+    return cuda_fail();
+  return KVQ_OK;
+}
+
+kvq_status kvq_paged_prefill(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             const int8_t* k_cache, const int8_t* v_cache,
+                             const uint16_t* k_scale, const uint16_t* v_scale,
+                             int32_t num_blocks, int32_t block_size,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t max_context_len,
+                             const int32_t* query_start, int32_t total_q, int32_t max_query_len,
+                             float sm_scale, void* out, kvq_stream_t stream) {
+  kvq_status s = check_decode(q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
+                              v_cache, k_scale, v_scale, true, num_blocks, block_size,
+                              block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                              sm_scale, out);
+  if (s != KVQ_OK || num_seqs == 0) return s;
+  if (!query_start || !aligned(query_start, 4) || max_query_len < 0 || total_q < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (max_query_len == 0 || total_q == 0) return KVQ_OK;
+  if (num_kv_heads > 65535 || num_seqs > 65535 || max_blocks_per_seq > INT32_MAX / kBlockSize)
+    return KVQ_ERR_UNSUPPORTED;
+  DeviceState* st = device_state();
+  if (!st) return cuda_fail();
+  const int32_t G = num_q_heads / num_kv_heads;
+  const int64_t per_tile = 64 / G;               // queries per CTA tile
+  const int64_t tiles = cdiv(max_query_len, per_tile);
+  if (tiles > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+  CUtensorMap maps[2];
+  const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
+  if (!make_map(&maps[0], k_cache, 1, head_dim, rows) ||
+      !make_map(&maps[1], v_cache, 1, head_dim, rows))
+    return cuda_fail();
+  PrefillParams p{};
+  p.q = q;
+  p.out = out;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start = query_start;
+  p.err = st->err;
+  p.B = num_seqs;
+  p.Hq = num_q_heads;
+  p.Hkv = num_kv_heads;
+  p.G = G;
+  p.max_blocks = max_blocks_per_seq;
+  p.max_ctx = max_context_len;
+  p.num_blocks = num_blocks;
+  p.total_q = total_q;
+  p.max_q = max_query_len;
+  p.scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
+  if (prefill_launch(head_dim, dtype == KVQ_BF16, maps, p, (int)tiles,
+                     reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_fail();
   return KVQ_OK;
 }

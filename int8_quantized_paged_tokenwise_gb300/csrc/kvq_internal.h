@@ -102,6 +102,26 @@ struct TrimParams {
   int32_t B, Hkv, max_blocks, max_tok, num_blocks, keep;
 };
 
+struct PrefillParams {
+  const void* q;            // [total_q][Hq][D]
+  void* out;                // [total_q][Hq][D]
+  const uint16_t* k_scale;
+  const uint16_t* v_scale;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start;   // [B + 1]
+  unsigned int* err;
+  int32_t B, Hq, Hkv, G, max_blocks, max_ctx, num_blocks;
+  int32_t total_q, max_q;   // rows of q/out; host bound on a sequence's queries
+  float scale_log2;         // sm_scale * log2(e)
+};
+
+// chunked prefill (kvq_prefill.cu); grid = (tiles, Hkv, B)
+size_t prefill_smem_bytes(int D);
+cudaError_t prefill_configure(int D, bool bf16);
+cudaError_t prefill_launch(int D, bool bf16, const CUtensorMap* maps, const PrefillParams& p,
+                           int tiles, cudaStream_t s);
+
 // decode (kvq_decode_int8.cu / kvq_decode_kv16.cu); D = head_dim, smem in bytes; maps =
 // {K tiles, V tiles}.
 size_t decode_smem_bytes_int8(int D, int B, int G);
