@@ -238,15 +238,17 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         pa[h] = h2_as_u32(__floats2half2_rn(pr[0], pr[1]));
         pa[2 + h] = h2_as_u32(__floats2half2_rn(pr[2], pr[3]));
       }
+      if (__any_sync(0xFFFFFFFFu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-      for (int cb = 0; cb < D / 16; ++cb)
+        for (int cb = 0; cb < D / 16; ++cb)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          o[cb][e][0] *= alpha[0];
-          o[cb][e][1] *= alpha[0];
-          o[cb][e][2] *= alpha[1];
-          o[cb][e][3] *= alpha[1];
-        }
+          for (int e = 0; e < 2; ++e) {
+            o[cb][e][0] *= alpha[0];
+            o[cb][e][1] *= alpha[0];
+            o[cb][e][2] *= alpha[1];
+            o[cb][e][3] *= alpha[1];
+          }
+      }
       // ---------- O += P V: V pairs of tokens per head dim, times V scales ----------
       const uint32_t* vsc = reinterpret_cast<const uint32_t*>(sc + kBlockSize);
       const __half2 vs01 = u32_as_h2(vsc[c]), vs89 = u32_as_h2(vsc[4 + c]);
