@@ -510,7 +510,8 @@ def main():
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
         gbs, n, t = time_oracle(w, budget_s=12.0)
         cpu = {"value": round(gbs, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"first {n} of {w.num_seqs} sequences of the {w.name} workload "
+               "sample": f"{n} whole-sequence steps, cycling over the {w.num_seqs} sequences of "
+                         f"the {w.name} workload "
                          f"(quantize-append of the step token + decode of all heads), "
                          f"{t:.1f} s single-thread FP64"}
     if rank != 0:

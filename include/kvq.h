@@ -384,6 +384,13 @@ kvq_status kvq_paged_decode_noalloc(const void* q, kvq_dtype dtype, int32_t num_
  * set, else KVQ_ERR_DEVICE_INDEX. */
 kvq_status kvq_get_error(kvq_stream_t stream, uint32_t* flags);
 
+/* Self-test of the device-side failure path (no page defines it): one warp
+ * waits on an mbarrier that nothing completes, gives up after limit_us
+ * microseconds (1 .. 1,000,000) and sets KVQ_DEVERR_TIMEOUT, exactly as a
+ * kernel whose copies never landed would; the context stays usable.  Follow
+ * with kvq_get_error, which then returns KVQ_ERR_DEVICE_TIMEOUT. */
+kvq_status kvq_selftest_wait_timeout(uint32_t limit_us, kvq_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* kvq_status_string(kvq_status status);
 

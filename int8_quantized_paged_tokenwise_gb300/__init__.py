@@ -30,7 +30,7 @@ __all__ = [
     "KvqError", "load", "kvq_quantize_append", "kvq_paged_decode", "kvq_paged_decode_kv16",
     "kvq_cache_append_kv16", "kvq_paged_decode_noalloc", "kvq_dequantize_window",
     "kvq_quantize_append_static", "kvq_paged_decode_static", "kvq_trim_front_keep_sink",
-    "kvq_paged_prefill",
+    "kvq_paged_prefill", "kvq_selftest_wait_timeout",
     "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
     "kvq_get_error", "kvq_status_string", "alloc_int8_cache", "alloc_kv16_cache",
     "HEADER_SYMBOLS", "BLOCK_SIZE", "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_CONTEXT",
@@ -51,7 +51,7 @@ HEADER_SYMBOLS = (
     "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split", "kvq_cache_append_kv16",
     "kvq_get_error", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
     "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static",
-    "kvq_trim_front_keep_sink", "kvq_paged_prefill",
+    "kvq_trim_front_keep_sink", "kvq_paged_prefill", "kvq_selftest_wait_timeout",
 )
 
 _lib = None
@@ -111,6 +111,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.kvq_decode_workspace_bytes_split.restype = sz
     L.kvq_decode_partition_pages.argtypes = [i32, i32, i32, i32, i32]
     L.kvq_decode_partition_pages.restype = i32
+    L.kvq_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+    L.kvq_selftest_wait_timeout.restype = ctypes.c_int
     L.kvq_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.kvq_get_error.restype = ctypes.c_int
     L.kvq_status_string.argtypes = [ctypes.c_int]
@@ -448,6 +450,13 @@ def kvq_paged_prefill(q, k_cache, v_cache, k_scale, v_scale, block_tables, conte
                              _ptr(out), _stream(stream))
     _check(st, "kvq_paged_prefill")
     return out
+
+
+def kvq_selftest_wait_timeout(limit_us: int, stream=None):
+    """Launch the bounded-wait self-test (a wait that nothing completes, given
+    up after limit_us); read the result with kvq_get_error."""
+    _check(load().kvq_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "kvq_selftest_wait_timeout")
 
 
 def kvq_get_error(stream=None):

@@ -8,12 +8,27 @@
 
 #include "kvq.h"
 #include "kvq_internal.h"
+#include "kvq_ptx.cuh"
 
 using namespace kvq;
 
 // Per-device error word: kernels OR KVQ_DEVERR_* bits into it, kvq_get_error
 // reads and clears it.
 __device__ unsigned int g_kvq_error_word = 0u;
+
+namespace {
+// Self-test of the bounded wait every kernel uses: one warp waits on an
+// mbarrier that nothing arrives on, gives up after limit_ns, and reports it
+// through the error word, as a decode whose copies never landed would.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  __syncwarp();
+  const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, limit_ns);
+  if (!ok && threadIdx.x == 0) atomicOr(err, KVQ_DEVERR_TIMEOUT);
+}
+}  // namespace
 
 namespace {
 
@@ -731,6 +746,15 @@ size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
   return layout_for(num_seqs, G, head_dim,
                     balanced_units_max(st, num_seqs, num_kv_heads, G, head_dim, max_context_len))
       .total;
+}
+
+kvq_status kvq_selftest_wait_timeout(uint32_t limit_us, kvq_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return KVQ_ERR_INVALID_ARGUMENT;
+  DeviceState* st = device_state();
+  if (!st) return cuda_fail();
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      (uint64_t)limit_us * 1000u, st->err);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : cuda_fail();
 }
 
 kvq_status kvq_get_error(kvq_stream_t stream, uint32_t* flags) {
