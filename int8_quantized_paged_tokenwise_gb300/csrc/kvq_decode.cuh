@@ -26,7 +26,8 @@
 //  * each warp keeps one continuous stream of page loads across its pieces:
 //    lanes 0..5 issue, S pages ahead of the consumer, TMA copies of the
 //    (page, KV head) K and V tiles (2-D tensor copies with the 128-/64-byte
-//    swizzle so that the ldmatrix reads are bank-conflict free) and, for INT8,
+//    swizzle so that the ldmatrix reads are bank-conflict free, L2
+//    evict-first since each tile is read once per call) and, for INT8,
 //    the two 32-byte scale rows (1-D bulk copies), all completing on the
 //    stage's mbarrier; a piece's first page also brings its query rows.
 //    Block ids come from the block table 32 pages at a time, the next piece's
@@ -465,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
       if (blk >= 0) {
         const int row = blk * Hkv + is_j;             // (block, KV head) tile index
         if (lane < kTensorCopies) {
-          tma_load_2d(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * kBlockSize, bar);
+          tma_load_2d_evict_first(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * kBlockSize,
+                                  bar);
         } else if (INT8 && !STATIC && lane < kTensorCopies + 2) {
           bulk_load(sc_dst + s * C::kScaleBytes, sc_src + (int64_t)row * kBlockSize,
                     kBlockSize * 2, bar);

@@ -107,6 +107,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same copy with an L2 evict-first policy: for data read once per call
+// (the K/V pages of a decode), so that its lines are the first to go instead
+// of lines other kernels still use or have yet to write back.
+__device__ __forceinline__ void tma_load_2d_evict_first(uint32_t dst, const CUtensorMap* map,
+                                                        int32_t x, int32_t y, uint32_t bar) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 // 1-D bulk copy; dst, src 16-byte aligned and bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
