@@ -672,7 +672,7 @@ kvq_status kvq_paged_prefill(const void* q, kvq_dtype dtype, int32_t num_seqs,
   DeviceState* st = device_state();
   if (!st) return cuda_fail();
   const int32_t G = num_q_heads / num_kv_heads;
-  const int64_t per_tile = 64 / G;               // queries per CTA tile
+  const int64_t per_tile = prefill_rows_per_cta() / G;   // queries per CTA tile
   const int64_t tiles = cdiv(max_query_len, per_tile);
   if (tiles > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
   CUtensorMap maps[2];

@@ -118,6 +118,7 @@ struct PrefillParams {
 
 // chunked prefill (kvq_prefill.cu); grid = (tiles, Hkv, B)
 size_t prefill_smem_bytes(int D);
+int prefill_rows_per_cta();   // (query, head) rows of one CTA tile
 cudaError_t prefill_configure(int D, bool bf16);
 cudaError_t prefill_launch(int D, bool bf16, const CUtensorMap* maps, const PrefillParams& p,
                            int tiles, cudaStream_t s);

@@ -1,4 +1,5 @@
-// Chunked-prefill attention over the tokenwise INT8 paged cache.
+// Chunked-prefill attention over the tokenwise INT8 paged cache, on the
+// 5th-generation tensor cores (tcgen05 MMAs with TMEM accumulators).
 //
 // What it computes ("fix(cuda/kv): correct Int8 KV per-token scale ..."
 // (mlxcel PR #717), "Server integration": Int8 chunked prefill + decode over
@@ -7,338 +8,481 @@
 // p = L - n + i attends causally to tokens 0..p:
 //   out[i][h] = softmax_{t<=p}(sm_scale * q[i][h] . s_k[t] code_k[t]) . (s_v code_v)
 //
-// A real dense contraction, so the whole tile works on the tensor cores:
-//  * CTA = (query tile, KV head, sequence); its 64 rows are (query, head of
-//    the GQA group) pairs, 16 per warp, so each K/V page is read once for all
-//    of them.  The Q tile is converted to FP16 once and its MMA A fragments
-//    stay in registers.
-//  * pages stream through an S-stage ring shared by the CTA's 4 warps: warp 0
-//    issues the TMA copies (K and V tiles, 128/64-byte swizzle) and the two
-//    32-byte scale rows, all completing on the stage's mbarrier; a block
-//    barrier per page frees the stage.
-//  * S = Q K^T with K as the B operand: codes become exact FP16 integers in
-//    registers (byte permute under exponent 0x64, minus 1152); the head dims
-//    are taken in the order {4c, 4c+1, 4c+2, 4c+3} <-> MMA k {2c, 2c+1, 2c+8,
-//    2c+9} on both operands, so each ldmatrix word is one B fragment pair.
-//  * K scales and sm_scale*log2(e) scale the FP32 scores; causal mask; online
-//    softmax per row (quad shuffles); P stays in registers as the A operand of
-//    P V; V pairs of consecutive tokens come from ldmatrix.trans, multiplied by
-//    their V scales; O accumulates in FP32.
+// One CTA = 128 (query, head-of-the-GQA-group) rows of one KV head of one
+// sequence (M = 128 of every MMA), streaming the sequence's tokens in tiles
+// of 64 (4 pages).  Warp roles:
+//  * warp 4, producer: block ids from the block table, TMA copies of each
+//    page's INT8 K and V tiles (2-D tensor copies, 128-/64-byte swizzle) and
+//    bulk copies of its two 32-byte scale rows into a 3-stage ring;
+//  * warps 6-9, converters: INT8 codes to exact FP16 integers (byte permute
+//    under exponent 0x64, minus 1152), K as a K-major [64 tokens][D] operand
+//    and V transposed to a K-major [D][64 tokens] operand, both 128-byte
+//    swizzled, double-buffered; the tile's K scales (times sm_scale log2 e)
+//    and V scales as FP32 columns;
+//  * warp 5, MMA issuer (one thread): S = Q K^T into one of two 128 x 64
+//    FP32 TMEM buffers (8 MMAs of K = 16 over the head dims), and, one tile
+//    behind, O += P V into a 128 x D FP32 TMEM accumulator (4 MMAs over the
+//    tokens), each group's completion signalled through tcgen05.commit;
+//  * warps 0-3, softmax (one thread per row = TMEM lane): the row of S,
+//    times the K-scale column, causal mask, running maximum, P = 2^(z - m)
+//    with the V scale of each token folded in (P' = P s_v, FP16, written as
+//    the K-major A operand of the next P V), row sums in FP32; O is rescaled
+//    in TMEM only when a row maximum grows by more than 2^8 over the one in
+//    use (the shift cancels in O / l, and P' stays below 2^8 s_v), and
+//    normalized and stored at the end.
+// All waits are bounded: a timeout sets an error bit, the roles leave their
+// loops, the copies and MMAs in flight are waited for, and TMEM is freed.
 #include "kvq_decode.cuh"
+#include "kvq_tc.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr int kPfWarps = 4;
-constexpr int kPfThreads = kPfWarps * 32;
-constexpr int kPfRows = 16 * kPfWarps;   // (query, head) rows per CTA
-constexpr int kPfStages = 4;
+constexpr int kTcRows = 128;                    // M: (query, head) rows per CTA
+constexpr int kTcKv = 64;                       // tokens per KV tile
+constexpr int kTcPages = kTcKv / kBlockSize;     // pages per KV tile
+constexpr int kTcRaw = 3;                       // INT8 staging ring depth
+constexpr int kTcWarps = 10;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kWarpTma = 4, kWarpMma = 5, kWarpCvt = 6;
+constexpr uint32_t kTcCols = 256;               // TMEM: O (D columns) + 2 S buffers of 64
 
+// barrier indices
+constexpr int kBarRawFull = 0, kBarRawEmpty = 3, kBarCvtFull = 6, kBarCvtEmpty = 8,
+              kBarSFull = 10, kBarPFull = 12, kBarPvDone = 14, kBarFin = 16, kNumBars = 17;
+
+// Shared memory (offsets from a 1024-aligned base; every operand tile starts
+// on a 1024-byte boundary).
 template <int D>
-struct PfLayout {
-  using C = TileCfg<D, true>;
-  static constexpr int kQStride = D * 2 + 32;               // bytes per Q row (padded)
-  static constexpr int kStage = 2 * C::kTile;               // K tile, V tile
-  static constexpr size_t kTiles = 0;
-  static constexpr size_t kScales = kTiles + (size_t)kPfStages * kStage;
-  static constexpr size_t kQ = kScales + (size_t)kPfStages * 64;
-  static constexpr size_t kBars = kQ + (size_t)kPfRows * kQStride;
-  static constexpr size_t kTotal = kBars + kPfStages * 8 + 1024;   // + base alignment slack
+struct TcLayout {
+  static constexpr int kQ = 0;                            // [128][D] FP16, D/64 tiles of 16 KB
+  static constexpr int kKcBytes = kTcKv * D * 2;         // [64][D] FP16, D/64 tiles of 8 KB
+  static constexpr int kKc = kQ + kTcRows * D * 2;       // 2 buffers
+  static constexpr int kVtBytes = D * kTcKv * 2;         // [D][64] FP16, one tile of D x 128 B
+  static constexpr int kVt = kKc + 2 * kKcBytes;         // 2 buffers
+  static constexpr int kPBytes = kTcRows * kTcKv * 2;    // [128][64] FP16
+  static constexpr int kP = kVt + 2 * kVtBytes;          // 2 buffers
+  static constexpr int kTile = kBlockSize * D;           // one page's INT8 K (or V) tile
+  static constexpr int kRawBytes = 2 * kTcPages * kTile; // K tiles of 4 pages, then V tiles
+  static constexpr int kRaw = kP + 2 * kPBytes;          // kTcRaw stages
+  static constexpr int kRawSc = kRaw + kTcRaw * kRawBytes;        // per page: K 32 B, V 32 B
+  static constexpr int kColSc = kRawSc + kTcRaw * kTcPages * 64;  // 2 x (K 64, V 64 floats)
+  static constexpr int kBars = kColSc + 2 * 2 * kTcKv * 4;
+  static constexpr int kMisc = kBars + kNumBars * 8;     // TMEM base, abort flag
+  static constexpr size_t kTotal = (size_t)kMisc + 16 + 1024;     // + base alignment slack
 };
 
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v) {
+  return h2_as_u32(__floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)));
+}
+
+// 4 x 4 byte transpose: out[d] = byte d of a0, a1, a2, a3.
+__device__ __forceinline__ void transpose4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t (&out)[4]) {
+  const uint32_t x01 = __byte_perm(a0, a1, 0x5140), y01 = __byte_perm(a0, a1, 0x7362);
+  const uint32_t x23 = __byte_perm(a2, a3, 0x5140), y23 = __byte_perm(a2, a3, 0x7362);
+  out[0] = __byte_perm(x01, x23, 0x5410);
+  out[1] = __byte_perm(x01, x23, 0x7632);
+  out[2] = __byte_perm(y01, y23, 0x5410);
+  out[3] = __byte_perm(y01, y23, 0x7632);
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kPfThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using C = TileCfg<D, true>;
-  using Ly = PfLayout<D>;
-  constexpr int KSTEPS = D / 16;
+  using Ly = TcLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kBars);
-  __shared__ int s_blk[kPfStages];               // block id of the page in each stage (-1: none)
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Ly::kMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, c = lane & 3;
   const int b = blockIdx.z, j = blockIdx.y, G = p.G;
-  const int TQ = kPfRows / G;                     // queries per tile
-  const int qt = blockIdx.x;
+  const int TQ = kTcRows / G;                     // queries per tile
+  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;   // latest (longest) tiles first
 
   if (tid == 0) {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
+    misc[1] = 0;
   }
-  if (tid < kPfStages) mbar_init(smem_u32(&bars[tid]), 1);
+  if (tid < kNumBars) {
+    const bool quad = (tid >= kBarRawEmpty && tid < kBarRawEmpty + kTcRaw) ||
+                      (tid >= kBarCvtFull && tid < kBarCvtFull + 2) ||
+                      (tid >= kBarPFull && tid < kBarPFull + 2);
+    mbar_init(bar(tid), quad ? 4 : 1);            // per-warp arrivals of 4 warps, else one
+  }
   griddep_wait();
-  fence_mbar_init();
 
   const int q0 = __ldg(&p.query_start[b]);
   const int n = __ldg(&p.query_start[b + 1]) - q0;
-  int L = __ldg(&p.context_lens[b]);
+  const int L = __ldg(&p.context_lens[b]);
   const int max_tok = min(p.max_blocks * kBlockSize, p.max_ctx);
   if (L < 0 || L > max_tok || n < 0 || n > L || n > p.max_q || q0 < 0 || q0 + n > p.total_q) {
     if (tid == 0 && qt == 0 && j == 0) atomicOr(p.err, 0x4u);
-    return;                                      // no copies issued yet
+    return;                                      // nothing issued or allocated yet
   }
   const int i_begin = qt * TQ;
   if (i_begin >= n) return;
   const int i_end = min(n, i_begin + TQ);
   const int p_last = L - n + i_end - 1;          // last query position of the tile
+  const int n_it = p_last / kTcKv + 1;           // KV tiles
   const int npages = p_last / kBlockSize + 1;
 
-  // ---- Q tile: rows r = (query i_begin + r / G, head j*G + r % G), as FP16 ----
-  uint8_t* qs = smem + Ly::kQ;
-  for (int e = tid; e < kPfRows * (D / 4); e += kPfThreads) {
-    const int r = e / (D / 4), d4 = e - r * (D / 4);
+  if (warp == kWarpMma) tc_alloc(smem_u32(&misc[0]), kTcCols);
+
+  // ---- Q tile: row r = (query i_begin + r / G, head j G + r % G), FP16, swizzled ----
+  for (int e = tid; e < kTcRows * (D / 8); e += kTcThreads) {
+    const int r = e / (D / 8), c8 = e - r * (D / 8);    // 16-byte chunk c8 of the row
     const int i = i_begin + r / G;
-    uint2 v = make_uint2(0, 0);
+    uint4 v = make_uint4(0, 0, 0, 0);
     if (r < TQ * G && i < i_end) {
       const uint16_t* src = static_cast<const uint16_t*>(p.q) +
-                            ((int64_t)(q0 + i) * p.Hq + (int64_t)j * G + r % G) * D + 4 * d4;
-      v = __ldg(reinterpret_cast<const uint2*>(src));
+                            ((int64_t)(q0 + i) * p.Hq + (int64_t)j * G + r % G) * D + 8 * c8;
+      v = __ldg(reinterpret_cast<const uint4*>(src));
       if constexpr (BF16) {
-        v.x = h2_as_u32(__floats2half2_rn(__uint_as_float(v.x << 16),
-                                          __uint_as_float(v.x & 0xFFFF0000u)));
-        v.y = h2_as_u32(__floats2half2_rn(__uint_as_float(v.y << 16),
-                                          __uint_as_float(v.y & 0xFFFF0000u)));
+        v.x = bf2_to_h2(v.x);
+        v.y = bf2_to_h2(v.y);
+        v.z = bf2_to_h2(v.z);
+        v.w = bf2_to_h2(v.w);
       }
     }
-    *reinterpret_cast<uint2*>(qs + r * Ly::kQStride + 8 * d4) = v;
+    *reinterpret_cast<uint4*>(smem + Ly::kQ + (c8 >> 3) * (kTcRows * 128) + r * 128 +
+                              (((c8 & 7) ^ (r & 7)) << 4)) = v;
   }
+  fence_proxy_async_smem();
+  fence_mbar_init();
+  tc_fence_before();
   __syncthreads();
-  // A fragments of this warp's 16 rows: per k-step, rows g / g+8, 8 bytes at d = 16ks + 4c
-  uint32_t qa[KSTEPS][4];
-  {
-    const uint8_t* r0 = qs + (16 * warp + g) * Ly::kQStride;
-    const uint8_t* r8 = r0 + 8 * Ly::kQStride;
-#pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-      const uint2 lo = *reinterpret_cast<const uint2*>(r0 + 32 * ks + 8 * c);
-      const uint2 hi = *reinterpret_cast<const uint2*>(r8 + 32 * ks + 8 * c);
-      qa[ks][0] = lo.x;   // row g,   k {2c, 2c+1}
-      qa[ks][1] = hi.x;   // row g+8
-      qa[ks][2] = lo.y;   // row g,   k {2c+8, 2c+9}
-      qa[ks][3] = hi.y;   // row g+8
-    }
-  }
-  // positions of the thread's two rows (-1: padding row, attends nothing)
-  int pos[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = 16 * warp + g + 8 * h;
-    const int i = i_begin + r / G;
-    pos[h] = (r < TQ * G && i < i_end) ? L - n + i : -1;
-  }
-
-  // ---- producer (warp 0): block ids 32 pages at a time, copies by lanes 0..3 ----
-  const uint32_t tiles_u32 = smem_u32(smem + Ly::kTiles);
-  const uint32_t scales_u32 = smem_u32(smem + Ly::kScales);
-  const int32_t* bt = p.block_tables + (int64_t)b * p.max_blocks;
-  int blk_chunk = -1, chunk_base = -32;
-  auto issue = [&](int k) {                      // warp 0 only; page k into stage k % S
-    // (s_blk is written before the arrive, which releases it to the waiting warps)
-    if (k >= chunk_base + 32) {
-      chunk_base = k - k % 32;
-      const int pg = chunk_base + lane;
-      blk_chunk = -1;
-      if (pg < npages) {
-        blk_chunk = __ldg(&bt[pg]);
-        if (blk_chunk < 0 || blk_chunk >= p.num_blocks) {
-          atomicOr(p.err, 0x2u);
-          blk_chunk = -1;
-        }
-      }
-    }
-    const int blk = __shfl_sync(0xFFFFFFFFu, blk_chunk, k - chunk_base);
-    const int s = k % kPfStages;
-    const uint32_t bar = smem_u32(&bars[s]);
-    if (lane == 0) {
-      s_blk[s] = blk;
-      if (blk >= 0) mbar_arrive_expect_tx(bar, 2 * C::kTile + 64);
-      else mbar_arrive(bar);
-    }
-    if (blk >= 0) {
-      const int row = (blk * p.Hkv + j) * kBlockSize;
-      const int64_t srow = (int64_t)(blk * p.Hkv + j) * kBlockSize;
-      if (lane == 0) tma_load_2d(tiles_u32 + s * Ly::kStage, &tmK, 0, row, bar);
-      else if (lane == 1) tma_load_2d(tiles_u32 + s * Ly::kStage + C::kTile, &tmV, 0, row, bar);
-      else if (lane == 2) bulk_load(scales_u32 + s * 64, p.k_scale + srow, 32, bar);
-      else if (lane == 3) bulk_load(scales_u32 + s * 64 + 32, p.v_scale + srow, 32, bar);
-    }
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint32_t tO = tmem, tS = tmem + D;        // S buffer k at tS + 64 k
+  auto fail = [&]() {
+    atomicOr(p.err, 0x8u);
+    *abort_flag = 1;
   };
-  int k_next = 0;                                // next page to issue (warp 0)
-  if (warp == 0)
-    for (; k_next < kPfStages && k_next < npages; ++k_next) issue(k_next);
 
-  // ---- consumer: all warps ----
-  float o[D / 16][2][4];                          // [16-dim block][even/odd dims][quad]
-#pragma unroll
-  for (int cb = 0; cb < D / 16; ++cb)
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-#pragma unroll
-      for (int x = 0; x < 4; ++x) o[cb][e][x] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  const int lt = (lane & 7) + ((lane >> 3) & 1) * 8;
-  bool aborted = false;
-  int k = 0;
-  for (; k < npages; ++k) {
-    const int s = k % kPfStages;
-    if (!mbar_wait_bounded(smem_u32(&bars[s]), (k / kPfStages) & 1)) aborted = true;
-    if (!aborted && s_blk[s] >= 0) {
-      const uint32_t kt = tiles_u32 + s * Ly::kStage, vt = kt + C::kTile;
-      const uint16_t* sc = reinterpret_cast<const uint16_t*>(smem + Ly::kScales + s * 64);
-      // ---------- S = Q K^T: n-tile 0 = tokens 0-7, n-tile 1 = tokens 8-15 ----------
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS / 2; ++kk) {
-        uint32_t r0, r1, r2, r3;   // (tok 0-7, k-step 2kk), (8-15, 2kk), (0-7, 2kk+1), (8-15, 2kk+1)
-        ldsm_x4(kt + tile_off<C>(lt, 2 * kk + (lane >> 4)), r0, r1, r2, r3);
-        uint32_t b0, b1;
-        i8x4_to_h2x2<0x4140u, 0x4342u>(r0, b0, b1);
-        mma_16816_acc<false>(s0, qa[2 * kk][0], qa[2 * kk][1], qa[2 * kk][2], qa[2 * kk][3], b0, b1);
-        i8x4_to_h2x2<0x4140u, 0x4342u>(r1, b0, b1);
-        mma_16816_acc<false>(s1, qa[2 * kk][0], qa[2 * kk][1], qa[2 * kk][2], qa[2 * kk][3], b0, b1);
-        i8x4_to_h2x2<0x4140u, 0x4342u>(r2, b0, b1);
-        mma_16816_acc<false>(s0, qa[2 * kk + 1][0], qa[2 * kk + 1][1], qa[2 * kk + 1][2],
-                             qa[2 * kk + 1][3], b0, b1);
-        i8x4_to_h2x2<0x4140u, 0x4342u>(r3, b0, b1);
-        mma_16816_acc<false>(s1, qa[2 * kk + 1][0], qa[2 * kk + 1][1], qa[2 * kk + 1][2],
-                             qa[2 * kk + 1][3], b0, b1);
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ producer
+    const int32_t* bt = p.block_tables + (int64_t)b * p.max_blocks;
+    const uint32_t raw_u32 = smem_u32(smem + Ly::kRaw);
+    const uint32_t rawsc_u32 = smem_u32(smem + Ly::kRawSc);
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % kTcRaw;
+      if (it >= kTcRaw && !mbar_wait_bounded(bar(kBarRawEmpty + s), ((it / kTcRaw) - 1) & 1)) {
+        if (lane == 0) fail();
+        break;
       }
-      // scores in log2 units; the thread's tokens: 2c, 2c+1 (s0) and 8+2c, 9+2c (s1)
-      const int t0 = k * kBlockSize;
-      float z[2][4];                              // [row g / g+8][tok 2c, 2c+1, 8+2c, 9+2c]
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int tok = (x < 2 ? 2 * c + x : 8 + 2 * c + (x - 2));
-        const float ks = p.scale_log2 * __half2float(__ushort_as_half(sc[tok]));
-        const float v0 = x < 2 ? s0[x] : s1[x - 2];
-        const float v8 = x < 2 ? s0[2 + x] : s1[x];
-        z[0][x] = t0 + tok <= pos[0] ? v0 * ks : -INFINITY;
-        z[1][x] = t0 + tok <= pos[1] ? v8 * ks : -INFINITY;
+      if (*abort_flag) break;
+      // lanes 4 k + pg: page pg of the tile, copy k (K tile, V tile, K scales, V scales)
+      const int pg = it * kTcPages + (lane & 3);
+      int blk = -1;
+      if (lane < 4 * kTcPages && pg < npages) {
+        blk = __ldg(&bt[pg]);
+        if (blk < 0 || blk >= p.num_blocks) {
+          if (lane < 4) atomicOr(p.err, 0x2u);
+          blk = -1;
+        }
       }
-      // ---------- online softmax per row (reduce over the quad) ----------
-      uint32_t pa[4];                             // A fragments of P (16 rows x 16 tokens)
-      float alpha[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float mx = fmaxf(fmaxf(z[h][0], z[h][1]), fmaxf(z[h][2], z[h][3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-        const float mn = fmaxf(m[h], mx);
-        const float ref = mn == -INFINITY ? 0.f : mn;
-        alpha[h] = fast_exp2(m[h] - ref);
-        float pr[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) pr[x] = fast_exp2(z[h][x] - ref);
-        l[h] = l[h] * alpha[h] + (pr[0] + pr[1] + pr[2] + pr[3]);
-        m[h] = mn;
-        // a0 / a1: rows g / g+8, tokens 2c, 2c+1; a2 / a3: tokens 8+2c, 9+2c
-        pa[h] = h2_as_u32(__floats2half2_rn(pr[0], pr[1]));
-        pa[2 + h] = h2_as_u32(__floats2half2_rn(pr[2], pr[3]));
+      const uint32_t loaded = __ballot_sync(0xFFFFFFFFu, lane < kTcPages && blk >= 0);
+      const uint32_t full = bar(kBarRawFull + s);
+      if (lane == 0) {
+        const uint32_t tx = (uint32_t)__popc(loaded) * (2u * Ly::kTile + 64u);
+        if (tx) mbar_arrive_expect_tx(full, tx);
+        else mbar_arrive(full);
       }
-      if (__any_sync(0xFFFFFFFFu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+      __syncwarp();
+      if (lane < 4 * kTcPages && blk >= 0) {
+        const int k = lane >> 2, pgl = lane & 3;
+        const int row = blk * p.Hkv + j;            // (block, KV head) tile index
+        const uint32_t stage = raw_u32 + s * Ly::kRawBytes;
+        if (k == 0) tma_load_2d(stage + pgl * Ly::kTile, &tmK, 0, row * kBlockSize, full);
+        else if (k == 1)
+          tma_load_2d(stage + (kTcPages + pgl) * Ly::kTile, &tmV, 0, row * kBlockSize, full);
+        else
+          bulk_load(rawsc_u32 + (s * kTcPages + pgl) * 64 + (k - 2) * 32,
+                    (k == 2 ? p.k_scale : p.v_scale) + (int64_t)row * kBlockSize, 32, full);
+      }
+      issued = it + 1;
+    }
+    // copies still in flight (the last stages issued) land before the CTA exits
+    for (int it = issued > kTcRaw ? issued - kTcRaw : 0; it < issued; ++it)
+      mbar_wait_bounded(bar(kBarRawFull + it % kTcRaw), (it / kTcRaw) & 1);
+  } else if (warp >= kWarpCvt) {
+    // ---------------------------------------------------------- converters
+    const int ct = tid - kWarpCvt * 32;           // 0..127
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % kTcRaw, kb = it & 1;
+      if (!mbar_wait_bounded(bar(kBarRawFull + s), (it / kTcRaw) & 1) ||
+          (it >= 2 && !mbar_wait_bounded(bar(kBarCvtEmpty + kb), ((it - 2) >> 1) & 1))) {
+        if (lane == 0) fail();
+        break;
+      }
+      if (*abort_flag) break;
+      const uint8_t* rawK = smem + Ly::kRaw + s * Ly::kRawBytes;
+      const uint8_t* rawV = rawK + kTcPages * Ly::kTile;
+      uint8_t* kc = smem + Ly::kKc + kb * Ly::kKcBytes;
+      uint8_t* vt = smem + Ly::kVt + kb * Ly::kVtBytes;
+      // K: 16 codes (chunk c of token t) -> FP16 chunks 2c, 2c+1 of row t
 #pragma unroll
-        for (int cb = 0; cb < D / 16; ++cb)
+      for (int pass = 0; pass < kTcKv * (D / 16) / 128; ++pass) {
+        const int e = ct + 128 * pass;
+        const int t = e / (D / 16), c = e - t * (D / 16);
+        const uint4 w = *reinterpret_cast<const uint4*>(rawK + (t >> 4) * Ly::kTile +
+                                                        tile_off<C>(t & 15, c));
+        uint4 lo, hi;
+        i8x4_to_h2x2<0x4140u, 0x4342u>(w.x, lo.x, lo.y);
+        i8x4_to_h2x2<0x4140u, 0x4342u>(w.y, lo.z, lo.w);
+        i8x4_to_h2x2<0x4140u, 0x4342u>(w.z, hi.x, hi.y);
+        i8x4_to_h2x2<0x4140u, 0x4342u>(w.w, hi.z, hi.w);
+        uint8_t* row = kc + (c >> 2) * (kTcKv * 128) + t * 128;
+        const int c0 = (2 * c) & 7;
+        *reinterpret_cast<uint4*>(row + ((c0 ^ (t & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (t & 7)) << 4)) = hi;
+      }
+      // V: head dims 4dg..4dg+3 of tokens 8tg..8tg+7 -> rows 4dg.. of V^T, chunk tg;
+      // a warp covers 8 dim groups x 4 token groups per pass
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            o[cb][e][0] *= alpha[0];
-            o[cb][e][1] *= alpha[0];
-            o[cb][e][2] *= alpha[1];
-            o[cb][e][3] *= alpha[1];
+      for (int pass = 0; pass < (D / 4) * (kTcKv / 8) / 128; ++pass) {
+        const int e = ct + 128 * pass;
+        const int wt = e >> 5;
+        const int dg = (e & 7) + 8 * (wt % (D / 32));
+        const int tg = ((e >> 3) & 3) + 4 * (wt / (D / 32));
+        uint32_t a[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int t = 8 * tg + k;
+          a[k] = *reinterpret_cast<const uint32_t*>(rawV + (t >> 4) * Ly::kTile +
+                                                    tile_off<C>(t & 15, dg >> 2) + 4 * (dg & 3));
+        }
+        uint32_t lo[4], hi[4];
+        transpose4(a[0], a[1], a[2], a[3], lo);
+        transpose4(a[4], a[5], a[6], a[7], hi);
+#pragma unroll
+        for (int dd = 0; dd < 4; ++dd) {
+          uint4 o;
+          i8x4_to_h2x2<0x4140u, 0x4342u>(lo[dd], o.x, o.y);
+          i8x4_to_h2x2<0x4140u, 0x4342u>(hi[dd], o.z, o.w);
+          const int d = 4 * dg + dd;
+          *reinterpret_cast<uint4*>(vt + d * 128 + ((tg ^ (d & 7)) << 4)) = o;
+        }
+      }
+      // scale columns: K (times sm_scale log2 e) for ct < 64, V for the others
+      {
+        const uint16_t* rs =
+            reinterpret_cast<const uint16_t*>(smem + Ly::kRawSc) + s * kTcPages * 32;
+        float* cs = reinterpret_cast<float*>(smem + Ly::kColSc) + kb * 2 * kTcKv;
+        const int t = ct & (kTcKv - 1), kind = ct >> 6;
+        const float sv = __half2float(__ushort_as_half(rs[(t >> 4) * 32 + kind * 16 + (t & 15)]));
+        cs[kind * kTcKv + t] = kind == 0 ? sv * p.scale_log2 : sv;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(kBarCvtFull + kb));
+        mbar_arrive(bar(kBarRawEmpty + s));
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = tc_idesc_f16(kTcKv, false);
+      constexpr uint32_t idO = tc_idesc_f16(D, false);
+      const uint32_t q_u32 = smem_u32(smem + Ly::kQ);
+      auto issue_pv = [&](int k) -> bool {
+        const int kb = k & 1;
+        if (!mbar_wait_bounded(bar(kBarPFull + kb), (k >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t pa = smem_u32(smem + Ly::kP + kb * Ly::kPBytes);
+        const uint32_t vb = smem_u32(smem + Ly::kVt + kb * Ly::kVtBytes);
+#pragma unroll
+        for (int ts = 0; ts < kTcKv / 16; ++ts)
+          tc_mma_f16(tO, tc_desc_sw128(pa + 32 * ts), tc_desc_sw128(vb + 32 * ts), idO,
+                     k > 0 || ts > 0);
+        tc_commit(bar(kBarPvDone + kb));
+        tc_commit(bar(kBarCvtEmpty + kb));
+        return true;
+      };
+      bool good = true;
+      for (int it = 0; it < n_it; ++it) {
+        const int kb = it & 1;
+        if (!mbar_wait_bounded(bar(kBarCvtFull + kb), (it >> 1) & 1) || *abort_flag) {
+          good = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(smem + Ly::kKc + kb * Ly::kKcBytes);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_f16(tS + kTcKv * kb,
+                     tc_desc_sw128(q_u32 + (ks >> 2) * (kTcRows * 128) + 32 * (ks & 3)),
+                     tc_desc_sw128(kbase + (ks >> 2) * (kTcKv * 128) + 32 * (ks & 3)), idS,
+                     ks > 0);
+        tc_commit(bar(kBarSFull + kb));
+        if (it > 0 && !issue_pv(it - 1)) {
+          good = false;
+          break;
+        }
+      }
+      if (good && !issue_pv(n_it - 1)) good = false;
+      if (!good) fail();
+      tc_commit(bar(kBarFin));                    // every MMA issued has completed
+      mbar_wait_bounded(bar(kBarFin), 0);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------- softmax
+    const int r = tid;                            // row = TMEM lane
+    const int iq = i_begin + r / G;
+    const int pos = (r < TQ * G && iq < i_end) ? L - n + iq : -1;   // -1: padding row
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    float m_use = -INFINITY, l = 0.f;
+    bool good = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int kb = it & 1;
+      bool w_ok = mbar_wait_bounded(bar(kBarCvtFull + kb), (it >> 1) & 1) &&
+                  mbar_wait_bounded(bar(kBarSFull + kb), (it >> 1) & 1);
+      if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+        good = false;
+        break;
+      }
+      tc_fence_after();
+      const float* cs = reinterpret_cast<const float*>(smem + Ly::kColSc) + kb * 2 * kTcKv;
+      const int t0 = it * kTcKv;
+      float z[kTcKv];
+#pragma unroll
+      for (int h = 0; h < kTcKv / 32; ++h) {
+        uint32_t sr[32];
+        tc_ld32(tS + kTcKv * kb + 32 * h + lanes, sr);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int t = 32 * h + x;
+          z[t] = t0 + t <= pos ? __uint_as_float(sr[x]) * cs[t] : -INFINITY;
+        }
+      }
+      float mx = z[0];
+#pragma unroll
+      for (int t = 1; t < kTcKv; ++t) mx = fmaxf(mx, z[t]);
+      const bool grow = mx > m_use + 8.f;
+      const float m_new = grow ? mx : m_use;
+      const bool resc = grow && m_use != -INFINITY;
+      if (__any_sync(0xFFFFFFFFu, resc)) {
+        // O holds P V of tiles 0..it-1: once the last has completed, rescale
+        // the rows whose maximum moved
+        w_ok = mbar_wait_bounded(bar(kBarPvDone + ((it - 1) & 1)), ((it - 1) >> 1) & 1);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+          good = false;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = resc ? fast_exp2(m_use - m_new) : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tc_ld32(tO + c0 + lanes, o);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+          tc_st32(tO + c0 + lanes, o);
+        }
+        tc_wait_st();
+        l *= alpha;
+      }
+      m_use = m_new;
+      const float ref = m_use == -INFINITY ? 0.f : m_use;
+      // the P buffer is free once P V of tile it-2 has completed
+      if (it >= 2) {
+        w_ok = mbar_wait_bounded(bar(kBarPvDone + kb), ((it - 2) >> 1) & 1);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+          good = false;
+          break;
+        }
+      }
+      uint8_t* prow = smem + Ly::kP + kb * Ly::kPBytes + r * 128;
+      float lsum = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < kTcKv / 8; ++cc) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const int t = 8 * cc + 2 * e2;
+          const float pa = fast_exp2(z[t] - ref), pb = fast_exp2(z[t + 1] - ref);
+          lsum += pa + pb;
+          const float va = z[t] == -INFINITY ? 0.f : pa * cs[kTcKv + t];
+          const float vb = z[t + 1] == -INFINITY ? 0.f : pb * cs[kTcKv + t + 1];
+          pk[e2] = h2_as_u32(__floats2half2_rn(va, vb));
+        }
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      l += lsum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPFull + kb));
+    }
+    if (good) {
+      const int last = n_it - 1;
+      const bool w_ok = mbar_wait_bounded(bar(kBarPvDone + (last & 1)), (last >> 1) & 1);
+      good = __all_sync(0xFFFFFFFFu, w_ok);
+    }
+    if (!good) {
+      if (lane == 0) fail();
+    } else {
+      // ---- epilogue: O / l, rounded to the activation dtype ----
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* dst = static_cast<uint16_t*>(p.out) +
+                      ((int64_t)(q0 + (pos >= 0 ? iq : 0)) * p.Hq + (int64_t)j * G + r % G) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tc_ld32(tO + c0 + lanes, o);
+        if (pos >= 0) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 8) {
+            uint4 w;
+            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const float a0 = __uint_as_float(o[x + 2 * e2]) * inv;
+              const float a1 = __uint_as_float(o[x + 2 * e2 + 1]) * inv;
+              if constexpr (BF16) wp[e2] = bf2_as_u32(__floats2bfloat162_rn(a0, a1));
+              else wp[e2] = h2_as_u32(__floats2half2_rn(a0, a1));
+            }
+            *reinterpret_cast<uint4*>(dst + c0 + x) = w;
           }
-      }
-      // ---------- O += P V: V pairs of tokens per head dim, times V scales ----------
-      const uint32_t* vsc = reinterpret_cast<const uint32_t*>(sc + kBlockSize);
-      const __half2 vs01 = u32_as_h2(vsc[c]), vs89 = u32_as_h2(vsc[4 + c]);
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS / 2; ++kk) {
-        uint32_t r[4];
-        ldsm_x4_trans(vt + tile_off<C>(lt, 2 * kk + (lane >> 4)), r[0], r[1], r[2], r[3]);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          // r[2hh]: tokens 2c, 2c+1; r[2hh+1]: tokens 8+2c, 9+2c; at dims
-          // d0 = 16cb + 2g (even n-tile) and d0 + 1 (odd n-tile)
-          uint32_t ev0, od0, ev1, od1;
-          i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * hh], ev0, od0);
-          i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * hh + 1], ev1, od1);
-          ev0 = h2_as_u32(__hmul2(u32_as_h2(ev0), vs01));
-          od0 = h2_as_u32(__hmul2(u32_as_h2(od0), vs01));
-          ev1 = h2_as_u32(__hmul2(u32_as_h2(ev1), vs89));
-          od1 = h2_as_u32(__hmul2(u32_as_h2(od1), vs89));
-          const int cb = 2 * kk + hh;
-          mma_16816_acc<false>(o[cb][0], pa[0], pa[1], pa[2], pa[3], ev0, ev1);
-          mma_16816_acc<false>(o[cb][1], pa[0], pa[1], pa[2], pa[3], od0, od1);
         }
       }
     }
-    // stage s consumed by every warp (and a timed-out wait anywhere stops all)
-    if (__syncthreads_or(aborted)) {
-      aborted = true;
-      break;
-    }
-    if (warp == 0 && k_next < npages) issue(k_next++);
   }
 
-  if (aborted) {
-    // a wait gave up: record it, then wait (bounded) for the copies still in
-    // flight (pages k .. k_next-1, known to warp 0) so none lands after exit
-    if (warp == 0) {
-      if (lane == 0) atomicOr(p.err, 0x8u);
-      for (int kp = k; kp < k_next; ++kp)
-        mbar_wait_bounded(smem_u32(&bars[kp % kPfStages]), (kp / kPfStages) & 1);
-    }
-    return;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tc_dealloc(tmem, kTcCols);
   }
-  // ---------- finalize: rows g and g+8; dims 16cb + 4c + {0, 1, 2, 3} ----------
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    l[h] += __shfl_xor_sync(0xFFFFFFFFu, l[h], 1);
-    l[h] += __shfl_xor_sync(0xFFFFFFFFu, l[h], 2);
-  }
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    if (pos[h] < 0) continue;
-    const int r = 16 * warp + g + 8 * h;
-    const int i = i_begin + r / G;
-    const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
-    uint16_t* dst = static_cast<uint16_t*>(p.out) +
-                    ((int64_t)(q0 + i) * p.Hq + (int64_t)j * G + r % G) * D + 4 * c;
-#pragma unroll
-    for (int cb = 0; cb < D / 16; ++cb) {
-      const float a = o[cb][0][2 * h] * inv, bq = o[cb][1][2 * h] * inv;
-      const float c2 = o[cb][0][2 * h + 1] * inv, d2 = o[cb][1][2 * h + 1] * inv;
-      uint2 w;
-      if constexpr (BF16) {
-        w.x = bf2_as_u32(__floats2bfloat162_rn(a, bq));
-        w.y = bf2_as_u32(__floats2bfloat162_rn(c2, d2));
-      } else {
-        w.x = h2_as_u32(__floats2half2_rn(a, bq));
-        w.y = h2_as_u32(__floats2half2_rn(c2, d2));
-      }
-      *reinterpret_cast<uint2*>(dst + 16 * cb) = w;
-    }
-  }
-}
-
-template <int D, bool BF16>
-const void* pf_ptr() {
-  return reinterpret_cast<const void*>(&paged_prefill_kernel<D, BF16>);
-}
-const void* pf_pick(int D, bool bf16) {
-  if (D == 128) return bf16 ? pf_ptr<128, true>() : pf_ptr<128, false>();
-  return bf16 ? pf_ptr<64, true>() : pf_ptr<64, false>();
 }
 
 }  // namespace
 
 size_t prefill_smem_bytes(int D) {
-  return D == 128 ? PfLayout<128>::kTotal : PfLayout<64>::kTotal;
+  return D == 128 ? TcLayout<128>::kTotal : TcLayout<64>::kTotal;
 }
 
+int prefill_rows_per_cta() { return kTcRows; }
+
 cudaError_t prefill_configure(int D, bool bf16) {
-  return cudaFuncSetAttribute(pf_pick(D, bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const void* f = D == 128 ? (bf16 ? reinterpret_cast<const void*>(&paged_prefill_kernel<128, true>)
+                                   : reinterpret_cast<const void*>(&paged_prefill_kernel<128, false>))
+                           : (bf16 ? reinterpret_cast<const void*>(&paged_prefill_kernel<64, true>)
+                                   : reinterpret_cast<const void*>(&paged_prefill_kernel<64, false>));
+  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)prefill_smem_bytes(D));
 }
 
@@ -346,7 +490,7 @@ cudaError_t prefill_launch(int D, bool bf16, const CUtensorMap* maps, const Pref
                            int tiles, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)tiles, (unsigned)p.Hkv, (unsigned)p.B);
-  cfg.blockDim = dim3(kPfThreads);
+  cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = prefill_smem_bytes(D);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
