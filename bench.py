@@ -13,10 +13,12 @@ buffers (pinned H2D of the step's inputs and D2H of the output inside the
 timed region) for the end-to-end figure.  L2 is flushed (512 MB write)
 between timed steps; each step is timed with CUDA events on the launching
 stream.  A context sweep (2K/8K/32K, 16 sequences) compares the INT8 decode
-with the BF16 twin.  The FP64 CPU oracle is timed on a bounded sample of the
-same workload as the CPU baseline.
+with the BF16 twin, and the chunked prefill over the INT8 cache is timed on
+an 8K-token causal chunk (GQA 8).  The FP64 CPU oracle is timed on a bounded
+sample of the same workload as the CPU baseline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --prefill all|SHAPE [--steps K] [--warmup W]   # prefill lines only
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
 replica of the workload (the path needs no exchange between GPUs).
@@ -50,6 +52,17 @@ DECODE_SOURCES = ("kvq_decode.cuh", "kvq_decode_int8.cu", "kvq_ptx.cuh", "kvq_co
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_int8_canonical.traffic.txt")
 
 
+# chunked-prefill shapes: (sequences, context L, chunk n = queries at the end
+# of each sequence, query heads, KV heads); head_dim 128, bf16 activations
+PREFILL_SHAPES = {
+    "8k_full_gqa8": (1, 8192, 8192, 64, 8),
+    "4k_chunk1k_gqa4": (4, 4096, 1024, 32, 8),
+    "2k_chunk512_gqa4": (16, 2048, 512, 32, 8),
+    "4k_full_mha": (2, 4096, 4096, 32, 32),
+    "2k_full_gqa8": (1, 2048, 2048, 64, 8),
+}
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -61,6 +74,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--settle", type=float, default=1.5,
                     help="seconds of untimed steps before the timed region (clock sampling)")
+    ap.add_argument("--prefill", default=None, choices=["all"] + list(PREFILL_SHAPES),
+                    help="chunked-prefill timing instead of the decode bench line: one JSON "
+                         "line per shape (causal attention TFLOP/s against the tensor peak)")
+    ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--profile-arm", choices=["int8", "kv16"], default=None,
                     help="profiling run: only this decode arm (one cache on the device), "
                          "warm-up + steps with L2 flushes, a short timing line; no bench line")
@@ -428,6 +445,55 @@ def sweep(torch, kvq, dev, flush, steps):
     return res
 
 
+def tensor_peak():
+    """Dense 16-bit tensor-core peak (TFLOP/s): the measured bf16 GEMM burst
+    figure (FP16 has the same nominal rate), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def prefill_measure(torch, kvq, dev, flush, names, steps, warmup):
+    """Chunked prefill over the INT8 cache: per shape, the median CUDA-event
+    time of one kvq_paged_prefill call (L2 flushed between calls) and the
+    causal-attention FLOPs it performs, 4 Hq D per (query, visible key)."""
+    peak, kind = tensor_peak()
+    gen = torch.Generator(device=dev)
+    res = []
+    for name in names:
+        B, L, n, Hq, Hkv = PREFILL_SHAPES[name]
+        D = 128
+        gen.manual_seed(L + n)
+        w = W.custom(B, Hq, Hkv, D, "bf16", [L] * B, seed=L, pool_factor=1)
+        nb, bt, _ = w.tables()
+        kc, vc, ksc, vsc = kvq.alloc_int8_cache(nb, Hkv, D, dev)
+        for b in range(B):
+            k = torch.randn((L, Hkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            v = torch.randn((L, Hkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            kvq.kvq_quantize_append(k, v, torch.from_numpy(w.slots(b, 0, L)).to(dev),
+                                    kc, vc, ksc, vsc)
+        q = torch.randn((B * n, Hq, D), generator=gen, device=dev, dtype=torch.bfloat16)
+        btd = torch.from_numpy(bt).to(dev)
+        cl = torch.full((B,), L, dtype=torch.int32, device=dev)
+        qs = torch.arange(0, B * n + 1, n, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        call = lambda: kvq.kvq_paged_prefill(q, kc, vc, ksc, vsc, btd, cl, qs, L, n,  # noqa
+                                             w.sm_scale, out=out)
+        _, t = time_arm(torch, flush, lambda: None, call, steps, warmup)
+        ms = statistics.median(t)
+        keys = B * sum(L - n + i + 1 for i in range(n))
+        tflops = 4.0 * Hq * D * keys / (ms * 1e-3) / 1e12
+        res.append({"shape": name, "num_seqs": B, "context": L, "chunk": n, "num_q_heads": Hq,
+                    "num_kv_heads": Hkv, "head_dim": D, "ms": round(ms, 4),
+                    "tflops": round(tflops, 1), "peak_tflops": peak, "peak_kind": kind,
+                    "frac": round(tflops / peak, 4)})
+        del kc, vc, ksc, vsc, q, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def profile_arm(torch, w, dev, args):
     """One decode arm alone (for ncu captures of a bounded device footprint)."""
     g = GpuWorkload(w, dev, arms=(args.profile_arm,))
@@ -462,6 +528,13 @@ def main():
         pg = dist
     kvq.load(build_if_missing=False)
 
+    if args.prefill:
+        flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        names = list(PREFILL_SHAPES) if args.prefill == "all" else [args.prefill]
+        for r in prefill_measure(torch, kvq, dev, lambda: flush_buf.zero_(), names,
+                                 args.steps, args.warmup):
+            print(json.dumps({"prefill": r}), flush=True)
+        return
     w = W.make(args.workload)
     if args.profile_arm:
         profile_arm(torch, w, dev, args)
@@ -506,6 +579,10 @@ def main():
     sw = None
     if not args.no_sweep:
         sw = sweep(torch, kvq, dev, flush, max(5, min(args.steps, 20)))
+    pf = None
+    if not args.no_prefill:
+        pf = prefill_measure(torch, kvq, dev, flush, ["8k_full_gqa8"], max(3, min(args.steps, 10)),
+                             3)[0]
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
         gbs, n, t = time_oracle(w, budget_s=12.0)
@@ -545,6 +622,7 @@ def main():
         "clocks": clk,
         "cpu_baseline": cpu,
         "context_sweep": sw,
+        "chunked_prefill": pf,
     }
     print(json.dumps(line), flush=True)
     if pg is not None:

@@ -15,10 +15,10 @@
 //    page's INT8 K and V tiles (2-D tensor copies, 128-/64-byte swizzle) and
 //    bulk copies of its two 32-byte scale rows into a 3-stage ring;
 //  * warps 6-9, converters: INT8 codes to exact FP16 integers (byte permute
-//    under exponent 0x64, minus 1152), K as a K-major [64 tokens][D] operand
-//    and V transposed to a K-major [D][64 tokens] operand, both 128-byte
-//    swizzled, double-buffered; the tile's K scales (times sm_scale log2 e)
-//    and V scales as FP32 columns;
+//    under exponent 0x64, minus 1152), K and V both as [64 tokens][D] tiles,
+//    128-byte swizzled, double-buffered: K is the K-major B operand of
+//    Q K^T, V the MN-major B operand of P V; the tile's K scales (times
+//    sm_scale log2 e) and V scales as FP32 columns;
 //  * warp 5, MMA issuer (one thread): S = Q K^T into one of two 128 x 64
 //    FP32 TMEM buffers (8 MMAs of K = 16 over the head dims), and, one tile
 //    behind, O += P V into a 128 x D FP32 TMEM accumulator (4 MMAs over the
@@ -58,7 +58,7 @@ struct TcLayout {
   static constexpr int kQ = 0;                            // [128][D] FP16, D/64 tiles of 16 KB
   static constexpr int kKcBytes = kTcKv * D * 2;         // [64][D] FP16, D/64 tiles of 8 KB
   static constexpr int kKc = kQ + kTcRows * D * 2;       // 2 buffers
-  static constexpr int kVtBytes = D * kTcKv * 2;         // [D][64] FP16, one tile of D x 128 B
+  static constexpr int kVtBytes = kTcKv * D * 2;         // [64][D] FP16, D/64 tiles of 8 KB
   static constexpr int kVt = kKc + 2 * kKcBytes;         // 2 buffers
   static constexpr int kPBytes = kTcRows * kTcKv * 2;    // [128][64] FP16
   static constexpr int kP = kVt + 2 * kVtBytes;          // 2 buffers
@@ -76,15 +76,20 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v) {
   return h2_as_u32(__floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)));
 }
 
-// 4 x 4 byte transpose: out[d] = byte d of a0, a1, a2, a3.
-__device__ __forceinline__ void transpose4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                           uint32_t (&out)[4]) {
-  const uint32_t x01 = __byte_perm(a0, a1, 0x5140), y01 = __byte_perm(a0, a1, 0x7362);
-  const uint32_t x23 = __byte_perm(a2, a3, 0x5140), y23 = __byte_perm(a2, a3, 0x7362);
-  out[0] = __byte_perm(x01, x23, 0x5410);
-  out[1] = __byte_perm(x01, x23, 0x7632);
-  out[2] = __byte_perm(y01, y23, 0x5410);
-  out[3] = __byte_perm(y01, y23, 0x7632);
+// 16 INT8 codes (chunk c of token row t of a page tile) -> FP16 chunks 2c,
+// 2c+1 of row t of a [64][D] 128-byte-swizzled operand tile.
+template <int D>
+__device__ __forceinline__ void convert_chunk(const uint8_t* src, uint8_t* dst, int t, int c) {
+  const uint4 w = *reinterpret_cast<const uint4*>(src);
+  uint4 lo, hi;
+  i8x4_to_h2x2<0x4140u, 0x4342u>(w.x, lo.x, lo.y);
+  i8x4_to_h2x2<0x4140u, 0x4342u>(w.y, lo.z, lo.w);
+  i8x4_to_h2x2<0x4140u, 0x4342u>(w.z, hi.x, hi.y);
+  i8x4_to_h2x2<0x4140u, 0x4342u>(w.w, hi.z, hi.w);
+  uint8_t* row = dst + (c >> 2) * (kTcKv * 128) + t * 128;
+  const int c0 = (2 * c) & 7;
+  *reinterpret_cast<uint4*>(row + ((c0 ^ (t & 7)) << 4)) = lo;
+  *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (t & 7)) << 4)) = hi;
 }
 
 template <int D, bool BF16>
@@ -228,49 +233,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint8_t* rawV = rawK + kTcPages * Ly::kTile;
       uint8_t* kc = smem + Ly::kKc + kb * Ly::kKcBytes;
       uint8_t* vt = smem + Ly::kVt + kb * Ly::kVtBytes;
-      // K: 16 codes (chunk c of token t) -> FP16 chunks 2c, 2c+1 of row t
+      // 16 codes (chunk c of token t) -> FP16 chunks 2c, 2c+1 of row t, K then V
 #pragma unroll
       for (int pass = 0; pass < kTcKv * (D / 16) / 128; ++pass) {
         const int e = ct + 128 * pass;
         const int t = e / (D / 16), c = e - t * (D / 16);
-        const uint4 w = *reinterpret_cast<const uint4*>(rawK + (t >> 4) * Ly::kTile +
-                                                        tile_off<C>(t & 15, c));
-        uint4 lo, hi;
-        i8x4_to_h2x2<0x4140u, 0x4342u>(w.x, lo.x, lo.y);
-        i8x4_to_h2x2<0x4140u, 0x4342u>(w.y, lo.z, lo.w);
-        i8x4_to_h2x2<0x4140u, 0x4342u>(w.z, hi.x, hi.y);
-        i8x4_to_h2x2<0x4140u, 0x4342u>(w.w, hi.z, hi.w);
-        uint8_t* row = kc + (c >> 2) * (kTcKv * 128) + t * 128;
-        const int c0 = (2 * c) & 7;
-        *reinterpret_cast<uint4*>(row + ((c0 ^ (t & 7)) << 4)) = lo;
-        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (t & 7)) << 4)) = hi;
-      }
-      // V: head dims 4dg..4dg+3 of tokens 8tg..8tg+7 -> rows 4dg.. of V^T, chunk tg;
-      // a warp covers 8 dim groups x 4 token groups per pass
-#pragma unroll
-      for (int pass = 0; pass < (D / 4) * (kTcKv / 8) / 128; ++pass) {
-        const int e = ct + 128 * pass;
-        const int wt = e >> 5;
-        const int dg = (e & 7) + 8 * (wt % (D / 32));
-        const int tg = ((e >> 3) & 3) + 4 * (wt / (D / 32));
-        uint32_t a[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int t = 8 * tg + k;
-          a[k] = *reinterpret_cast<const uint32_t*>(rawV + (t >> 4) * Ly::kTile +
-                                                    tile_off<C>(t & 15, dg >> 2) + 4 * (dg & 3));
-        }
-        uint32_t lo[4], hi[4];
-        transpose4(a[0], a[1], a[2], a[3], lo);
-        transpose4(a[4], a[5], a[6], a[7], hi);
-#pragma unroll
-        for (int dd = 0; dd < 4; ++dd) {
-          uint4 o;
-          i8x4_to_h2x2<0x4140u, 0x4342u>(lo[dd], o.x, o.y);
-          i8x4_to_h2x2<0x4140u, 0x4342u>(hi[dd], o.z, o.w);
-          const int d = 4 * dg + dd;
-          *reinterpret_cast<uint4*>(vt + d * 128 + ((tg ^ (d & 7)) << 4)) = o;
-        }
+        const int src = (t >> 4) * Ly::kTile + tile_off<C>(t & 15, c);
+        convert_chunk<D>(rawK + src, kc, t, c);
+        convert_chunk<D>(rawV + src, vt, t, c);
       }
       // scale columns: K (times sm_scale log2 e) for ct < 64, V for the others
       {
@@ -292,7 +262,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = tc_idesc_f16(kTcKv, false);
-      constexpr uint32_t idO = tc_idesc_f16(D, false);
+      constexpr uint32_t idO = tc_idesc_f16(D, false, true);
       const uint32_t q_u32 = smem_u32(smem + Ly::kQ);
       auto issue_pv = [&](int k) -> bool {
         const int kb = k & 1;
@@ -302,7 +272,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t vb = smem_u32(smem + Ly::kVt + kb * Ly::kVtBytes);
 #pragma unroll
         for (int ts = 0; ts < kTcKv / 16; ++ts)
-          tc_mma_f16(tO, tc_desc_sw128(pa + 32 * ts), tc_desc_sw128(vb + 32 * ts), idO,
+          tc_mma_f16(tO, tc_desc_sw128(pa + 32 * ts),
+                     tc_desc_sw128_mn(vb + 16 * 128 * ts, kTcKv * 128), idO,
                      k > 0 || ts > 0);
         tc_commit(bar(kBarPvDone + kb));
         tc_commit(bar(kBarCvtEmpty + kb));
@@ -352,22 +323,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const float* cs = reinterpret_cast<const float*>(smem + Ly::kColSc) + kb * 2 * kTcKv;
+      // scale columns of the tile: K (times sm_scale log2 e) at [0, 64), V at [64, 128)
+      const float4* cs4 = reinterpret_cast<const float4*>(smem + Ly::kColSc) + kb * (kTcKv / 2);
       const int t0 = it * kTcKv;
+      const bool masked = t0 + kTcKv - 1 > pos;    // some token of the tile is past this row
       float z[kTcKv];
 #pragma unroll
       for (int h = 0; h < kTcKv / 32; ++h) {
         uint32_t sr[32];
         tc_ld32(tS + kTcKv * kb + 32 * h + lanes, sr);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int t = 32 * h + x;
-          z[t] = t0 + t <= pos ? __uint_as_float(sr[x]) * cs[t] : -INFINITY;
+        for (int x = 0; x < 32; x += 4) {
+          const float4 k4 = cs4[(32 * h + x) / 4];
+          z[32 * h + x] = __uint_as_float(sr[x]) * k4.x;
+          z[32 * h + x + 1] = __uint_as_float(sr[x + 1]) * k4.y;
+          z[32 * h + x + 2] = __uint_as_float(sr[x + 2]) * k4.z;
+          z[32 * h + x + 3] = __uint_as_float(sr[x + 3]) * k4.w;
         }
       }
-      float mx = z[0];
+      if (masked) {
 #pragma unroll
-      for (int t = 1; t < kTcKv; ++t) mx = fmaxf(mx, z[t]);
+        for (int t = 0; t < kTcKv; ++t)
+          if (t0 + t > pos) z[t] = -INFINITY;
+      }
+      float mx;
+      {
+        float mr[kTcKv / 2];                       // pairwise tree: short dependency chains
+#pragma unroll
+        for (int t = 0; t < kTcKv / 2; ++t) mr[t] = fmaxf(z[t], z[t + kTcKv / 2]);
+#pragma unroll
+        for (int w = kTcKv / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int t = 0; t < w; ++t) mr[t] = fmaxf(mr[t], mr[t + w]);
+        mx = mr[0];
+      }
       const bool grow = mx > m_use + 8.f;
       const float m_new = grow ? mx : m_use;
       const bool resc = grow && m_use != -INFINITY;
@@ -402,22 +391,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
       }
+      // P = 2^(z - m): the row sum takes P, the P V operand P' = P s_v (0 for
+      // tokens past the row, whose scale slots may hold anything)
+#pragma unroll
+      for (int t = 0; t < kTcKv; ++t) z[t] = fast_exp2(z[t] - ref);
+      float lsum;
+      {
+        float sr2[kTcKv / 2];
+#pragma unroll
+        for (int t = 0; t < kTcKv / 2; ++t) sr2[t] = z[t] + z[t + kTcKv / 2];
+#pragma unroll
+        for (int w = kTcKv / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int t = 0; t < w; ++t) sr2[t] += sr2[t + w];
+        lsum = sr2[0];
+      }
       uint8_t* prow = smem + Ly::kP + kb * Ly::kPBytes + r * 128;
-      float lsum = 0.f;
 #pragma unroll
       for (int cc = 0; cc < kTcKv / 8; ++cc) {
-        uint32_t pk[4];
+        const float4 v0 = cs4[(kTcKv + 8 * cc) / 4], v1 = cs4[(kTcKv + 8 * cc) / 4 + 1];
+        float a8[8] = {z[8 * cc] * v0.x,     z[8 * cc + 1] * v0.y, z[8 * cc + 2] * v0.z,
+                       z[8 * cc + 3] * v0.w, z[8 * cc + 4] * v1.x, z[8 * cc + 5] * v1.y,
+                       z[8 * cc + 6] * v1.z, z[8 * cc + 7] * v1.w};
+        if (masked) {
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const int t = 8 * cc + 2 * e2;
-          const float pa = fast_exp2(z[t] - ref), pb = fast_exp2(z[t + 1] - ref);
-          lsum += pa + pb;
-          const float va = z[t] == -INFINITY ? 0.f : pa * cs[kTcKv + t];
-          const float vb = z[t + 1] == -INFINITY ? 0.f : pb * cs[kTcKv + t + 1];
-          pk[e2] = h2_as_u32(__floats2half2_rn(va, vb));
+          for (int e2 = 0; e2 < 8; ++e2)
+            if (t0 + 8 * cc + e2 > pos) a8[e2] = 0.f;
         }
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        uint4 pk;
+        pk.x = h2_as_u32(__floats2half2_rn(a8[0], a8[1]));
+        pk.y = h2_as_u32(__floats2half2_rn(a8[2], a8[3]));
+        pk.z = h2_as_u32(__floats2half2_rn(a8[4], a8[5]));
+        pk.w = h2_as_u32(__floats2half2_rn(a8[6], a8[7]));
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = pk;
       }
       l += lsum;
       fence_proxy_async_smem();

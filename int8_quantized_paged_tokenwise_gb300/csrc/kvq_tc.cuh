@@ -4,11 +4,14 @@
 // tensor-memory loads and stores of the accumulators.
 //
 // Conventions used by the kernels:
-//  * operands are K-major 16-bit tiles in shared memory with the 128-byte
-//    swizzle: row r of a tile is 128 bytes (64 elements of K) at r * 128,
-//    its 16-byte chunk c stored at chunk position c ^ (r % 8); a tile's base
-//    is 1024-byte aligned, and a wider K is a sequence of such tiles.  The
-//    descriptor of K-step s (16 elements) starts 32 * s bytes into the row.
+//  * operands are 16-bit tiles in shared memory with the 128-byte swizzle:
+//    row r of a tile is 128 bytes (64 elements) at r * 128, its 16-byte
+//    chunk c stored at chunk position c ^ (r % 8); a tile's base is
+//    1024-byte aligned.  K-major: a row holds 64 elements of K of one M (or
+//    N) index, a wider K is a sequence of such tiles, and the descriptor of
+//    K-step s (16 elements) starts 32 * s bytes into the row.  MN-major: a
+//    row holds 64 consecutive M (or N) indices of one k, and K-step s starts
+//    16 rows (2048 bytes) further.
 //  * accumulators are FP32 in tensor memory with M = 128: row i of the
 //    result is TMEM lane i, column j is TMEM column base + j.  Warp w of a
 //    warpgroup reaches lanes 32 (w % 4) .. 32 (w % 4) + 31.
@@ -54,11 +57,23 @@ __device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16 with FP32 accumulation, both operands
-// K-major, M = 128: FP16 (or BF16) A and B.
-__host__ __device__ constexpr uint32_t tc_idesc_f16(int n, bool bf16) {
+// Shared-memory descriptor of an MN-major, 128-byte-swizzled operand: rows
+// of 64 consecutive MN elements (128 bytes), one row per k, 8-row (k) groups
+// 1024 bytes apart, and the next 64 MN elements `mn_stride` bytes further.
+__device__ __forceinline__ uint64_t tc_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;   // leading byte offset: MN atoms
+  d |= (uint64_t)(1024 >> 4) << 32;                     // stride byte offset: 8 k-rows
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with FP32 accumulation, M = 128: FP16
+// (or BF16) A and B, A K-major, B K-major or (b_mn) MN-major.
+__host__ __device__ constexpr uint32_t tc_idesc_f16(int n, bool bf16, bool b_mn = false) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
 // D[tmem] (+)= A[desc] * B[desc]^T for one K-step of 16; issued by one thread.
