@@ -11,22 +11,27 @@
 // One CTA = 128 (query, head-of-the-GQA-group) rows of one KV head of one
 // sequence (M = 128 of every MMA), streaming the sequence's tokens in tiles
 // of 64 (4 pages).  Warp roles:
-//  * warp 4, producer: block ids from the block table, TMA copies of each
+//  * warp 8, producer: block ids from the block table, TMA copies of each
 //    page's INT8 K and V tiles (2-D tensor copies, 128-/64-byte swizzle) and
 //    bulk copies of its two 32-byte scale rows into a 3-stage ring;
-//  * warps 6-9, converters: INT8 codes to exact FP16 integers (byte permute
-//    under exponent 0x64, minus 1152), K and V both as [64 tokens][D] tiles,
-//    128-byte swizzled, double-buffered: K is the K-major B operand of
+//  * warps 10-13, converters: INT8 codes to exact FP16 integers (byte
+//    permute under exponent 0x64, minus 1152), K and V both as [64 tokens][D]
+//    tiles, 128-byte swizzled, in 3 buffers: K is the K-major B operand of
 //    Q K^T, V the MN-major B operand of P V; the tile's K scales (times
 //    sm_scale log2 e) and V scales as FP32 columns;
-//  * warp 5, MMA issuer (one thread): S = Q K^T into one of two 128 x 64
+//  * warp 9, MMA issuer (one thread): S = Q K^T into one of two 128 x 64
 //    FP32 TMEM buffers (8 MMAs of K = 16 over the head dims), and, one tile
 //    behind, O += P V into a 128 x D FP32 TMEM accumulator (4 MMAs over the
-//    tokens), each group's completion signalled through tcgen05.commit;
-//  * warps 0-3, softmax (one thread per row = TMEM lane): the row of S,
-//    times the K-scale column, causal mask, running maximum, P = 2^(z - m)
-//    with the V scale of each token folded in (P' = P s_v, FP16, written as
-//    the K-major A operand of the next P V), row sums in FP32; O is rescaled
+//    tokens, A = P read from TMEM), each group's completion signalled
+//    through tcgen05.commit;
+//  * warps 0-7, softmax (two threads per row = TMEM lane, warps w and w + 4
+//    taking the two halves of the tile's 64 columns and exchanging the row
+//    maximum through shared memory at a named barrier of the pair): the
+//    row of S, times the K-scale column, causal mask, running maximum,
+//    P = 2^(z - m)
+//    with the V scale of each token folded in (P' = P s_v, FP16, stored into
+//    one of two TMEM buffers as the A operand of the next P V), row sums in
+//    FP32; O is rescaled
 //    in TMEM only when a row maximum grows by more than 2^8 over the one in
 //    use (the shift cancels in O / l, and P' stays below 2^8 s_v), and
 //    normalized and stored at the end.
@@ -40,36 +45,42 @@ namespace {
 
 constexpr int kTcRows = 128;                    // M: (query, head) rows per CTA
 constexpr int kTcKv = 64;                       // tokens per KV tile
+constexpr int kTcHalf = kTcKv / 2;              // columns per softmax thread
 constexpr int kTcPages = kTcKv / kBlockSize;     // pages per KV tile
 constexpr int kTcRaw = 3;                       // INT8 staging ring depth
-constexpr int kTcWarps = 10;
+constexpr int kTcConv = 3;                      // converted (FP16) operand buffers
+constexpr int kTcWarps = 14;
 constexpr int kTcThreads = kTcWarps * 32;
-constexpr int kWarpTma = 4, kWarpMma = 5, kWarpCvt = 6;
-constexpr uint32_t kTcCols = 256;               // TMEM: O (D columns) + 2 S buffers of 64
+constexpr int kSoftmaxWarps = 8, kWarpTma = 8, kWarpMma = 9, kWarpCvt = 10;
+
+// TMEM columns: O (D), two S buffers (64 FP32 each), two P buffers (64 FP16
+// = 32 columns each)
+template <int D>
+__host__ __device__ constexpr uint32_t tc_cols() {
+  return D + 2 * kTcKv + kTcKv > 256 ? 512u : 256u;
+}
 
 // barrier indices
-constexpr int kBarRawFull = 0, kBarRawEmpty = 3, kBarCvtFull = 6, kBarCvtEmpty = 8,
-              kBarSFull = 10, kBarPFull = 12, kBarPvDone = 14, kBarFin = 16, kNumBars = 17;
+constexpr int kBarRawFull = 0, kBarRawEmpty = 3, kBarCvtFull = 6, kBarCvtEmpty = 9,
+              kBarSFull = 12, kBarPFull = 14, kBarPvDone = 16, kBarFin = 18, kNumBars = 19;
 
 // Shared memory (offsets from a 1024-aligned base; every operand tile starts
 // on a 1024-byte boundary).
 template <int D>
 struct TcLayout {
   static constexpr int kQ = 0;                            // [128][D] FP16, D/64 tiles of 16 KB
-  static constexpr int kKcBytes = kTcKv * D * 2;         // [64][D] FP16, D/64 tiles of 8 KB
-  static constexpr int kKc = kQ + kTcRows * D * 2;       // 2 buffers
-  static constexpr int kVtBytes = kTcKv * D * 2;         // [64][D] FP16, D/64 tiles of 8 KB
-  static constexpr int kVt = kKc + 2 * kKcBytes;         // 2 buffers
-  static constexpr int kPBytes = kTcRows * kTcKv * 2;    // [128][64] FP16
-  static constexpr int kP = kVt + 2 * kVtBytes;          // 2 buffers
+  static constexpr int kConvBytes = kTcKv * D * 2;        // [64][D] FP16, D/64 tiles of 8 KB
+  static constexpr int kKc = kQ + kTcRows * D * 2;       // kTcConv K buffers
+  static constexpr int kVc = kKc + kTcConv * kConvBytes; // kTcConv V buffers
   static constexpr int kTile = kBlockSize * D;           // one page's INT8 K (or V) tile
   static constexpr int kRawBytes = 2 * kTcPages * kTile; // K tiles of 4 pages, then V tiles
-  static constexpr int kRaw = kP + 2 * kPBytes;          // kTcRaw stages
-  static constexpr int kRawSc = kRaw + kTcRaw * kRawBytes;        // per page: K 32 B, V 32 B
-  static constexpr int kColSc = kRawSc + kTcRaw * kTcPages * 64;  // 2 x (K 64, V 64 floats)
-  static constexpr int kBars = kColSc + 2 * 2 * kTcKv * 4;
+  static constexpr int kRaw = kVc + kTcConv * kConvBytes;          // kTcRaw stages
+  static constexpr int kRawSc = kRaw + kTcRaw * kRawBytes;         // per page: K 32 B, V 32 B
+  static constexpr int kColSc = kRawSc + kTcRaw * kTcPages * 64;   // per buffer: K 64, V 64 floats
+  static constexpr int kXchg = kColSc + kTcConv * 2 * kTcKv * 4;   // [2 parities][2 halves][128]
+  static constexpr int kBars = kXchg + 2 * 2 * kTcRows * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;     // TMEM base, abort flag
-  static constexpr size_t kTotal = (size_t)kMisc + 16 + 1024;     // + base alignment slack
+  static constexpr size_t kTotal = (size_t)kMisc + 16 + 1024;      // + base alignment slack
 };
 
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v) {
@@ -90,6 +101,42 @@ __device__ __forceinline__ void convert_chunk(const uint8_t* src, uint8_t* dst, 
   const int c0 = (2 * c) & 7;
   *reinterpret_cast<uint4*>(row + ((c0 ^ (t & 7)) << 4)) = lo;
   *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (t & 7)) << 4)) = hi;
+}
+
+// Named barrier of the two softmax warps that share a row block (ids 1..4),
+// with an AND over the 64 threads' predicates.
+__device__ __forceinline__ bool pair_and(bool v, int id) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 64, p;\n\tselp.b32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
+// 16 consecutive FP32 columns of this thread's TMEM lane (warp-wide), waited for.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
 }
 
 template <int D, bool BF16>
@@ -116,10 +163,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     misc[1] = 0;
   }
   if (tid < kNumBars) {
-    const bool quad = (tid >= kBarRawEmpty && tid < kBarRawEmpty + kTcRaw) ||
-                      (tid >= kBarCvtFull && tid < kBarCvtFull + 2) ||
-                      (tid >= kBarPFull && tid < kBarPFull + 2);
-    mbar_init(bar(tid), quad ? 4 : 1);            // per-warp arrivals of 4 warps, else one
+    uint32_t count = 1;                           // TMA transactions, commits
+    if (tid >= kBarRawEmpty && tid < kBarRawEmpty + kTcRaw) count = 4;     // converter warps
+    if (tid >= kBarCvtFull && tid < kBarCvtFull + kTcConv) count = 4;      // converter warps
+    if (tid >= kBarPFull && tid < kBarPFull + 2) count = kSoftmaxWarps;    // softmax warps
+    mbar_init(bar(tid), count);
   }
   griddep_wait();
 
@@ -138,7 +186,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_it = p_last / kTcKv + 1;           // KV tiles
   const int npages = p_last / kBlockSize + 1;
 
-  if (warp == kWarpMma) tc_alloc(smem_u32(&misc[0]), kTcCols);
+  if (warp == kWarpMma) tc_alloc(smem_u32(&misc[0]), tc_cols<D>());
 
   // ---- Q tile: row r = (query i_begin + r / G, head j G + r % G), FP16, swizzled ----
   for (int e = tid; e < kTcRows * (D / 8); e += kTcThreads) {
@@ -166,6 +214,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const uint32_t tO = tmem, tS = tmem + D;        // S buffer k at tS + 64 k
+  const uint32_t tP = tS + 2 * kTcKv;             // P buffer k at tP + 32 k
   auto fail = [&]() {
     atomicOr(p.err, 0x8u);
     *abort_flag = 1;
@@ -222,17 +271,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------------------------------------------------- converters
     const int ct = tid - kWarpCvt * 32;           // 0..127
     for (int it = 0; it < n_it; ++it) {
-      const int s = it % kTcRaw, kb = it & 1;
+      const int s = it % kTcRaw, cb = it % kTcConv;
       if (!mbar_wait_bounded(bar(kBarRawFull + s), (it / kTcRaw) & 1) ||
-          (it >= 2 && !mbar_wait_bounded(bar(kBarCvtEmpty + kb), ((it - 2) >> 1) & 1))) {
+          (it >= kTcConv &&
+           !mbar_wait_bounded(bar(kBarCvtEmpty + cb), ((it / kTcConv) - 1) & 1))) {
         if (lane == 0) fail();
         break;
       }
       if (*abort_flag) break;
       const uint8_t* rawK = smem + Ly::kRaw + s * Ly::kRawBytes;
       const uint8_t* rawV = rawK + kTcPages * Ly::kTile;
-      uint8_t* kc = smem + Ly::kKc + kb * Ly::kKcBytes;
-      uint8_t* vt = smem + Ly::kVt + kb * Ly::kVtBytes;
+      uint8_t* kc = smem + Ly::kKc + cb * Ly::kConvBytes;
+      uint8_t* vc = smem + Ly::kVc + cb * Ly::kConvBytes;
       // 16 codes (chunk c of token t) -> FP16 chunks 2c, 2c+1 of row t, K then V
 #pragma unroll
       for (int pass = 0; pass < kTcKv * (D / 16) / 128; ++pass) {
@@ -240,13 +290,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int t = e / (D / 16), c = e - t * (D / 16);
         const int src = (t >> 4) * Ly::kTile + tile_off<C>(t & 15, c);
         convert_chunk<D>(rawK + src, kc, t, c);
-        convert_chunk<D>(rawV + src, vt, t, c);
+        convert_chunk<D>(rawV + src, vc, t, c);
       }
       // scale columns: K (times sm_scale log2 e) for ct < 64, V for the others
       {
         const uint16_t* rs =
             reinterpret_cast<const uint16_t*>(smem + Ly::kRawSc) + s * kTcPages * 32;
-        float* cs = reinterpret_cast<float*>(smem + Ly::kColSc) + kb * 2 * kTcKv;
+        float* cs = reinterpret_cast<float*>(smem + Ly::kColSc) + cb * 2 * kTcKv;
         const int t = ct & (kTcKv - 1), kind = ct >> 6;
         const float sv = __half2float(__ushort_as_half(rs[(t >> 4) * 32 + kind * 16 + (t & 15)]));
         cs[kind * kTcKv + t] = kind == 0 ? sv * p.scale_log2 : sv;
@@ -254,7 +304,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(kBarCvtFull + kb));
+        mbar_arrive(bar(kBarCvtFull + cb));
         mbar_arrive(bar(kBarRawEmpty + s));
       }
     }
@@ -265,36 +315,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idO = tc_idesc_f16(D, false, true);
       const uint32_t q_u32 = smem_u32(smem + Ly::kQ);
       auto issue_pv = [&](int k) -> bool {
-        const int kb = k & 1;
-        if (!mbar_wait_bounded(bar(kBarPFull + kb), (k >> 1) & 1)) return false;
+        const int sb = k & 1, cb = k % kTcConv;
+        if (!mbar_wait_bounded(bar(kBarPFull + sb), (k >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t pa = smem_u32(smem + Ly::kP + kb * Ly::kPBytes);
-        const uint32_t vb = smem_u32(smem + Ly::kVt + kb * Ly::kVtBytes);
+        const uint32_t vb = smem_u32(smem + Ly::kVc + cb * Ly::kConvBytes);
 #pragma unroll
         for (int ts = 0; ts < kTcKv / 16; ++ts)
-          tc_mma_f16(tO, tc_desc_sw128(pa + 32 * ts),
-                     tc_desc_sw128_mn(vb + 16 * 128 * ts, kTcKv * 128), idO,
-                     k > 0 || ts > 0);
-        tc_commit(bar(kBarPvDone + kb));
-        tc_commit(bar(kBarCvtEmpty + kb));
+          tc_mma_f16_tmem_a(tO, tP + kTcHalf * sb + 8 * ts,
+                            tc_desc_sw128_mn(vb + 16 * 128 * ts, kTcKv * 128), idO,
+                            k > 0 || ts > 0);
+        tc_commit(bar(kBarPvDone + sb));
+        tc_commit(bar(kBarCvtEmpty + cb));
         return true;
       };
       bool good = true;
       for (int it = 0; it < n_it; ++it) {
-        const int kb = it & 1;
-        if (!mbar_wait_bounded(bar(kBarCvtFull + kb), (it >> 1) & 1) || *abort_flag) {
+        const int sb = it & 1, cb = it % kTcConv;
+        if (!mbar_wait_bounded(bar(kBarCvtFull + cb), (it / kTcConv) & 1) || *abort_flag) {
           good = false;
           break;
         }
         tc_fence_after();
-        const uint32_t kbase = smem_u32(smem + Ly::kKc + kb * Ly::kKcBytes);
+        const uint32_t kbase = smem_u32(smem + Ly::kKc + cb * Ly::kConvBytes);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_f16(tS + kTcKv * kb,
+          tc_mma_f16(tS + kTcKv * sb,
                      tc_desc_sw128(q_u32 + (ks >> 2) * (kTcRows * 128) + 32 * (ks & 3)),
                      tc_desc_sw128(kbase + (ks >> 2) * (kTcKv * 128) + 32 * (ks & 3)), idS,
                      ks > 0);
-        tc_commit(bar(kBarSFull + kb));
+        tc_commit(bar(kBarSFull + sb));
         if (it > 0 && !issue_pv(it - 1)) {
           good = false;
           break;
@@ -306,77 +355,86 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait_bounded(bar(kBarFin), 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else {
     // ------------------------------------------------------------- softmax
-    const int r = tid;                            // row = TMEM lane
+    const int rb = warp & 3, hh = warp >> 2;      // row block, column half
+    const int r = 32 * rb + lane;                 // row = TMEM lane
+    const int pair = 1 + rb;                      // named barrier of warps rb, rb + 4
     const int iq = i_begin + r / G;
     const int pos = (r < TQ * G && iq < i_end) ? L - n + iq : -1;   // -1: padding row
-    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
-    float m_use = -INFINITY, l = 0.f;
+    const uint32_t lanes = (uint32_t)(32 * rb) << 16;
+    float* xchg = reinterpret_cast<float*>(smem + Ly::kXchg);         // [parity][half][row]
+    float m_use = -INFINITY, l = 0.f;             // l: this half's share of the row sum
     bool good = true;
     for (int it = 0; it < n_it; ++it) {
-      const int kb = it & 1;
-      bool w_ok = mbar_wait_bounded(bar(kBarCvtFull + kb), (it >> 1) & 1) &&
-                  mbar_wait_bounded(bar(kBarSFull + kb), (it >> 1) & 1);
-      if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+      const int sb = it & 1, cb = it % kTcConv;
+      bool w_ok = mbar_wait_bounded(bar(kBarCvtFull + cb), (it / kTcConv) & 1) &&
+                  mbar_wait_bounded(bar(kBarSFull + sb), (it >> 1) & 1);
+      if (!pair_and(__all_sync(0xFFFFFFFFu, w_ok), pair)) {
         good = false;
         break;
       }
       tc_fence_after();
-      // scale columns of the tile: K (times sm_scale log2 e) at [0, 64), V at [64, 128)
-      const float4* cs4 = reinterpret_cast<const float4*>(smem + Ly::kColSc) + kb * (kTcKv / 2);
-      const int t0 = it * kTcKv;
-      const bool masked = t0 + kTcKv - 1 > pos;    // some token of the tile is past this row
-      float z[kTcKv];
+      // this half's scale columns: K (times sm_scale log2 e), then V
+      const float4* cs4 = reinterpret_cast<const float4*>(smem + Ly::kColSc) +
+                          cb * (kTcKv / 2) + hh * (kTcHalf / 4);
+      const int t0 = it * kTcKv + hh * kTcHalf;   // first token of this half
+      const bool masked = t0 + kTcHalf - 1 > pos;  // some token of the half is past the row
+      float z[kTcHalf];
 #pragma unroll
-      for (int h = 0; h < kTcKv / 32; ++h) {
-        uint32_t sr[32];
-        tc_ld32(tS + kTcKv * kb + 32 * h + lanes, sr);
+      for (int h = 0; h < kTcHalf / 16; ++h) {
+        uint32_t sr[16];
+        tc_ld16(tS + kTcKv * sb + kTcHalf * hh + 16 * h + lanes, sr);
 #pragma unroll
-        for (int x = 0; x < 32; x += 4) {
-          const float4 k4 = cs4[(32 * h + x) / 4];
-          z[32 * h + x] = __uint_as_float(sr[x]) * k4.x;
-          z[32 * h + x + 1] = __uint_as_float(sr[x + 1]) * k4.y;
-          z[32 * h + x + 2] = __uint_as_float(sr[x + 2]) * k4.z;
-          z[32 * h + x + 3] = __uint_as_float(sr[x + 3]) * k4.w;
+        for (int x = 0; x < 16; x += 4) {
+          const float4 k4 = cs4[(16 * h + x) / 4];
+          z[16 * h + x] = __uint_as_float(sr[x]) * k4.x;
+          z[16 * h + x + 1] = __uint_as_float(sr[x + 1]) * k4.y;
+          z[16 * h + x + 2] = __uint_as_float(sr[x + 2]) * k4.z;
+          z[16 * h + x + 3] = __uint_as_float(sr[x + 3]) * k4.w;
         }
       }
       if (masked) {
 #pragma unroll
-        for (int t = 0; t < kTcKv; ++t)
+        for (int t = 0; t < kTcHalf; ++t)
           if (t0 + t > pos) z[t] = -INFINITY;
       }
       float mx;
       {
-        float mr[kTcKv / 2];                       // pairwise tree: short dependency chains
+        float mr[kTcHalf / 2];                     // pairwise tree: short dependency chains
 #pragma unroll
-        for (int t = 0; t < kTcKv / 2; ++t) mr[t] = fmaxf(z[t], z[t + kTcKv / 2]);
+        for (int t = 0; t < kTcHalf / 2; ++t) mr[t] = fmaxf(z[t], z[t + kTcHalf / 2]);
 #pragma unroll
-        for (int w = kTcKv / 4; w >= 1; w >>= 1)
+        for (int w = kTcHalf / 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int t = 0; t < w; ++t) mr[t] = fmaxf(mr[t], mr[t + w]);
         mx = mr[0];
       }
+      // row maximum over both halves (buffers alternate by iteration parity)
+      xchg[(sb * 2 + hh) * kTcRows + r] = mx;
+      pair_and(true, pair);
+      mx = fmaxf(mx, xchg[(sb * 2 + (hh ^ 1)) * kTcRows + r]);
       const bool grow = mx > m_use + 8.f;
       const float m_new = grow ? mx : m_use;
       const bool resc = grow && m_use != -INFINITY;
       if (__any_sync(0xFFFFFFFFu, resc)) {
         // O holds P V of tiles 0..it-1: once the last has completed, rescale
-        // the rows whose maximum moved
+        // this half's columns of the rows whose maximum moved (the partner
+        // warp decides identically: same rows, same maxima)
         w_ok = mbar_wait_bounded(bar(kBarPvDone + ((it - 1) & 1)), ((it - 1) >> 1) & 1);
-        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+        if (!pair_and(__all_sync(0xFFFFFFFFu, w_ok), pair)) {
           good = false;
           break;
         }
         tc_fence_after();
         const float alpha = resc ? fast_exp2(m_use - m_new) : 1.f;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tc_ld32(tO + c0 + lanes, o);
+        for (int c0 = 0; c0 < D / 2; c0 += 16) {
+          uint32_t o[16];
+          tc_ld16(tO + hh * (D / 2) + c0 + lanes, o);
 #pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          tc_st32(tO + c0 + lanes, o);
+          for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+          tc_st16(tO + hh * (D / 2) + c0 + lanes, o);
         }
         tc_wait_st();
         l *= alpha;
@@ -385,8 +443,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float ref = m_use == -INFINITY ? 0.f : m_use;
       // the P buffer is free once P V of tile it-2 has completed
       if (it >= 2) {
-        w_ok = mbar_wait_bounded(bar(kBarPvDone + kb), ((it - 2) >> 1) & 1);
-        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+        w_ok = mbar_wait_bounded(bar(kBarPvDone + sb), ((it - 2) >> 1) & 1);
+        if (!pair_and(__all_sync(0xFFFFFFFFu, w_ok), pair)) {
           good = false;
           break;
         }
@@ -394,22 +452,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // P = 2^(z - m): the row sum takes P, the P V operand P' = P s_v (0 for
       // tokens past the row, whose scale slots may hold anything)
 #pragma unroll
-      for (int t = 0; t < kTcKv; ++t) z[t] = fast_exp2(z[t] - ref);
-      float lsum;
+      for (int t = 0; t < kTcHalf; ++t) z[t] = fast_exp2(z[t] - ref);
       {
-        float sr2[kTcKv / 2];
+        float sr2[kTcHalf / 2];
 #pragma unroll
-        for (int t = 0; t < kTcKv / 2; ++t) sr2[t] = z[t] + z[t + kTcKv / 2];
+        for (int t = 0; t < kTcHalf / 2; ++t) sr2[t] = z[t] + z[t + kTcHalf / 2];
 #pragma unroll
-        for (int w = kTcKv / 4; w >= 1; w >>= 1)
+        for (int w = kTcHalf / 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int t = 0; t < w; ++t) sr2[t] += sr2[t + w];
-        lsum = sr2[0];
+        l += sr2[0];
       }
-      uint8_t* prow = smem + Ly::kP + kb * Ly::kPBytes + r * 128;
+      uint32_t pk[kTcHalf / 2];                   // P' packed two FP16 per TMEM column
 #pragma unroll
-      for (int cc = 0; cc < kTcKv / 8; ++cc) {
-        const float4 v0 = cs4[(kTcKv + 8 * cc) / 4], v1 = cs4[(kTcKv + 8 * cc) / 4 + 1];
+      for (int cc = 0; cc < kTcHalf / 8; ++cc) {
+        const float4 v0 = cs4[kTcKv / 4 + 2 * cc], v1 = cs4[kTcKv / 4 + 2 * cc + 1];
         float a8[8] = {z[8 * cc] * v0.x,     z[8 * cc + 1] * v0.y, z[8 * cc + 2] * v0.z,
                        z[8 * cc + 3] * v0.w, z[8 * cc + 4] * v1.x, z[8 * cc + 5] * v1.y,
                        z[8 * cc + 6] * v1.z, z[8 * cc + 7] * v1.w};
@@ -418,39 +475,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int e2 = 0; e2 < 8; ++e2)
             if (t0 + 8 * cc + e2 > pos) a8[e2] = 0.f;
         }
-        uint4 pk;
-        pk.x = h2_as_u32(__floats2half2_rn(a8[0], a8[1]));
-        pk.y = h2_as_u32(__floats2half2_rn(a8[2], a8[3]));
-        pk.z = h2_as_u32(__floats2half2_rn(a8[4], a8[5]));
-        pk.w = h2_as_u32(__floats2half2_rn(a8[6], a8[7]));
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = pk;
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2)
+          pk[4 * cc + e2] = h2_as_u32(__floats2half2_rn(a8[2 * e2], a8[2 * e2 + 1]));
       }
-      l += lsum;
-      fence_proxy_async_smem();
+      tc_st16(tP + kTcHalf * sb + (kTcHalf / 2) * hh + lanes, pk);
+      tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + kb));
+      if (lane == 0) mbar_arrive(bar(kBarPFull + sb));
     }
     if (good) {
       const int last = n_it - 1;
       const bool w_ok = mbar_wait_bounded(bar(kBarPvDone + (last & 1)), (last >> 1) & 1);
-      good = __all_sync(0xFFFFFFFFu, w_ok);
+      good = pair_and(__all_sync(0xFFFFFFFFu, w_ok), pair);
     }
     if (!good) {
       if (lane == 0) fail();
     } else {
-      // ---- epilogue: O / l, rounded to the activation dtype ----
+      // ---- epilogue: this half's columns of O / l, rounded to the activation dtype ----
+      xchg[hh * kTcRows + r] = l;
+      pair_and(true, pair);
+      const float lt = l + xchg[(hh ^ 1) * kTcRows + r];
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       uint16_t* dst = static_cast<uint16_t*>(p.out) +
-                      ((int64_t)(q0 + (pos >= 0 ? iq : 0)) * p.Hq + (int64_t)j * G + r % G) * D;
+                      ((int64_t)(q0 + (pos >= 0 ? iq : 0)) * p.Hq + (int64_t)j * G + r % G) * D +
+                      hh * (D / 2);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tc_ld32(tO + c0 + lanes, o);
+      for (int c0 = 0; c0 < D / 2; c0 += 16) {
+        uint32_t o[16];
+        tc_ld16(tO + hh * (D / 2) + c0 + lanes, o);
         if (pos >= 0) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 8) {
+          for (int x = 0; x < 16; x += 8) {
             uint4 w;
             uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
@@ -471,7 +529,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == kWarpMma) {
     tc_fence_after();
-    tc_dealloc(tmem, kTcCols);
+    tc_dealloc(tmem, tc_cols<D>());
   }
 }
 

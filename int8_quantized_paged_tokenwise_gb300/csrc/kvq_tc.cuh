@@ -86,6 +86,19 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[desc]^T for one K-step of 16, A read from tensor
+// memory: row i of A in TMEM lane i, its 16 elements packed two per 32-bit
+// column (element 2c in the low half of column c), 8 columns per K-step.
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
 // One arrival on the mbarrier once every tcgen05 operation this thread has
 // issued so far has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
