@@ -226,6 +226,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t raw_u32 = smem_u32(smem + Ly::kRaw);
     const uint32_t rawsc_u32 = smem_u32(smem + Ly::kRawSc);
     int issued = 0;
+    // block ids of 32 pages (8 tiles) at a time, one per lane, checked once
+    auto load_ids = [&](int base) -> int {
+      int id = -1;
+      if (base + lane < npages) {
+        id = __ldg(&bt[base + lane]);
+        if (id < 0 || id >= p.num_blocks) {
+          atomicOr(p.err, 0x2u);
+          id = -1;
+        }
+      }
+      return id;
+    };
+    int ids = load_ids(0), ids_next = npages > 32 ? load_ids(32) : -1;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % kTcRaw;
       if (it >= kTcRaw && !mbar_wait_bounded(bar(kBarRawEmpty + s), ((it / kTcRaw) - 1) & 1)) {
@@ -233,16 +246,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       if (*abort_flag) break;
-      // lanes 4 k + pg: page pg of the tile, copy k (K tile, V tile, K scales, V scales)
-      const int pg = it * kTcPages + (lane & 3);
-      int blk = -1;
-      if (lane < 4 * kTcPages && pg < npages) {
-        blk = __ldg(&bt[pg]);
-        if (blk < 0 || blk >= p.num_blocks) {
-          if (lane < 4) atomicOr(p.err, 0x2u);
-          blk = -1;
-        }
+      const int chunk_it = it % (32 / kTcPages);
+      if (it > 0 && chunk_it == 0) {              // next 32 pages; prefetch the ones after
+        ids = ids_next;
+        const int nb = (it / (32 / kTcPages) + 1) * 32;
+        ids_next = nb < npages ? load_ids(nb) : -1;
       }
+      // lanes 4 k + pg: page pg of the tile, copy k (K tile, V tile, K scales, V scales)
+      int blk = __shfl_sync(0xFFFFFFFFu, ids, kTcPages * chunk_it + (lane & 3));
+      if (lane >= 4 * kTcPages) blk = -1;
       const uint32_t loaded = __ballot_sync(0xFFFFFFFFu, lane < kTcPages && blk >= 0);
       const uint32_t full = bar(kBarRawFull + s);
       if (lane == 0) {
@@ -381,17 +393,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int t0 = it * kTcKv + hh * kTcHalf;   // first token of this half
       const bool masked = t0 + kTcHalf - 1 > pos;  // some token of the half is past the row
       float z[kTcHalf];
+      {
+        uint32_t sr[kTcHalf];                     // one TMEM load (and wait) for the half row
+        tc_ld32(tS + kTcKv * sb + kTcHalf * hh + lanes, sr);
 #pragma unroll
-      for (int h = 0; h < kTcHalf / 16; ++h) {
-        uint32_t sr[16];
-        tc_ld16(tS + kTcKv * sb + kTcHalf * hh + 16 * h + lanes, sr);
-#pragma unroll
-        for (int x = 0; x < 16; x += 4) {
-          const float4 k4 = cs4[(16 * h + x) / 4];
-          z[16 * h + x] = __uint_as_float(sr[x]) * k4.x;
-          z[16 * h + x + 1] = __uint_as_float(sr[x + 1]) * k4.y;
-          z[16 * h + x + 2] = __uint_as_float(sr[x + 2]) * k4.z;
-          z[16 * h + x + 3] = __uint_as_float(sr[x + 3]) * k4.w;
+        for (int x = 0; x < kTcHalf; x += 4) {
+          const float4 k4 = cs4[x / 4];
+          z[x] = __uint_as_float(sr[x]) * k4.x;
+          z[x + 1] = __uint_as_float(sr[x + 1]) * k4.y;
+          z[x + 2] = __uint_as_float(sr[x + 2]) * k4.z;
+          z[x + 3] = __uint_as_float(sr[x + 3]) * k4.w;
         }
       }
       if (masked) {
