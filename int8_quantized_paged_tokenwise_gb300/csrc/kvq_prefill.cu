@@ -8,10 +8,11 @@
 // p = L - n + i attends causally to tokens 0..p:
 //   out[i][h] = softmax_{t<=p}(sm_scale * q[i][h] . s_k[t] code_k[t]) . (s_v code_v)
 //
-// One CTA = 128 (query, head-of-the-GQA-group) rows of one KV head of one
-// sequence (M = 128 of every MMA), streaming the sequence's tokens in tiles
-// of 64 (4 pages).  Warp roles:
-//  * warp 8, producer: block ids from the block table, TMA copies of each
+// One CTA = two consecutive tiles ("halves" A and B) of 128 (query,
+// head-of-the-GQA-group) rows of one KV head of one sequence; each half is
+// the M = 128 of its own MMAs, and both share every converted K/V tile.  The
+// sequence's tokens stream in tiles of 64 (4 pages).  Warp roles:
+//  * warp 8, producer: block ids 32 pages at a time, TMA copies of each
 //    page's INT8 K and V tiles (2-D tensor copies, 128-/64-byte swizzle) and
 //    bulk copies of its two 32-byte scale rows into a 3-stage ring;
 //  * warps 10-13, converters: INT8 codes to exact FP16 integers (byte
@@ -19,22 +20,19 @@
 //    tiles, 128-byte swizzled, in 3 buffers: K is the K-major B operand of
 //    Q K^T, V the MN-major B operand of P V; the tile's K scales (times
 //    sm_scale log2 e) and V scales as FP32 columns;
-//  * warp 9, MMA issuer (one thread): S = Q K^T into one of two 128 x 64
-//    FP32 TMEM buffers (8 MMAs of K = 16 over the head dims), and, one tile
-//    behind, O += P V into a 128 x D FP32 TMEM accumulator (4 MMAs over the
-//    tokens, A = P read from TMEM), each group's completion signalled
-//    through tcgen05.commit;
-//  * warps 0-7, softmax (two threads per row = TMEM lane, warps w and w + 4
-//    taking the two halves of the tile's 64 columns and exchanging the row
-//    maximum through shared memory at a named barrier of the pair): the
-//    row of S, times the K-scale column, causal mask, running maximum,
-//    P = 2^(z - m)
-//    with the V scale of each token folded in (P' = P s_v, FP16, stored into
-//    one of two TMEM buffers as the A operand of the next P V), row sums in
-//    FP32; O is rescaled
-//    in TMEM only when a row maximum grows by more than 2^8 over the one in
-//    use (the shift cancels in O / l, and P' stays below 2^8 s_v), and
-//    normalized and stored at the end.
+//  * warp 9, MMA issuer (one thread): per KV tile and half, P V of the
+//    previous tile (A = P read from TMEM, into the half's 128 x D FP32
+//    accumulator) and then S = Q K^T (D/16 MMAs of K = 16) into the half's
+//    128 x 64 FP32 S buffer; a commit after S therefore also covers the P V
+//    before it, so the softmax may rescale O and overwrite P as soon as S
+//    has landed;
+//  * warps 0-3 (half A) and 4-7 (half B), softmax (one thread per row =
+//    TMEM lane): the row of S times the K-scale column, causal mask, running
+//    maximum, P = 2^(z - m); the row sum takes P, and P' = P s_v (FP16) is
+//    stored into the half's TMEM P buffer as the A operand of the next P V.
+//    O is rescaled in TMEM only when a row maximum grows by more than 2^8
+//    over the one in use (the shift cancels in O / l, and P' stays below
+//    2^8 s_v); the epilogue normalizes O and stores it.
 // All waits are bounded: a timeout sets an error bit, the roles leave their
 // loops, the copies and MMAs in flight are waited for, and TMEM is freed.
 #include "kvq_decode.cuh"
@@ -43,42 +41,39 @@
 namespace kvq {
 namespace {
 
-constexpr int kTcRows = 128;                    // M: (query, head) rows per CTA
+constexpr int kTcRows = 128;                    // M: (query, head) rows per half
+constexpr int kTcHalves = 2;                    // row tiles per CTA
 constexpr int kTcKv = 64;                       // tokens per KV tile
-constexpr int kTcHalf = kTcKv / 2;              // columns per softmax thread
 constexpr int kTcPages = kTcKv / kBlockSize;     // pages per KV tile
 constexpr int kTcRaw = 3;                       // INT8 staging ring depth
 constexpr int kTcConv = 3;                      // converted (FP16) operand buffers
 constexpr int kTcWarps = 14;
 constexpr int kTcThreads = kTcWarps * 32;
-constexpr int kSoftmaxWarps = 8, kWarpTma = 8, kWarpMma = 9, kWarpCvt = 10;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpCvt = 10;
+constexpr uint32_t kTcCols = 512;
 
-// TMEM columns: O (D), two S buffers (64 FP32 each), two P buffers (64 FP16
-// = 32 columns each)
-template <int D>
-__host__ __device__ constexpr uint32_t tc_cols() {
-  return D + 2 * kTcKv + kTcKv > 256 ? 512u : 256u;
-}
+// TMEM columns of half h: O at h D, S at 2 D + 64 h, P (64 FP16 = 32 columns)
+// at 2 D + 128 + 32 h; 2 D + 192 <= 448 < 512.
 
 // barrier indices
 constexpr int kBarRawFull = 0, kBarRawEmpty = 3, kBarCvtFull = 6, kBarCvtEmpty = 9,
-              kBarSFull = 12, kBarPFull = 14, kBarPvDone = 16, kBarFin = 18, kNumBars = 19;
+              kBarSFull = 12, kBarPFull = 14, kBarODone = 16, kBarFin = 18, kNumBars = 19;
 
 // Shared memory (offsets from a 1024-aligned base; every operand tile starts
 // on a 1024-byte boundary).
 template <int D>
 struct TcLayout {
-  static constexpr int kQ = 0;                            // [128][D] FP16, D/64 tiles of 16 KB
+  static constexpr int kQBytes = kTcRows * D * 2;        // [128][D] FP16, D/64 tiles of 16 KB
+  static constexpr int kQ = 0;                            // one per half
   static constexpr int kConvBytes = kTcKv * D * 2;        // [64][D] FP16, D/64 tiles of 8 KB
-  static constexpr int kKc = kQ + kTcRows * D * 2;       // kTcConv K buffers
+  static constexpr int kKc = kQ + kTcHalves * kQBytes;   // kTcConv K buffers
   static constexpr int kVc = kKc + kTcConv * kConvBytes; // kTcConv V buffers
   static constexpr int kTile = kBlockSize * D;           // one page's INT8 K (or V) tile
   static constexpr int kRawBytes = 2 * kTcPages * kTile; // K tiles of 4 pages, then V tiles
   static constexpr int kRaw = kVc + kTcConv * kConvBytes;          // kTcRaw stages
   static constexpr int kRawSc = kRaw + kTcRaw * kRawBytes;         // per page: K 32 B, V 32 B
   static constexpr int kColSc = kRawSc + kTcRaw * kTcPages * 64;   // per buffer: K 64, V 64 floats
-  static constexpr int kXchg = kColSc + kTcConv * 2 * kTcKv * 4;   // [2 parities][2 halves][128]
-  static constexpr int kBars = kXchg + 2 * 2 * kTcRows * 4;
+  static constexpr int kBars = kColSc + kTcConv * 2 * kTcKv * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;     // TMEM base, abort flag
   static constexpr size_t kTotal = (size_t)kMisc + 16 + 1024;      // + base alignment slack
 };
@@ -103,42 +98,6 @@ __device__ __forceinline__ void convert_chunk(const uint8_t* src, uint8_t* dst, 
   *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (t & 7)) << 4)) = hi;
 }
 
-// Named barrier of the two softmax warps that share a row block (ids 1..4),
-// with an AND over the 64 threads' predicates.
-__device__ __forceinline__ bool pair_and(bool v, int id) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, 64, p;\n\tselp.b32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(v ? 1u : 0u), "r"(id)
-      : "memory");
-  return r != 0;
-}
-
-// 16 consecutive FP32 columns of this thread's TMEM lane (warp-wide), waited for.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -154,8 +113,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z, j = blockIdx.y, G = p.G;
-  const int TQ = kTcRows / G;                     // queries per tile
-  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;   // latest (longest) tiles first
+  const int TH = kTcRows / G;                     // queries per half
+  const int ct_idx = (int)gridDim.x - 1 - (int)blockIdx.x;   // latest (longest) tiles first
 
   if (tid == 0) {
     prefetch_tensormap(&tmK);
@@ -166,7 +125,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t count = 1;                           // TMA transactions, commits
     if (tid >= kBarRawEmpty && tid < kBarRawEmpty + kTcRaw) count = 4;     // converter warps
     if (tid >= kBarCvtFull && tid < kBarCvtFull + kTcConv) count = 4;      // converter warps
-    if (tid >= kBarPFull && tid < kBarPFull + 2) count = kSoftmaxWarps;    // softmax warps
+    if (tid >= kBarPFull && tid < kBarPFull + kTcHalves) count = 4;        // a half's softmax warps
     mbar_init(bar(tid), count);
   }
   griddep_wait();
@@ -176,24 +135,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int L = __ldg(&p.context_lens[b]);
   const int max_tok = min(p.max_blocks * kBlockSize, p.max_ctx);
   if (L < 0 || L > max_tok || n < 0 || n > L || n > p.max_q || q0 < 0 || q0 + n > p.total_q) {
-    if (tid == 0 && qt == 0 && j == 0) atomicOr(p.err, 0x4u);
+    if (tid == 0 && ct_idx == 0 && j == 0) atomicOr(p.err, 0x4u);
     return;                                      // nothing issued or allocated yet
   }
-  const int i_begin = qt * TQ;
+  const int i_begin = ct_idx * kTcHalves * TH;   // first query of half A
   if (i_begin >= n) return;
-  const int i_end = min(n, i_begin + TQ);
-  const int p_last = L - n + i_end - 1;          // last query position of the tile
-  const int n_it = p_last / kTcKv + 1;           // KV tiles
-  const int npages = p_last / kBlockSize + 1;
+  // KV tiles of each half (0: no queries); half B has at least as many
+  int n_half[kTcHalves];
+#pragma unroll
+  for (int h = 0; h < kTcHalves; ++h) {
+    const int hb = i_begin + h * TH, he = min(n, hb + TH);
+    n_half[h] = hb < n ? (L - n + he - 1) / kTcKv + 1 : 0;
+  }
+  const int n_it = max(n_half[0], n_half[1]);    // KV tiles of the CTA
+  const int npages = min((L - n + min(n, i_begin + kTcHalves * TH) - 1) / kBlockSize + 1,
+                         n_it * kTcPages);
 
-  if (warp == kWarpMma) tc_alloc(smem_u32(&misc[0]), tc_cols<D>());
+  if (warp == kWarpMma) tc_alloc(smem_u32(&misc[0]), kTcCols);
 
-  // ---- Q tile: row r = (query i_begin + r / G, head j G + r % G), FP16, swizzled ----
-  for (int e = tid; e < kTcRows * (D / 8); e += kTcThreads) {
-    const int r = e / (D / 8), c8 = e - r * (D / 8);    // 16-byte chunk c8 of the row
-    const int i = i_begin + r / G;
+  // ---- Q tiles: row r of half h = (query i_begin + h TH + r / G, head j G + r % G), FP16 ----
+  for (int e = tid; e < kTcHalves * kTcRows * (D / 8); e += kTcThreads) {
+    const int hr = e / (D / 8), c8 = e - hr * (D / 8);  // 16-byte chunk c8 of row hr
+    const int h = hr / kTcRows, r = hr - h * kTcRows;
+    const int i = i_begin + h * TH + r / G;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < TQ * G && i < i_end) {
+    if (r < TH * G && i < n) {
       const uint16_t* src = static_cast<const uint16_t*>(p.q) +
                             ((int64_t)(q0 + i) * p.Hq + (int64_t)j * G + r % G) * D + 8 * c8;
       v = __ldg(reinterpret_cast<const uint4*>(src));
@@ -204,8 +170,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         v.w = bf2_to_h2(v.w);
       }
     }
-    *reinterpret_cast<uint4*>(smem + Ly::kQ + (c8 >> 3) * (kTcRows * 128) + r * 128 +
-                              (((c8 & 7) ^ (r & 7)) << 4)) = v;
+    *reinterpret_cast<uint4*>(smem + Ly::kQ + h * Ly::kQBytes + (c8 >> 3) * (kTcRows * 128) +
+                              r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) = v;
   }
   fence_proxy_async_smem();
   fence_mbar_init();
@@ -213,8 +179,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const uint32_t tO = tmem, tS = tmem + D;        // S buffer k at tS + 64 k
-  const uint32_t tP = tS + 2 * kTcKv;             // P buffer k at tP + 32 k
+  auto tO = [&](int h) { return tmem + (uint32_t)(h * D); };
+  auto tS = [&](int h) { return tmem + (uint32_t)(2 * D + kTcKv * h); };
+  auto tP = [&](int h) { return tmem + (uint32_t)(2 * D + 2 * kTcKv + (kTcKv / 2) * h); };
   auto fail = [&]() {
     atomicOr(p.err, 0x8u);
     *abort_flag = 1;
@@ -325,43 +292,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = tc_idesc_f16(kTcKv, false);
       constexpr uint32_t idO = tc_idesc_f16(D, false, true);
-      const uint32_t q_u32 = smem_u32(smem + Ly::kQ);
-      auto issue_pv = [&](int k) -> bool {
-        const int sb = k & 1, cb = k % kTcConv;
-        if (!mbar_wait_bounded(bar(kBarPFull + sb), (k >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(smem + Ly::kVc + cb * Ly::kConvBytes);
-#pragma unroll
-        for (int ts = 0; ts < kTcKv / 16; ++ts)
-          tc_mma_f16_tmem_a(tO, tP + kTcHalf * sb + 8 * ts,
-                            tc_desc_sw128_mn(vb + 16 * 128 * ts, kTcKv * 128), idO,
-                            k > 0 || ts > 0);
-        tc_commit(bar(kBarPvDone + sb));
-        tc_commit(bar(kBarCvtEmpty + cb));
-        return true;
-      };
       bool good = true;
-      for (int it = 0; it < n_it; ++it) {
-        const int sb = it & 1, cb = it % kTcConv;
-        if (!mbar_wait_bounded(bar(kBarCvtFull + cb), (it / kTcConv) & 1) || *abort_flag) {
-          good = false;
-          break;
+      // step it: P V of tile it-1 then S of tile it, for each half in range
+      for (int it = 0; it <= n_it && good; ++it) {
+        const int cb = it % kTcConv, pcb = (it + kTcConv - 1) % kTcConv;
+        if (it < n_it) {
+          if (!mbar_wait_bounded(bar(kBarCvtFull + cb), (it / kTcConv) & 1) || *abort_flag) {
+            good = false;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-        const uint32_t kbase = smem_u32(smem + Ly::kKc + cb * Ly::kConvBytes);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_f16(tS + kTcKv * sb,
-                     tc_desc_sw128(q_u32 + (ks >> 2) * (kTcRows * 128) + 32 * (ks & 3)),
-                     tc_desc_sw128(kbase + (ks >> 2) * (kTcKv * 128) + 32 * (ks & 3)), idS,
-                     ks > 0);
-        tc_commit(bar(kBarSFull + sb));
-        if (it > 0 && !issue_pv(it - 1)) {
-          good = false;
-          break;
+        for (int h = 0; h < kTcHalves; ++h) {
+          if (it >= 1 && it <= n_half[h]) {
+            const int k = it - 1;
+            if (!mbar_wait_bounded(bar(kBarPFull + h), k & 1)) {
+              good = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vb = smem_u32(smem + Ly::kVc + pcb * Ly::kConvBytes);
+#pragma unroll
+            for (int ts = 0; ts < kTcKv / 16; ++ts)
+              tc_mma_f16_tmem_a(tO(h), tP(h) + 8 * ts,
+                                tc_desc_sw128_mn(vb + 16 * 128 * ts, kTcKv * 128), idO,
+                                k > 0 || ts > 0);
+            if (it == n_half[h]) tc_commit(bar(kBarODone + h));   // the half's O is final
+          }
+          if (it < n_half[h]) {
+            const uint32_t qa = smem_u32(smem + Ly::kQ + h * Ly::kQBytes);
+            const uint32_t kbase = smem_u32(smem + Ly::kKc + cb * Ly::kConvBytes);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+              tc_mma_f16(tS(h), tc_desc_sw128(qa + (ks >> 2) * (kTcRows * 128) + 32 * (ks & 3)),
+                         tc_desc_sw128(kbase + (ks >> 2) * (kTcKv * 128) + 32 * (ks & 3)), idS,
+                         ks > 0);
+            tc_commit(bar(kBarSFull + h));         // also covers the P V above
+          }
         }
+        if (good && it >= 1) tc_commit(bar(kBarCvtEmpty + pcb));   // tile it-1 fully used
       }
-      if (good && !issue_pv(n_it - 1)) good = false;
       if (!good) fail();
       tc_commit(bar(kBarFin));                    // every MMA issued has completed
       mbar_wait_bounded(bar(kBarFin), 0);
@@ -369,114 +340,83 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
-    const int rb = warp & 3, hh = warp >> 2;      // row block, column half
-    const int r = 32 * rb + lane;                 // row = TMEM lane
-    const int pair = 1 + rb;                      // named barrier of warps rb, rb + 4
-    const int iq = i_begin + r / G;
-    const int pos = (r < TQ * G && iq < i_end) ? L - n + iq : -1;   // -1: padding row
-    const uint32_t lanes = (uint32_t)(32 * rb) << 16;
-    float* xchg = reinterpret_cast<float*>(smem + Ly::kXchg);         // [parity][half][row]
-    float m_use = -INFINITY, l = 0.f;             // l: this half's share of the row sum
+    const int h = warp >> 2;                      // half
+    const int r = 32 * (warp & 3) + lane;         // row = TMEM lane
+    const int iq = i_begin + h * TH + r / G;
+    const int pos = (r < TH * G && iq < n) ? L - n + iq : -1;   // -1: padding row
+    const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
+    const int nh = n_half[h];
+    float m_use = -INFINITY, l = 0.f;
     bool good = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int sb = it & 1, cb = it % kTcConv;
-      bool w_ok = mbar_wait_bounded(bar(kBarCvtFull + cb), (it / kTcConv) & 1) &&
-                  mbar_wait_bounded(bar(kBarSFull + sb), (it >> 1) & 1);
-      if (!pair_and(__all_sync(0xFFFFFFFFu, w_ok), pair)) {
+    for (int it = 0; it < nh; ++it) {
+      const int cb = it % kTcConv;
+      // S of this tile has landed (and with it the P V of the previous tile)
+      const bool w_ok = mbar_wait_bounded(bar(kBarCvtFull + cb), (it / kTcConv) & 1) &&
+                        mbar_wait_bounded(bar(kBarSFull + h), it & 1);
+      if (!__all_sync(0xFFFFFFFFu, w_ok)) {
         good = false;
         break;
       }
       tc_fence_after();
-      // this half's scale columns: K (times sm_scale log2 e), then V
-      const float4* cs4 = reinterpret_cast<const float4*>(smem + Ly::kColSc) +
-                          cb * (kTcKv / 2) + hh * (kTcHalf / 4);
-      const int t0 = it * kTcKv + hh * kTcHalf;   // first token of this half
-      const bool masked = t0 + kTcHalf - 1 > pos;  // some token of the half is past the row
-      float z[kTcHalf];
-      {
-        uint32_t sr[kTcHalf];                     // one TMEM load (and wait) for the half row
-        tc_ld32(tS + kTcKv * sb + kTcHalf * hh + lanes, sr);
+      // scale columns of the tile: K (times sm_scale log2 e) at [0, 64), V at [64, 128)
+      const float4* cs4 = reinterpret_cast<const float4*>(smem + Ly::kColSc) + cb * (kTcKv / 2);
+      const int t0 = it * kTcKv;
+      const bool masked = t0 + kTcKv - 1 > pos;    // some token of the tile is past the row
+      float z[kTcKv];
 #pragma unroll
-        for (int x = 0; x < kTcHalf; x += 4) {
-          const float4 k4 = cs4[x / 4];
-          z[x] = __uint_as_float(sr[x]) * k4.x;
-          z[x + 1] = __uint_as_float(sr[x + 1]) * k4.y;
-          z[x + 2] = __uint_as_float(sr[x + 2]) * k4.z;
-          z[x + 3] = __uint_as_float(sr[x + 3]) * k4.w;
+      for (int hc = 0; hc < kTcKv / 32; ++hc) {
+        uint32_t sr[32];
+        tc_ld32(tS(h) + 32 * hc + lanes, sr);
+#pragma unroll
+        for (int x = 0; x < 32; x += 4) {
+          const float4 k4 = cs4[(32 * hc + x) / 4];
+          z[32 * hc + x] = __uint_as_float(sr[x]) * k4.x;
+          z[32 * hc + x + 1] = __uint_as_float(sr[x + 1]) * k4.y;
+          z[32 * hc + x + 2] = __uint_as_float(sr[x + 2]) * k4.z;
+          z[32 * hc + x + 3] = __uint_as_float(sr[x + 3]) * k4.w;
         }
       }
       if (masked) {
 #pragma unroll
-        for (int t = 0; t < kTcHalf; ++t)
+        for (int t = 0; t < kTcKv; ++t)
           if (t0 + t > pos) z[t] = -INFINITY;
       }
       float mx;
       {
-        float mr[kTcHalf / 2];                     // pairwise tree: short dependency chains
+        float mr[kTcKv / 2];                       // pairwise tree: short dependency chains
 #pragma unroll
-        for (int t = 0; t < kTcHalf / 2; ++t) mr[t] = fmaxf(z[t], z[t + kTcHalf / 2]);
+        for (int t = 0; t < kTcKv / 2; ++t) mr[t] = fmaxf(z[t], z[t + kTcKv / 2]);
 #pragma unroll
-        for (int w = kTcHalf / 4; w >= 1; w >>= 1)
+        for (int w = kTcKv / 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int t = 0; t < w; ++t) mr[t] = fmaxf(mr[t], mr[t + w]);
         mx = mr[0];
       }
-      // row maximum over both halves (buffers alternate by iteration parity)
-      xchg[(sb * 2 + hh) * kTcRows + r] = mx;
-      pair_and(true, pair);
-      mx = fmaxf(mx, xchg[(sb * 2 + (hh ^ 1)) * kTcRows + r]);
       const bool grow = mx > m_use + 8.f;
       const float m_new = grow ? mx : m_use;
       const bool resc = grow && m_use != -INFINITY;
-      if (__any_sync(0xFFFFFFFFu, resc)) {
-        // O holds P V of tiles 0..it-1: once the last has completed, rescale
-        // this half's columns of the rows whose maximum moved (the partner
-        // warp decides identically: same rows, same maxima)
-        w_ok = mbar_wait_bounded(bar(kBarPvDone + ((it - 1) & 1)), ((it - 1) >> 1) & 1);
-        if (!pair_and(__all_sync(0xFFFFFFFFu, w_ok), pair)) {
-          good = false;
-          break;
-        }
-        tc_fence_after();
-        const float alpha = resc ? fast_exp2(m_use - m_new) : 1.f;
-#pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 16) {
-          uint32_t o[16];
-          tc_ld16(tO + hh * (D / 2) + c0 + lanes, o);
-#pragma unroll
-          for (int x = 0; x < 16; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          tc_st16(tO + hh * (D / 2) + c0 + lanes, o);
-        }
-        tc_wait_st();
-        l *= alpha;
-      }
+      const float alpha = resc ? fast_exp2(m_use - m_new) : 1.f;
       m_use = m_new;
       const float ref = m_use == -INFINITY ? 0.f : m_use;
-      // the P buffer is free once P V of tile it-2 has completed
-      if (it >= 2) {
-        w_ok = mbar_wait_bounded(bar(kBarPvDone + sb), ((it - 2) >> 1) & 1);
-        if (!pair_and(__all_sync(0xFFFFFFFFu, w_ok), pair)) {
-          good = false;
-          break;
-        }
-      }
       // P = 2^(z - m): the row sum takes P, the P V operand P' = P s_v (0 for
       // tokens past the row, whose scale slots may hold anything)
 #pragma unroll
-      for (int t = 0; t < kTcHalf; ++t) z[t] = fast_exp2(z[t] - ref);
+      for (int t = 0; t < kTcKv; ++t) z[t] = fast_exp2(z[t] - ref);
+      float lsum;
       {
-        float sr2[kTcHalf / 2];
+        float sr2[kTcKv / 2];
 #pragma unroll
-        for (int t = 0; t < kTcHalf / 2; ++t) sr2[t] = z[t] + z[t + kTcHalf / 2];
+        for (int t = 0; t < kTcKv / 2; ++t) sr2[t] = z[t] + z[t + kTcKv / 2];
 #pragma unroll
-        for (int w = kTcHalf / 4; w >= 1; w >>= 1)
+        for (int w = kTcKv / 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int t = 0; t < w; ++t) sr2[t] += sr2[t + w];
-        l += sr2[0];
+        lsum = sr2[0];
       }
-      uint32_t pk[kTcHalf / 2];                   // P' packed two FP16 per TMEM column
+      l = l * alpha + lsum;
+      uint32_t pk[kTcKv / 2];                     // P' packed two FP16 per TMEM column
 #pragma unroll
-      for (int cc = 0; cc < kTcHalf / 8; ++cc) {
+      for (int cc = 0; cc < kTcKv / 8; ++cc) {
         const float4 v0 = cs4[kTcKv / 4 + 2 * cc], v1 = cs4[kTcKv / 4 + 2 * cc + 1];
         float a8[8] = {z[8 * cc] * v0.x,     z[8 * cc + 1] * v0.y, z[8 * cc + 2] * v0.z,
                        z[8 * cc + 3] * v0.w, z[8 * cc + 4] * v1.x, z[8 * cc + 5] * v1.y,
@@ -490,36 +430,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int e2 = 0; e2 < 4; ++e2)
           pk[4 * cc + e2] = h2_as_u32(__floats2half2_rn(a8[2 * e2], a8[2 * e2 + 1]));
       }
-      tc_st16(tP + kTcHalf * sb + (kTcHalf / 2) * hh + lanes, pk);
-      tc_wait_st();
+      tc_st32(tP(h) + lanes, pk);
+      if (__any_sync(0xFFFFFFFFu, resc)) {
+        // O holds P V of tiles 0..it-1 (complete: S of this tile was
+        // committed after them): rescale the rows whose maximum moved
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tc_ld32(tO(h) + c0 + lanes, o);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+          tc_st32(tO(h) + c0 + lanes, o);
+        }
+      }
+      tc_st32(tP(h) + lanes, pk);
+      tc_wait_st();                               // P and any rescaled O are in TMEM
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + sb));
+      if (lane == 0) mbar_arrive(bar(kBarPFull + h));
     }
-    if (good) {
-      const int last = n_it - 1;
-      const bool w_ok = mbar_wait_bounded(bar(kBarPvDone + (last & 1)), (last >> 1) & 1);
-      good = pair_and(__all_sync(0xFFFFFFFFu, w_ok), pair);
+    if (good && nh > 0) {
+      const bool w_ok = mbar_wait_bounded(bar(kBarODone + h), 0);
+      good = __all_sync(0xFFFFFFFFu, w_ok);
     }
     if (!good) {
       if (lane == 0) fail();
-    } else {
-      // ---- epilogue: this half's columns of O / l, rounded to the activation dtype ----
-      xchg[hh * kTcRows + r] = l;
-      pair_and(true, pair);
-      const float lt = l + xchg[(hh ^ 1) * kTcRows + r];
+    } else if (nh > 0) {
+      // ---- epilogue: O / l, rounded to the activation dtype ----
       tc_fence_after();
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
       uint16_t* dst = static_cast<uint16_t*>(p.out) +
-                      ((int64_t)(q0 + (pos >= 0 ? iq : 0)) * p.Hq + (int64_t)j * G + r % G) * D +
-                      hh * (D / 2);
+                      ((int64_t)(q0 + (pos >= 0 ? iq : 0)) * p.Hq + (int64_t)j * G + r % G) * D;
 #pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 16) {
-        uint32_t o[16];
-        tc_ld16(tO + hh * (D / 2) + c0 + lanes, o);
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tc_ld32(tO(h) + c0 + lanes, o);
         if (pos >= 0) {
 #pragma unroll
-          for (int x = 0; x < 16; x += 8) {
+          for (int x = 0; x < 32; x += 8) {
             uint4 w;
             uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
@@ -540,7 +488,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == kWarpMma) {
     tc_fence_after();
-    tc_dealloc(tmem, tc_cols<D>());
+    tc_dealloc(tmem, kTcCols);
   }
 }
 
@@ -550,7 +498,7 @@ size_t prefill_smem_bytes(int D) {
   return D == 128 ? TcLayout<128>::kTotal : TcLayout<64>::kTotal;
 }
 
-int prefill_rows_per_cta() { return kTcRows; }
+int prefill_rows_per_cta() { return kTcHalves * kTcRows; }
 
 cudaError_t prefill_configure(int D, bool bf16) {
   const void* f = D == 128 ? (bf16 ? reinterpret_cast<const void*>(&paged_prefill_kernel<128, true>)
