@@ -77,3 +77,28 @@ def test_prefill_flags_chunk_longer_than_context():
     st, flags = kvq.kvq_get_error()
     assert st == 5 and flags & kvq.DEVERR_CONTEXT
     assert kvq.kvq_get_error() == (0, 0)
+
+
+@pytest.mark.slow
+def test_prefill_full_size_sampled():
+    """The timed 8K shape (one sequence of 8192 cached tokens, all of them
+    queries, 64 query / 8 KV heads, bf16) in the launch configuration the
+    bench times; sampled query rows (both ends, tile and CTA boundaries, and
+    random ones) against the oracle's decode over the row's causal prefix (a
+    one-query chunk at position p is the decode over tokens 0..p)."""
+    L, Hq, Hkv, D = 8192, 64, 8, 128
+    w = W.custom(1, Hq, Hkv, D, "bf16", [L], seed=97)
+    case = Case(w)
+    case.write_prefix()
+    qb = _queries(w, [L], seed=98)
+    qs = torch.tensor([0, L], dtype=torch.int32, device="cuda")
+    out = kvq.kvq_paged_prefill(to_dev(qb, "bf16"), *case.int8, case.bt, case.cl, qs, L, L,
+                                w.sm_scale)
+    ob = out_bits(out)
+    k, v = w.seq_kv(0)
+    rows = {0, 1, 15, 16, 31, 32, 63, 64, 4095, 4096, 8190, 8191}
+    rows |= set(np.random.default_rng(99).integers(0, L, 12).tolist())
+    for i in sorted(rows):
+        ref, _ = oracle.decode_sequence(qb[i], k[:i + 1], v[:i + 1], "bf16", w.sm_scale)
+        assert_attention_close(ob[i], ref, "bf16", f"query {i}")
+    assert kvq.kvq_get_error() == (0, 0)
