@@ -11,7 +11,7 @@ import torch
 import int8_quantized_paged_tokenwise_gb300 as kvq
 import oracle
 import workloads as W
-from _harness import Case, assert_attention_close, out_bits, to_dev
+from _harness import Case, assert_attention_close, bits_f64, out_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -101,4 +101,47 @@ def test_prefill_full_size_sampled():
     for i in sorted(rows):
         ref, _ = oracle.decode_sequence(qb[i], k[:i + 1], v[:i + 1], "bf16", w.sm_scale)
         assert_attention_close(ob[i], ref, "bf16", f"query {i}")
+    assert kvq.kvq_get_error() == (0, 0)
+
+
+def _ramped(w, b, gain, spike=None):
+    """Sequence b's K with magnitudes growing along the sequence (token t
+    scaled by 1 + gain t), so the scores of later tiles exceed a row's
+    running maximum by far more than 2^8 and the kernels' rescale of O runs
+    again and again; `spike` = (token, factor) multiplies one token's key."""
+    k, v = w.seq_kv(b)
+    kf = bits_f64(k, w.dtype)
+    kf *= (1.0 + gain * np.arange(kf.shape[0]))[:, None, None]
+    if spike is not None:
+        kf[spike[0]] *= spike[1]
+    return W.to_bits(kf.astype(np.float32), w.dtype), v
+
+
+@pytest.mark.parametrize("G,dtype,chunk", [(4, "bf16", 700), (1, "fp16", 700), (8, "bf16", 130)])
+def test_prefill_rescale_path(G, dtype, chunk):
+    """Scores that keep growing along the sequence (and one outsized key)
+    drive the softmax's rescale of the TMEM accumulator: every row against
+    the oracle (which has no such shortcut)."""
+    Hkv, D, L = 2, 128, 700
+    w = W.custom(2, G * Hkv, Hkv, D, dtype, [L, L], seed=101 + G)
+    case = Case(w)
+    seqs = [_ramped(w, 0, 0.02), _ramped(w, 1, 0.0, spike=(400, 40.0))]
+    for b, (k, v) in enumerate(seqs):
+        case._write(k, v, w.slots(b, 0, L))
+    chunks = [chunk, chunk]
+    qb = _queries(w, chunks, seed=102 + G)
+    qs = torch.tensor([0, chunk, 2 * chunk], dtype=torch.int32, device="cuda")
+    out = kvq.kvq_paged_prefill(to_dev(qb, dtype), *case.int8, case.bt, case.cl, qs, L, chunk,
+                                w.sm_scale)
+    ob = out_bits(out)
+    for b, (k, v) in enumerate(seqs):
+        ref, _ = oracle.prefill_sequence(qb[b * chunk:(b + 1) * chunk], k, v, dtype, w.sm_scale)
+        for i in range(chunk):
+            assert_attention_close(ob[b * chunk + i], ref[i], dtype, f"seq {b} query {i}")
+    # the same caches through the decode (its running maximum moves every page)
+    out_d = kvq.kvq_paged_decode(to_dev(qb[[chunk - 1, 2 * chunk - 1]], dtype), *case.int8,
+                                 case.bt, case.cl, L, w.sm_scale)
+    for b, (k, v) in enumerate(seqs):
+        ref, _ = oracle.decode_sequence(qb[(b + 1) * chunk - 1], k, v, dtype, w.sm_scale)
+        assert_attention_close(out_bits(out_d)[b], ref, dtype, f"decode seq {b}")
     assert kvq.kvq_get_error() == (0, 0)
