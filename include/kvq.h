@@ -201,8 +201,12 @@ size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
  *     sequence's L_b = context_lens[b] tokens; query i sits at position
  *     p = L_b - n_b + i and attends to tokens 0..p:
  *     out[query_start[b] + i][h] = softmax_{t<=p}(sm_scale q . k_hat_t) . v_hat
- * Arithmetic: q and codes in FP16 on the tensor cores, FP32 accumulation and
- * softmax, output rounded to `dtype`.
+ * Arithmetic: q and codes in FP16 on the 5th-generation tensor cores
+ * (tcgen05, FP32 accumulators in tensor memory), K scales on the FP32
+ * scores, softmax in FP32, V scales folded into the FP16 probabilities
+ * (P s_v), output rounded to `dtype`.  Each CTA covers 256 (query, head)
+ * rows of one KV head, so the grid is ceil(max_query_len / (256 / G)) x
+ * num_kv_heads x num_seqs.
  *
  *   q, out          [total_q][num_q_heads][head_dim] of `dtype`, 16-byte aligned.
  *   query_start     device int32 [num_seqs + 1], non-decreasing, from 0.
