@@ -443,8 +443,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_st32(tO(h) + c0 + lanes, o);
         }
       }
-      tc_st32(tP(h) + lanes, pk);
-      tc_wait_st();                               // P and any rescaled O are in TMEM
+      tc_wait_st();                               // P' and any rescaled O are in TMEM
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPFull + h));
