@@ -89,6 +89,26 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def max_over_ranks(pg, device, xs):
+    """Per-rank values -> their maximum over the ranks of `pg` (one
+    all-reduce; unchanged without a process group).  The bench reports the
+    slowest rank's time for every arm."""
+    vals = [float(x) for x in xs]
+    if pg is None:
+        return vals
+    import torch
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(world: int, bytes_per_rank_step: float, step_ms: float) -> float:
+    """Whole-job GB/s of `world` independent replicas, each moving
+    `bytes_per_rank_step` per step, over the slowest rank's step time
+    (weak scaling: the per-GPU work is fixed as the job grows)."""
+    return world * bytes_per_rank_step / (step_ms * 1e-3) / 1e9
+
+
 def decode_source_hash() -> str:
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
@@ -548,13 +568,6 @@ def main():
         if pg is not None:
             pg.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if pg is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        return float(t.item())
-
     clocks = ClockSampler(local_rank)
     barrier()
     t_step, t_dec = time_arm(torch, flush, g.append_int8, g.decode_int8, args.steps, args.warmup,
@@ -566,13 +579,10 @@ def main():
     t_e2e, h2d, d2h = time_e2e(torch, g, flush, args.steps, args.warmup)
     barrier()
 
-    step_ms = max_over_ranks(statistics.mean(t_step))
-    dec_ms = max_over_ranks(statistics.mean(t_dec))
-    step16_ms = max_over_ranks(statistics.mean(t_step16))
-    dec16_ms = max_over_ranks(statistics.mean(t_dec16))
-    e2e_ms = max_over_ranks(statistics.mean(t_e2e))
+    step_ms, dec_ms, step16_ms, dec16_ms, e2e_ms = max_over_ranks(
+        pg, dev, [statistics.mean(t) for t in (t_step, t_dec, t_step16, t_dec16, t_e2e)])
     step_bytes = w.append_bytes_int8() + w.decode_bytes_int8()
-    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    value = job_throughput(world, step_bytes, step_ms)
     dec_gbs = w.decode_bytes_int8() / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
     traffic = read_traffic(w.name)
@@ -615,7 +625,7 @@ def main():
                      "peak_kind": peak_kind,
                      "kernel": "kvq_paged_decode (decode + split-K combine), algorithmic bytes "
                                f"{w.decode_bytes_int8()} per launch"},
-        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+        "e2e": {"value": round(job_throughput(world, step_bytes, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": args.steps * g.launches_per_step(),
