@@ -155,10 +155,12 @@ def config_of(w: W.Workload, extra=None):
 
 
 # ------------------------------------------------------------- CPU oracle ---
-def time_oracle(w: W.Workload, budget_s: float, start_seq: int = 0, max_seqs: int | None = None):
+def time_oracle(w: W.Workload, budget_s: float, start_seq: int = 0, max_seqs: int | None = None,
+                stride: int = 1):
     """The FP64 oracle as it stands, single thread: quantize-append of the
     step's token + decode (it re-quantizes the context from the unpaged token
-    arrays) for whole sequences until the time budget is spent."""
+    arrays) for whole sequences start_seq, start_seq + stride, ... until the
+    time budget is spent.  Returns (GB/s, sequences, busy seconds)."""
     import oracle
     oracle.build()
     nb, bt, _ = w.tables()
@@ -179,8 +181,48 @@ def time_oracle(w: W.Workload, budget_s: float, start_seq: int = 0, max_seqs: in
         bytes_done += L * w.num_kv_heads * (2 * w.head_dim + 4) + w.pages(L) * 4 + \
             2 * w.num_q_heads * w.head_dim * 2
         n += 1
-        b += 1
+        b += stride
     return bytes_done / t_total / 1e9, n, t_total
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_job(job):
+    """Pool worker: the oracle on sequences start, start + stride, ... (bytes, n)."""
+    name, budget_s, start, stride, max_seqs = job
+    w = W.make(name)
+    gbs, n, t = time_oracle(w, budget_s, start_seq=start, max_seqs=max_seqs, stride=stride)
+    return gbs * 1e9 * t, n
+
+
+def time_oracle_parallel(w: W.Workload, budget_s: float, workers: int, rounds: int = 1,
+                         warmup_rounds: int = 1):
+    """The same oracle calls on `workers` spawned host processes (one sequence
+    stream each, disjoint), `rounds` times: per round either one sequence per
+    worker (budget_s == 0) or about budget_s of work per worker.  Returns the
+    per-round (GB/s over the round's wall time, sequences, wall seconds)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    per = 1 if budget_s <= 0 else None
+    out = []
+    with ctx.Pool(workers) as pool:
+        jobs = lambda r: [(w.name, budget_s, r * workers + i, 1 if per else workers, per)  # noqa
+                          for i in range(workers)]
+        limit = 120.0 + 4 * max(budget_s, 1.0)          # seconds a round may take
+        for r in range(warmup_rounds):                # imports and library load in each worker
+            warm = [(w.name, 0.0, r * workers + i, 1, 1) for i in range(workers)]
+            pool.map_async(_oracle_job, warm).get(timeout=limit)
+        for r in range(rounds):
+            t0 = time.perf_counter()
+            res = pool.map_async(_oracle_job, jobs(warmup_rounds + r)).get(timeout=limit)
+            wall = time.perf_counter() - t0
+            out.append((sum(x[0] for x in res) / wall / 1e9, sum(x[1] for x in res), wall))
+    return out
 
 
 def run_reference(args):
@@ -188,24 +230,32 @@ def run_reference(args):
     if rank != 0:
         return
     w = W.make(args.workload)
-    per_step = 4
-    for i in range(args.warmup):
-        time_oracle(w, 0.0, start_seq=i * per_step, max_seqs=per_step)
-    vals, times = [], []
-    for i in range(args.steps):
-        gbs, n, t = time_oracle(w, 0.0, start_seq=(args.warmup + i) * per_step, max_seqs=per_step)
-        vals.append(gbs)
-        times.append(t)
-    total_bytes = sum(v * t for v, t in zip(vals, times))
+    cores = host_cores()
+    how = "one per host core in spawned processes"
+    try:
+        # each step: one whole sequence per host core, all cores at once
+        res = time_oracle_parallel(w, 0.0, cores, rounds=args.steps,
+                                   warmup_rounds=max(args.warmup, 1))
+    except Exception as e:  # the process pool is unavailable: one core, labelled as such
+        how = f"on one core (process pool failed: {type(e).__name__})"
+        cores = 1
+        for i in range(args.warmup):
+            time_oracle(w, 0.0, start_seq=i, max_seqs=1)
+        res = [time_oracle(w, 0.0, start_seq=args.warmup + i, max_seqs=1)
+               for i in range(args.steps)]
+    times = [t for _, _, t in res]
+    total_bytes = sum(g * t for g, _, t in res)
     value = total_bytes / sum(times)
+    per_step = cores
     line = {
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "impl": "reference",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, {"sample": f"{per_step} sequences per step"}),
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step} whole sequences of the {w.name} workload per step "
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} whole sequences of the {w.name} workload per step, "
+                                   f"{how} "
                                    "(quantize-append of the step token + decode, all heads)"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -595,12 +645,22 @@ def main():
                              3)[0]
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
-        gbs, n, t = time_oracle(w, budget_s=12.0)
-        cpu = {"value": round(gbs, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} whole-sequence steps, cycling over the {w.num_seqs} sequences of "
-                         f"the {w.name} workload "
-                         f"(quantize-append of the step token + decode of all heads), "
-                         f"{t:.1f} s single-thread FP64"}
+        gbs1, n1, t1 = time_oracle(w, budget_s=6.0)
+        single = f"{n1} whole-sequence steps, {t1:.1f} s on one core"
+        cores = host_cores()
+        try:
+            gbs, n, t = time_oracle_parallel(w, 6.0, cores)[0]
+            cpu = {"value": round(gbs, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                   "sample": f"{n} whole-sequence steps over {t:.1f} s of wall time on {cores} "
+                             f"host cores (spawned processes, disjoint sequences), cycling over "
+                             f"the {w.num_seqs} sequences of the {w.name} workload "
+                             f"(quantize-append of the step token + decode of all heads), FP64",
+                   "single_thread_value": round(gbs1, 6), "single_thread_sample": single}
+        except Exception as e:  # the process pool is unavailable: the one-core figure
+            cpu = {"value": round(gbs1, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{single} of the {w.name} workload (quantize-append of the step "
+                             f"token + decode of all heads), FP64; process pool failed: "
+                             f"{type(e).__name__}"}
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()
