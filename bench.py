@@ -225,6 +225,29 @@ def time_oracle_parallel(w: W.Workload, budget_s: float, workers: int, rounds: i
     return out
 
 
+def cpu_baseline(w: W.Workload, budget_s: float = 6.0) -> dict:
+    """The bench line's `cpu_baseline`: the oracle as it stands on a bounded
+    sample of workload `w`, on every host core (spawned processes, disjoint
+    sequences, about budget_s each), with the single-thread figure beside it;
+    the one-core figure, labelled, if the process pool cannot run."""
+    gbs1, n1, t1 = time_oracle(w, budget_s=budget_s)
+    single = f"{n1} whole-sequence steps, {t1:.1f} s on one core"
+    cores = host_cores()
+    try:
+        gbs, n, t = time_oracle_parallel(w, budget_s, cores)[0]
+        return {"value": round(gbs, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": f"{n} whole-sequence steps over {t:.1f} s of wall time on {cores} "
+                          f"host cores (spawned processes, disjoint sequences), cycling over "
+                          f"the {w.num_seqs} sequences of the {w.name} workload "
+                          f"(quantize-append of the step token + decode of all heads), FP64",
+                "single_thread_value": round(gbs1, 6), "single_thread_sample": single}
+    except Exception as e:  # the process pool is unavailable: the one-core figure
+        return {"value": round(gbs1, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{single} of the {w.name} workload (quantize-append of the step "
+                          f"token + decode of all heads), FP64; process pool failed: "
+                          f"{type(e).__name__}"}
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -645,22 +668,7 @@ def main():
                              3)[0]
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
-        gbs1, n1, t1 = time_oracle(w, budget_s=6.0)
-        single = f"{n1} whole-sequence steps, {t1:.1f} s on one core"
-        cores = host_cores()
-        try:
-            gbs, n, t = time_oracle_parallel(w, 6.0, cores)[0]
-            cpu = {"value": round(gbs, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                   "sample": f"{n} whole-sequence steps over {t:.1f} s of wall time on {cores} "
-                             f"host cores (spawned processes, disjoint sequences), cycling over "
-                             f"the {w.num_seqs} sequences of the {w.name} workload "
-                             f"(quantize-append of the step token + decode of all heads), FP64",
-                   "single_thread_value": round(gbs1, 6), "single_thread_sample": single}
-        except Exception as e:  # the process pool is unavailable: the one-core figure
-            cpu = {"value": round(gbs1, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{single} of the {w.name} workload (quantize-append of the step "
-                             f"token + decode of all heads), FP64; process pool failed: "
-                             f"{type(e).__name__}"}
+        cpu = cpu_baseline(w, budget_s=6.0)
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()

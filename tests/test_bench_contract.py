@@ -56,3 +56,12 @@ def test_reference_arm_other_ranks_are_silent():
                env={"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_cpu_baseline_entry_runs_on_all_host_cores():
+    import bench
+    w = W.make("tiny")
+    cb = bench.cpu_baseline(w, budget_s=0.5)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0
+    assert cb["cores"] == bench.host_cores()
+    assert cb["single_thread_value"] > 0 and "host cores" in cb["sample"]
