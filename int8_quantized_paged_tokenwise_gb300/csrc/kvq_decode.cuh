@@ -503,6 +503,14 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
 #pragma unroll
     for (int i = 0; i < NOUT; ++i) o[i] = 0.f;
     const bool has_head = g < G;   // this lane provides a real query column
+    // BF16 queries enter the FP16 MMAs as q * 2^-sh per head (exact: the
+    // head's largest |q| lands in [2^14, 2^15)); qs0/qs1 = 2^sh of the heads
+    // 2c, 2c+1 of this thread's score columns multiply their scores.
+    float qs0 = 1.f, qs1 = 1.f;
+    // Tokenwise V scales go onto P: P' = p * s_v * 2^(15 - vfb), vfb the FP16
+    // biased exponent of the largest V scale of the piece so far (so P' < 2);
+    // O accumulates in units of 2^(vfb - 15) and is rescaled when vfb grows.
+    int vfb = 0;
 
     for (int pg = 0; pg < it_npg; ++pg) {
       const int s = cs_slot;
@@ -518,9 +526,30 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
       if (pg == 0) {
         // query fragments (the MMA B operand, column g = head g < G), from the
         // raw rows to this lane's slots of the fragment buffer
+        const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + lay.q) +
+                             (size_t)warp * (lay.q_bytes / 2) + g * D;
+        float qinv = 1.f;            // 2^-sh of head g (BF16 queries)
+        if constexpr (INT8 && QBF16) {
+          // the head's largest |q| over its four lanes' elements
+          uint32_t mx = 0;
+          if (has_head) {
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+              const uint2 v = *reinterpret_cast<const uint2*>(qs + 16 * ks + 4 * c);
+              mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
+            }
+          }
+          mx = max(mx & 0xFFFFu, mx >> 16);
+          mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+          mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+          const int sh = bf16_fp16_shift(mx);
+          qinv = exp2i(-sh);
+          // padded heads mirror the real head whose fragment they read
+          const float qsg = __shfl_sync(0xFFFFFFFFu, exp2i(sh), lane % (4 * G));
+          qs0 = __shfl_sync(0xFFFFFFFFu, qsg, 8 * c);
+          qs1 = __shfl_sync(0xFFFFFFFFu, qsg, 8 * c + 4);
+        }
         if (has_head) {
-          const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + lay.q) +
-                               (size_t)warp * (lay.q_bytes / 2) + g * D;
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             uint2 f;
@@ -528,10 +557,10 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
               // logical k {2c,2c+1,2c+8,2c+9} of step ks <-> head-dim 16ks+4c+{0..3}
               const uint2 v = *reinterpret_cast<const uint2*>(qs + 16 * ks + 4 * c);
               if constexpr (QBF16) {
-                f.x = h2_as_u32(__floats2half2_rn(__uint_as_float(v.x << 16),
-                                                  __uint_as_float(v.x & 0xFFFF0000u)));
-                f.y = h2_as_u32(__floats2half2_rn(__uint_as_float(v.y << 16),
-                                                  __uint_as_float(v.y & 0xFFFF0000u)));
+                f.x = h2_as_u32(__floats2half2_rn(__uint_as_float(v.x << 16) * qinv,
+                                                  __uint_as_float(v.x & 0xFFFF0000u) * qinv));
+                f.y = h2_as_u32(__floats2half2_rn(__uint_as_float(v.y << 16) * qinv,
+                                                  __uint_as_float(v.y & 0xFFFF0000u) * qinv));
               } else {
                 f = v;
               }
@@ -605,44 +634,84 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
         }
 
         // ---------- online softmax per head column (reduce over the 8 g-lanes) ----------
+        // true scores are z * qs (BF16 queries); the factor enters the max
+        // once and each exponent through an FMA
         float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
         }
+        if constexpr (INT8 && QBF16) {
+          mx0 *= qs0;
+          mx1 *= qs1;
+        }
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-        const float p0 = fast_exp2(z0 - mn0), p1 = fast_exp2(z1 - mn1);
-        const float p2 = fast_exp2(z2 - mn0), p3 = fast_exp2(z3 - mn1);
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
+        // tokenwise V scales: the page's largest V scale (valid tokens) moves
+        // the O unit up when it exceeds the running one; lg = 15 - vfb
+        // shifts the exponents so that p' = p * 2^lg, and P' = p' * s_v < 2
+        float ra = 1.f;     // O's unit change (power of two)
+        int lg = 0;
+        float sv_g = 1.f, sv_g8 = 1.f;
+        if constexpr (INT8 && !STATIC) {
+          const uint16_t* vsc = scales_w + s * (C::kScaleBytes / 2) + kBlockSize;
+          const uint32_t vmax = redux_max_u32((lane & 15) < nvalid ? (uint32_t)vsc[lane & 15] : 0u);
+          const int eb = max((int)(vmax >> 10), 1);
+          if (eb > vfb) {
+            if (pg > 0) ra = exp2i(vfb - eb);   // the first page starts from O = 0
+            vfb = eb;
+          }
+          lg = 15 - vfb;
+          sv_g = g < nvalid ? __half2float(__ushort_as_half(vsc[g])) : 0.f;
+          sv_g8 = g + 8 < nvalid ? __half2float(__ushort_as_half(vsc[g + 8])) : 0.f;
+        }
+        const float o0 = (float)lg - mn0, o1 = (float)lg - mn1;
+        float p0, p1, p2, p3;
+        if constexpr (INT8 && QBF16) {
+          p0 = fast_exp2(fmaf(z0, qs0, o0));
+          p1 = fast_exp2(fmaf(z1, qs1, o1));
+          p2 = fast_exp2(fmaf(z2, qs0, o0));
+          p3 = fast_exp2(fmaf(z3, qs1, o1));
+        } else {
+          p0 = fast_exp2(z0 + o0);
+          p1 = fast_exp2(z1 + o1);
+          p2 = fast_exp2(z2 + o0);
+          p3 = fast_exp2(z3 + o1);
+        }
+        if constexpr (INT8 && !STATIC) {
+          const float ul = exp2i(-lg);
+          l0 = fmaf(p0 + p2, ul, l0 * al0);
+          l1 = fmaf(p1 + p3, ul, l1 * al1);
+          p0 *= sv_g;
+          p1 *= sv_g;
+          p2 *= sv_g8;
+          p3 *= sv_g8;
+        } else {
+          l0 = l0 * al0 + (p0 + p2);
+          l1 = l1 * al1 + (p1 + p3);
+        }
         m0 = mn0;
         m1 = mn1;
-        if (__any_sync(0xFFFFFFFFu, (al0 != 1.f) || (al1 != 1.f))) {
+        const float ra0 = al0 * ra, ra1 = al1 * ra;
+        if (__any_sync(0xFFFFFFFFu, (ra0 != 1.f) || (ra1 != 1.f))) {
 #pragma unroll
           for (int cb = 0; cb < D / 16; ++cb) {
-            o[4 * cb + 0] *= al0;
-            o[4 * cb + 1] *= al1;
-            o[4 * cb + 2] *= al0;
-            o[4 * cb + 3] *= al1;
+            o[4 * cb + 0] *= ra0;
+            o[4 * cb + 1] *= ra1;
+            o[4 * cb + 2] *= ra0;
+            o[4 * cb + 3] *= ra1;
           }
         }
 
-        // P^T as the B operand: b0 = P[tokens 2c, 2c+1][head g], b1 = tokens 2c+8, 2c+9
+        // P'^T as the B operand: b0 = P'[tokens 2c, 2c+1][head g], b1 = tokens 2c+8, 2c+9
         const uint32_t pb0 = movmatrix_trans(pack2<MMA_BF16>(p0, p1));
         const uint32_t pb1 = movmatrix_trans(pack2<MMA_BF16>(p2, p3));
 
         // ---------- O^T[d][head] += V^T P^T: M = 16 head-dims, N = 8 heads ----------
         if constexpr (INT8) {
-          // per-token V scales multiply the converted pairs; a static V scale
-          // is applied once to the output instead
-          __half2 vs01 = __float2half2_rn(1.f), vs89 = vs01;
-          if constexpr (!STATIC) {
-            const uint16_t* vsc = scales_w + s * (C::kScaleBytes / 2) + kBlockSize;
-            vs01 = u32_as_h2(reinterpret_cast<const uint32_t*>(vsc)[c]);
-            vs89 = u32_as_h2(reinterpret_cast<const uint32_t*>(vsc)[4 + c]);
-          }
+          // exact codes; the V scales are in P' (tokenwise) or applied once
+          // to the output (static)
 #pragma unroll
           for (int kk = 0; kk < KSTEPS / 2; ++kk) {
             uint32_t r[4];
@@ -654,12 +723,6 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
               uint32_t ev0, od0, ev1, od1;
               i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h], ev0, od0);
               i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h + 1], ev1, od1);
-              if constexpr (!STATIC) {
-                ev0 = h2_as_u32(__hmul2(u32_as_h2(ev0), vs01));
-                od0 = h2_as_u32(__hmul2(u32_as_h2(od0), vs01));
-                ev1 = h2_as_u32(__hmul2(u32_as_h2(ev1), vs89));
-                od1 = h2_as_u32(__hmul2(u32_as_h2(od1), vs89));
-              }
               const int cb = 2 * kk + h;
               float* oq = o + 4 * cb;
               mma_16816_acc<false>(*reinterpret_cast<float(*)[4]>(oq), ev0, od0, ev1, od1, pb0, pb1);
@@ -697,7 +760,9 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
       if (head >= G) continue;
       const float l = hh ? l1 : l0;
       const float m = hh ? m1 : m0;
-      const float inv = l > 0.f ? (STATIC ? p.v_static : 1.f) / l : 0.f;
+      // O's unit: the static V scale, or 2^(vfb - 15) (tokenwise), or 1 (twin)
+      const float unit = STATIC ? p.v_static : (INT8 ? exp2i(vfb - 15) : 1.f);
+      const float inv = l > 0.f ? unit / l : 0.f;
       const int64_t hrow = (int64_t)it.b * p.Hq + (int64_t)it.j * G + head;
       if (it.flags & 1) {
         uint16_t* dst = static_cast<uint16_t*>(p.out) + hrow * D;

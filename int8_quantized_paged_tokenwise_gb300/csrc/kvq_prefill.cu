@@ -73,13 +73,17 @@ struct TcLayout {
   static constexpr int kRaw = kVc + kTcConv * kConvBytes;          // kTcRaw stages
   static constexpr int kRawSc = kRaw + kTcRaw * kRawBytes;         // per page: K 32 B, V 32 B
   static constexpr int kColSc = kRawSc + kTcRaw * kTcPages * 64;   // per buffer: K 64, V 64 floats
-  static constexpr int kBars = kColSc + kTcConv * 2 * kTcKv * 4;
+  static constexpr int kVmax = kColSc + kTcConv * 2 * kTcKv * 4;  // per buffer: 2 floats
+  static constexpr int kQsh = kVmax + kTcConv * 2 * 4;             // per half and row: shift
+  static constexpr int kBars = kQsh + kTcHalves * kTcRows * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;     // TMEM base, abort flag
   static constexpr size_t kTotal = (size_t)kMisc + 16 + 1024;      // + base alignment slack
 };
 
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v) {
-  return h2_as_u32(__floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)));
+// Two BF16 values times a power of two `f`, as an FP16 pair.
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v, float f) {
+  return h2_as_u32(
+      __floats2half2_rn(__uint_as_float(v << 16) * f, __uint_as_float(v & 0xFFFF0000u) * f));
 }
 
 // 16 INT8 codes (chunk c of token row t of a page tile) -> FP16 chunks 2c,
@@ -154,6 +158,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == kWarpMma) tc_alloc(smem_u32(&misc[0]), kTcCols);
 
   // ---- Q tiles: row r of half h = (query i_begin + h TH + r / G, head j G + r % G), FP16 ----
+  // BF16 rows enter as q * 2^-sh (exact: the row's largest |q| lands in
+  // [2^14, 2^15)); the row's softmax multiplies its scores by 2^sh.  The D/8
+  // chunks of a row are handled by D/8 consecutive lanes of one warp (the
+  // loop's stride is a multiple of 32, so a warp runs an iteration whole).
+  int* qsh = reinterpret_cast<int*>(smem + Ly::kQsh);
   for (int e = tid; e < kTcHalves * kTcRows * (D / 8); e += kTcThreads) {
     const int hr = e / (D / 8), c8 = e - hr * (D / 8);  // 16-byte chunk c8 of row hr
     const int h = hr / kTcRows, r = hr - h * kTcRows;
@@ -163,12 +172,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint16_t* src = static_cast<const uint16_t*>(p.q) +
                             ((int64_t)(q0 + i) * p.Hq + (int64_t)j * G + r % G) * D + 8 * c8;
       v = __ldg(reinterpret_cast<const uint4*>(src));
-      if constexpr (BF16) {
-        v.x = bf2_to_h2(v.x);
-        v.y = bf2_to_h2(v.y);
-        v.z = bf2_to_h2(v.z);
-        v.w = bf2_to_h2(v.w);
-      }
+    }
+    if constexpr (BF16) {
+      uint32_t mx = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                             __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+      mx = max(mx & 0xFFFFu, mx >> 16);
+#pragma unroll
+      for (int o = 1; o < D / 8; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      const int sh = bf16_fp16_shift(mx);
+      if (c8 == 0) qsh[hr] = sh;
+      const float inv = exp2i(-sh);
+      v.x = bf2_to_h2(v.x, inv);
+      v.y = bf2_to_h2(v.y, inv);
+      v.z = bf2_to_h2(v.z, inv);
+      v.w = bf2_to_h2(v.w, inv);
+    } else if (c8 == 0) {
+      qsh[hr] = 0;
     }
     *reinterpret_cast<uint4*>(smem + Ly::kQ + h * Ly::kQBytes + (c8 >> 3) * (kTcRows * 128) +
                               r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) = v;
@@ -279,6 +298,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int t = ct & (kTcKv - 1), kind = ct >> 6;
         const float sv = __half2float(__ushort_as_half(rs[(t >> 4) * 32 + kind * 16 + (t & 15)]));
         cs[kind * kTcKv + t] = kind == 0 ? sv * p.scale_log2 : sv;
+        if (kind == 1) {
+          // the largest V scale of the tile's tokens that were copied and
+          // belong to the sequence (other slots may hold anything): one per
+          // V warp
+          const int tg = it * kTcKv + t;
+          const uint32_t vm =
+              redux_max_u32(tg < L && tg < npages * kBlockSize ? __float_as_uint(sv) : 0u);
+          if (lane == 0)
+            reinterpret_cast<float*>(smem + Ly::kVmax)[2 * cb + (warp - kWarpCvt - 2)] =
+                __uint_as_float(vm);
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -347,6 +377,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
     const int nh = n_half[h];
     float m_use = -INFINITY, l = 0.f;
+    // the row's scores are (S * K scale) * qf (BF16 queries entered as q / qf)
+    const float qf = exp2i(qsh[h * kTcRows + r]);
+    // V scales go onto P: P' = P s_v 2^(127 - vfb) with vfb the FP32 biased
+    // exponent of the largest V scale so far (all rows see the same tokens,
+    // so it moves for all rows at once); O accumulates in units of
+    // 2^(vfb - 127) and is rescaled when vfb grows
+    int vfb = 0;
     bool good = true;
     for (int it = 0; it < nh; ++it) {
       const int cb = it % kTcConv;
@@ -390,7 +427,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int w = kTcKv / 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int t = 0; t < w; ++t) mr[t] = fmaxf(mr[t], mr[t + w]);
-        mx = mr[0];
+        mx = mr[0] * qf;
       }
       const bool grow = mx > m_use + 8.f;
       const float m_new = grow ? mx : m_use;
@@ -398,10 +435,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float alpha = resc ? fast_exp2(m_use - m_new) : 1.f;
       m_use = m_new;
       const float ref = m_use == -INFINITY ? 0.f : m_use;
-      // P = 2^(z - m): the row sum takes P, the P V operand P' = P s_v (0 for
-      // tokens past the row, whose scale slots may hold anything)
+      float fs = 1.f;                             // O's unit change
+      {
+        const float* vm = reinterpret_cast<const float*>(smem + Ly::kVmax) + 2 * cb;
+        const int eb = (int)(max(__float_as_uint(vm[0]), __float_as_uint(vm[1])) >> 23);
+        if (eb > vfb) {
+          if (it > 0) fs = exp2i(vfb - eb);       // the first tile starts from O = 0
+          vfb = eb;
+        }
+      }
+      const int lg = 127 - vfb;
+      // P = 2^(z qf - m) scaled by 2^lg: the row sum takes P, the P V operand
+      // P' = P 2^lg s_v (0 for tokens past the row, whose scale slots may
+      // hold anything)
+      const float off = (float)lg - ref;
 #pragma unroll
-      for (int t = 0; t < kTcKv; ++t) z[t] = fast_exp2(z[t] - ref);
+      for (int t = 0; t < kTcKv; ++t) z[t] = fast_exp2(fmaf(z[t], qf, off));
       float lsum;
       {
         float sr2[kTcKv / 2];
@@ -413,7 +462,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int t = 0; t < w; ++t) sr2[t] += sr2[t + w];
         lsum = sr2[0];
       }
-      l = l * alpha + lsum;
+      l = fmaf(lsum, exp2i(-lg), l * alpha);
       uint32_t pk[kTcKv / 2];                     // P' packed two FP16 per TMEM column
 #pragma unroll
       for (int cc = 0; cc < kTcKv / 8; ++cc) {
@@ -431,15 +480,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           pk[4 * cc + e2] = h2_as_u32(__floats2half2_rn(a8[2 * e2], a8[2 * e2 + 1]));
       }
       tc_st32(tP(h) + lanes, pk);
-      if (__any_sync(0xFFFFFFFFu, resc)) {
+      if (__any_sync(0xFFFFFFFFu, resc) || fs != 1.f) {
         // O holds P V of tiles 0..it-1 (complete: S of this tile was
-        // committed after them): rescale the rows whose maximum moved
+        // committed after them): rescale the rows whose maximum moved, and
+        // every row when the unit moved
+        const float ra = alpha * fs;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
           tc_ld32(tO(h) + c0 + lanes, o);
 #pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * ra);
           tc_st32(tO(h) + c0 + lanes, o);
         }
       }
@@ -457,7 +508,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (nh > 0) {
       // ---- epilogue: O / l, rounded to the activation dtype ----
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? exp2i(vfb - 127) / l : 0.f;
       uint16_t* dst = static_cast<uint16_t*>(p.out) +
                       ((int64_t)(q0 + (pos >= 0 ? iq : 0)) * p.Hq + (int64_t)j * G + r % G) * D;
 #pragma unroll

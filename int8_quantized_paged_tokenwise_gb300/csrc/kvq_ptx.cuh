@@ -213,7 +213,28 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
+// Largest of the 32 lanes' values (every lane gets it).
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t x) {
+  uint32_t y;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // ------------------------------------------------------------ numerics ---
+// 2^e as a float, for e in [-126, 127] (exact; built from the exponent field).
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// Power-of-two exponent that brings a set of BF16 values into FP16's normal
+// range without loss: given the largest magnitude's bit pattern (sign
+// cleared), the shift sh such that that magnitude times 2^-sh lies in
+// [2^14, 2^15); sh is kept in [-126, 113] so that 2^sh and 2^-sh are normal
+// floats.  A zero (or subnormal) maximum gives -126.
+__device__ __forceinline__ int bf16_fp16_shift(uint32_t max_bits) {
+  const int eb = (int)(max_bits >> 7);          // biased BF16 exponent, 0..255
+  const int sh = eb - 127 - 14;
+  return sh < -126 ? -126 : (sh > 113 ? 113 : sh);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -8,6 +8,15 @@
 - bf16 -> FP16 for the queries: every bf16 value whose magnitude lies in
   FP16's normal range [2^-14, 65504] is representable in FP16 (8 significant
   bits into 11), so the rounding to FP16 is exact there.
+- Outside FP16's normal range the BF16 queries are first multiplied by a
+  power of two 2^-sh chosen from the largest magnitude of the row (or head):
+  it lands in [2^14, 2^15), so nothing overflows, and every element within
+  2^-28 of that magnitude is still exact in FP16.
+- The tokenwise V scales multiply the softmax weights, not the codes:
+  P' = p * s_v * 2^-E with E the exponent of the largest scale seen (FP16
+  biased exponent in the decode, FP32 in the prefill) stays below 2 (times
+  the prefill's 2^8 lazy-rescale slack), far inside FP16, for every FP16
+  scale, where code * s_v itself can exceed 65504.
 - The static-scale decode folds the K scale into the score scale and the V
   scale into the output; the tokenwise one multiplies the scale after the
   integer dot product: both are re-associations of the same product, checked
@@ -51,3 +60,46 @@ def test_scale_folding_is_a_reassociation():
     direct = sm * (q[None, :] * (s[:, None] * codes)).sum(1)     # dequantize, then dot
     folded = (sm * s) * (codes @ q)                               # integer dot, then scale
     assert np.allclose(direct, folded, rtol=1e-13, atol=0)
+
+
+def _bf16_fp16_shift(max_bits: np.ndarray) -> np.ndarray:
+    """The kernels' shift: biased BF16 exponent - 127 - 14, kept in [-126, 113]."""
+    return np.clip((max_bits >> 7).astype(np.int64) - 141, -126, 113)
+
+
+def test_bf16_query_shift_maps_the_maximum_into_fp16_and_keeps_near_elements_exact():
+    bits = np.arange(1, 0x7F80, dtype=np.uint32)                  # positive finite BF16
+    x = (bits << 16).view(np.float32).astype(np.float64)
+    sh = _bf16_fp16_shift(bits)
+    y = x * 2.0 ** (-sh)
+    unclamped = (bits >> 7).astype(np.int64) - 141 >= -126          # normal maxima
+    assert np.all((y[unclamped] >= 2.0 ** 14) & (y[unclamped] < 2.0 ** 15))
+    assert np.all(y <= 65504.0)                                     # never overflows FP16
+    # every element of the row is exact in FP16 unless it is below 2^-14 after
+    # the shift, i.e. 2^28 times smaller than the row's maximum
+    for m in (0x3F80, 0x4780, 0x4B7D, 0x3380, 0x7F7F, 0x0080):      # 1, 65536, ~1.7e7, ...
+        shm = int(_bf16_fp16_shift(np.array([m], np.uint32))[0])
+        xs = x[bits <= m] * 2.0 ** (-shm)
+        ok = xs >= 2.0 ** -14
+        assert np.array_equal(xs[ok].astype(np.float16).astype(np.float64), xs[ok])
+        assert np.all(x[bits <= m][~ok] < x[bits == m][0] * 2.0 ** -27)
+
+
+def test_v_scale_on_p_stays_inside_fp16():
+    s_bits = np.arange(1, 0x7C00, dtype=np.uint16)                  # every positive FP16 scale
+    s = s_bits.view(np.float16).astype(np.float64)
+    assert s.max() == 65504.0
+    # decode: E = max(FP16 biased exponent, 1); p <= 1
+    e16 = np.maximum(s_bits >> 10, 1).astype(np.int64)
+    r16 = s * 2.0 ** (15 - e16)
+    assert np.all((r16 < 2.0)) and np.all(r16[s_bits >= 0x0400] >= 1.0)
+    # the running maximum only grows, so every earlier scale is below it too
+    # prefill: E = FP32 biased exponent of the scale; p <= 2^8 between rescales
+    e32 = (s.astype(np.float32).view(np.uint32) >> 23).astype(np.int64)
+    r32 = s * 2.0 ** (127 - e32)
+    assert np.all((r32 >= 1.0) & (r32 < 2.0))
+    assert 2.0 ** 8 * r32.max() < 65504.0
+    # where the old formulation overflowed: 127 * s rounded to FP16
+    with np.errstate(over="ignore"):
+        big = (127.0 * s).astype(np.float16)
+    assert np.isinf(big).sum() > 0 and not np.isinf(r16.astype(np.float16)).any()

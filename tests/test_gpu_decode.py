@@ -33,11 +33,12 @@ def _check_all(case, out, quantized=True, what=""):
     return max(errs) if errs else 0.0
 
 
-def _check_sampled(case, out, n_pairs, seed=0, quantized=True, what=""):
+def _check_sampled(case, out, n_pairs, seed=0, quantized=True, what="", seqs=None):
     w = case.w
     ob = out_bits(out)
     r = np.random.default_rng(seed)
-    bs = r.choice(w.num_seqs, size=min(n_pairs, w.num_seqs), replace=False)
+    bs = seqs if seqs is not None else r.choice(w.num_seqs, size=min(n_pairs, w.num_seqs),
+                                                replace=False)
     for b in bs:
         heads = sorted(r.choice(w.num_q_heads, size=min(4, w.num_q_heads), replace=False))
         ref = _oracle_seq(w, int(b), quantized, heads=heads)
@@ -79,6 +80,12 @@ def test_decode_full_workload_sampled(name):
     out = case.decode()
     _check_sampled(case, out, 6, seed=1, what=name)
     _check_sampled(case, case.decode(kv16=True), 3, seed=2, quantized=False, what=name + " kv16")
+    if name == "serving":
+        # the fragmented split-K extremes: the longest sequences (many ranges
+        # each) and the shortest (a piece of a single page)
+        order = np.argsort(w.context_lens, kind="stable")
+        _check_sampled(case, out, 0, seed=5, what="serving extremes",
+                       seqs=[int(b) for b in (*order[:3], *order[-3:])])
     assert bool(torch.isfinite(out.float()).all())
     assert kvq.kvq_get_error() == (0, 0)
 
