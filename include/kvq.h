@@ -364,12 +364,17 @@ kvq_status kvq_trim_front_keep_sink(int8_t* k_cache, int8_t* v_cache, uint16_t* 
  *
  * Same arguments and result as kvq_paged_decode, minus the workspace: the
  * split-K scratch is a static device array of KVQ_NOALLOC_SCRATCH_BYTES built
- * into the library (held on every GPU that loads it, until exit).  Returns
- * KVQ_ERR_WORKSPACE_TOO_SMALL when kvq_decode_workspace_bytes(...) for these
- * sizes exceeds that limit.  Allocates nothing.  The first call on a device
- * looks up the array's device address (make that first call before any
- * stream capture).  All calls on a device share the array: calls that
- * overlap on the GPU race.  Nothing in it needs clearing between calls.
+ * into the library (held on every GPU that loads it, until exit), passed to
+ * kvq_paged_decode as its workspace.  Where kvq_decode_workspace_bytes(...)
+ * recommends more, the launcher uses fewer, longer work ranges (or one range
+ * per sequence), with the same results; KVQ_ERR_WORKSPACE_TOO_SMALL is
+ * returned only when not even one range per KV head fits (about
+ * 16 MiB / (8 G (D + 1)) KV heads).  Allocates nothing.  The first call on a
+ * device looks up the array's device address (make that first call before
+ * any stream capture); the address is not valid across cudaDeviceReset, after
+ * which this call must not be used in the process.  All calls on a device
+ * share the array: calls that overlap on the GPU race.  Nothing in it needs
+ * clearing between calls.
  */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -15,11 +15,20 @@
 // code cannot use the array's name as a device address, so its address is
 // looked up with cudaGetSymbolAddress once per device, on the first call made
 // while that device is current (make that first call before any stream
-// capture).  All calls on a device share the one array: calls that overlap on
-// the GPU (different streams, no ordering between them) race on it.  The
-// split-K partials it holds are fully written before they are read, so
-// nothing in it needs clearing between calls; it keeps the last call's
-// contents.
+// capture).  That address belongs to the device's context: after
+// cudaDeviceReset (or anything else that destroys and recreates the primary
+// context) this entry point must not be called again in the process.  All
+// calls on a device share the one array: calls that overlap on the GPU
+// (different streams, no ordering between them) race on it.  The split-K
+// partials it holds are fully written before they are read, so nothing in it
+// needs clearing between calls; it keeps the last call's contents.
+//
+// The array is handed to kvq_paged_decode as a workspace of exactly
+// KVQ_NOALLOC_SCRATCH_BYTES.  That launcher fits its split-K work ranges into
+// whatever workspace it is given (fewer, longer ranges when it is smaller
+// than kvq_decode_workspace_bytes recommends, or one range per sequence), so
+// only shapes for which not even one range per KV head fits are refused, with
+// KVQ_ERR_WORKSPACE_TOO_SMALL.
 #include <mutex>
 
 #include "kvq.h"
@@ -57,11 +66,9 @@ kvq_status kvq_paged_decode_noalloc(const void* q, kvq_dtype dtype, int32_t num_
                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
                                     const int32_t* context_lens, int32_t max_context_len,
                                     float sm_scale, void* out, kvq_stream_t stream) {
+  // checks that need no device, so that they answer without one
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0)
     return KVQ_ERR_INVALID_ARGUMENT;
-  const size_t need = kvq_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                                 max_context_len);
-  if (need > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = scratch_address();
   if (scratch == nullptr) return KVQ_ERR_CUDA;
   return kvq_paged_decode(q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,

@@ -71,6 +71,16 @@ def test_decode_host_validation(kw, status):
     assert kvq.load().kvq_paged_decode(*_decode_args(**kw)) == status
 
 
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(Hq=0), dict(Hkv=0), dict(Hq=-8),
+                                dict(mc=-1)])
+def test_noalloc_rejects_before_any_device_work(kw):
+    """kvq_paged_decode_noalloc answers these without looking the scratch up
+    (so without a device)."""
+    args = _decode_args(**kw)
+    del args[18:20]                        # no workspace arguments
+    assert kvq.load().kvq_paged_decode_noalloc(*args) == INVALID
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(T=0), OK),
     (dict(bs=8), UNSUPPORTED),
