@@ -1,21 +1,26 @@
 #!/usr/bin/env python3
 """Benchmark of the INT8 paged KV-cache hot path on GB300.
 
-One step = one layer's decode step of the canonical GQA workload (32
-sequences, contexts U[512, 2048] + 1 appended token, 32 query / 8 KV heads,
-d 128, bf16, block 16, shuffled block pool):
+One step = one layer's decode step of a workload: quantize-append of the
+step's new tokens (if the workload appends), then the paged decode:
 
-    kvq_quantize_append (1 new token per sequence)  ->  kvq_paged_decode
+    kvq_quantize_append  ->  kvq_paged_decode
 
-The same step is timed on the native-BF16 twin (kvq_cache_append_kv16 ->
+The headline line is taken on the largest workload that fits one GPU, the MHA
+decode (64 sequences x 4096 tokens, 32 query = 32 KV heads, d 128, fp16,
+2.18 GB of INT8 K/V per step); ``--workload`` picks another.  The same step is
+timed on the native-16-bit twin (kvq_cache_append_kv16 ->
 kvq_paged_decode_kv16) for the steps/s A/B, and through the C ABI with host
 buffers (pinned H2D of the step's inputs and D2H of the output inside the
-timed region) for the end-to-end figure.  L2 is flushed (512 MB write)
-between timed steps; each step is timed with CUDA events on the launching
-stream.  A context sweep (2K/8K/32K, 16 sequences) compares the INT8 decode
-with the BF16 twin, and the chunked prefill over the INT8 cache is timed on
-an 8K-token causal chunk (GQA 8).  The FP64 CPU oracle is timed on a bounded
-sample of the same workload as the CPU baseline.
+timed region) for the end-to-end figure.  ``configs`` repeats the INT8 and
+twin timings on all five workloads (tiny, canonical, long, mha, serving).
+L2 is flushed (512 MB write) between timed steps; each step is timed with
+CUDA events on the launching stream.  A context sweep (2K/8K/32K, 16
+sequences) compares the INT8 decode with the twin, and the chunked prefill
+over the INT8 cache is timed on an 8K-token causal chunk (GQA 8).  The FP64
+CPU oracle is timed on a bounded sample of the headline workload as the CPU
+baseline.  K/V values are drawn on the GPU (``Workload.seq_kv_device``: the
+workloads' recipe, torch's generator).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --prefill all|SHAPE [--steps K] [--warmup W]   # prefill lines only
@@ -47,9 +52,13 @@ METRIC = "INT8-KV paged decode HBM GB/s (% of GB300 peak); decode steps/s vs BF1
 UNIT = "GB/s"
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
-# the kernels whose DRAM traffic the committed ncu summary measured
+# the kernels whose DRAM traffic the committed ncu summaries measured
 DECODE_SOURCES = ("kvq_decode.cuh", "kvq_decode_int8.cu", "kvq_ptx.cuh", "kvq_combine.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_int8_canonical.traffic.txt")
+HEADLINE = "mha"
+
+
+def traffic_file(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"decode_int8_{workload}.traffic.txt")
 
 
 # chunked-prefill shapes: (sequences, context L, chunk n = queries at the end
@@ -69,7 +78,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="canonical", choices=list(W.NAMES))
+    ap.add_argument("--workload", default=HEADLINE, choices=list(W.NAMES))
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload timings of all five workloads")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--settle", type=float, default=1.5,
@@ -122,7 +133,7 @@ def read_traffic(workload: str):
     lines), or None when it was taken on other sources or another workload."""
     try:
         kv = {}
-        with open(TRAFFIC_FILE) as f:
+        with open(traffic_file(workload)) as f:
             for line in f:
                 line = line.strip()
                 if line and not line.startswith("#") and ":" in line:
@@ -155,34 +166,60 @@ def config_of(w: W.Workload, extra=None):
 
 
 # ------------------------------------------------------------- CPU oracle ---
-def time_oracle(w: W.Workload, budget_s: float, start_seq: int = 0, max_seqs: int | None = None,
-                stride: int = 1):
-    """The FP64 oracle as it stands, single thread: quantize-append of the
-    step's token + decode (it re-quantizes the context from the unpaged token
-    arrays) for whole sequences start_seq, start_seq + stride, ... until the
-    time budget is spent.  Returns (GB/s, sequences, busy seconds)."""
+def oracle_inputs(w: W.Workload, seqs):
+    """The oracle's inputs for whole sequences `seqs` (numpy draws of the
+    workload recipe), generated before any timing starts."""
+    return [(b, w.seq_q(b)) + tuple(w.seq_kv(b)) for b in seqs]
+
+
+def oracle_seq_bytes(w: W.Workload, L: int) -> int:
+    """Algorithmic bytes of one sequence's step: its decode (K/V payload and
+    scales of L tokens, table entries, q and out) plus, when the workload
+    appends, the quantize-append of its new token."""
+    n = w.decode_bytes_int8_seq(L)
+    if w.append:
+        n += w.num_kv_heads * (2 * 2 * w.head_dim + 2 * (w.head_dim + 2)) + 8
+    return n
+
+
+def oracle_run(w: W.Workload, inputs):
+    """The FP64 oracle as it stands, single thread, over prepared inputs: per
+    sequence the quantize-append of its step token (if the workload appends;
+    into a one-page cache) and the decode of all heads (which re-quantizes
+    the context from the unpaged token arrays).  Returns (bytes, seconds)."""
     import oracle
     oracle.build()
-    nb, bt, _ = w.tables()
-    bytes_done, t_total, n = 0, 0.0, 0
+    kc = np.zeros((1, w.num_kv_heads, 16, w.head_dim), np.int8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((1, w.num_kv_heads, 16), np.uint16)
+    vs = np.zeros_like(ks)
+    nbytes, t = 0, 0.0
+    for b, q, k, v in inputs:
+        L = len(k)
+        slot = np.array([(L - 1) % 16], np.int64)
+        t0 = time.perf_counter()
+        if w.append and L:
+            oracle.quantize_append(k[L - 1:], v[L - 1:], w.dtype, slot, kc, vc, ks, vs, 16)
+        oracle.decode_sequence(q, k, v, w.dtype, w.sm_scale)
+        t += time.perf_counter() - t0
+        nbytes += oracle_seq_bytes(w, L)
+    return nbytes, t
+
+
+def time_oracle(w: W.Workload, budget_s: float, start_seq: int = 0, max_seqs: int | None = None,
+                stride: int = 1):
+    """Single thread: whole sequences start_seq, start_seq + stride, ... until
+    the time budget is spent (each sequence's inputs drawn before its timed
+    call).  Returns (GB/s, sequences, busy seconds)."""
+    nbytes, t_total, n = 0, 0.0, 0
     b = start_seq
     while (max_seqs is None or n < max_seqs) and (t_total < budget_s or n == 0):
-        b = b % w.num_seqs
-        k, v = w.seq_kv(b)
-        q = w.seq_q(b)
-        L = len(k)
-        kc = np.zeros((nb, w.num_kv_heads, 16, w.head_dim), np.int8)
-        ks = np.zeros((nb, w.num_kv_heads, 16), np.uint16)
-        t0 = time.perf_counter()
-        oracle.quantize_append(k[L - 1:], v[L - 1:], w.dtype, w.slots(b, L - 1, L), kc, kc.copy(),
-                               ks, ks.copy(), 16)
-        oracle.decode_sequence(q, k, v, w.dtype, w.sm_scale)
-        t_total += time.perf_counter() - t0
-        bytes_done += L * w.num_kv_heads * (2 * w.head_dim + 4) + w.pages(L) * 4 + \
-            2 * w.num_q_heads * w.head_dim * 2
+        x, t = oracle_run(w, oracle_inputs(w, [b % w.num_seqs]))
+        nbytes += x
+        t_total += t
         n += 1
         b += stride
-    return bytes_done / t_total / 1e9, n, t_total
+    return nbytes / t_total / 1e9, n, t_total
 
 
 def host_cores() -> int:
@@ -193,34 +230,44 @@ def host_cores() -> int:
 
 
 def _oracle_job(job):
-    """Pool worker: the oracle on sequences start, start + stride, ... (bytes, n)."""
-    name, budget_s, start, stride, max_seqs = job
+    """Pool worker: draw the inputs of its sequences, wait for every worker at
+    the barrier, then run the oracle on them.  Returns (bytes, sequences,
+    start, end) with wall-clock start/end times."""
+    name, seqs, barrier = job
     w = W.make(name)
-    gbs, n, t = time_oracle(w, budget_s, start_seq=start, max_seqs=max_seqs, stride=stride)
-    return gbs * 1e9 * t, n
+    inputs = oracle_inputs(w, seqs)
+    import oracle
+    oracle.build()
+    barrier.wait(timeout=600)
+    t0 = time.time()
+    nbytes, _ = oracle_run(w, inputs)
+    return nbytes, len(seqs), t0, time.time()
 
 
-def time_oracle_parallel(w: W.Workload, budget_s: float, workers: int, rounds: int = 1,
+def time_oracle_parallel(w: W.Workload, seqs_per_worker: int, workers: int, rounds: int = 1,
                          warmup_rounds: int = 1):
-    """The same oracle calls on `workers` spawned host processes (one sequence
-    stream each, disjoint), `rounds` times: per round either one sequence per
-    worker (budget_s == 0) or about budget_s of work per worker.  Returns the
-    per-round (GB/s over the round's wall time, sequences, wall seconds)."""
+    """The same oracle calls on `workers` spawned host processes, disjoint
+    sequences, `rounds` times: each worker draws the inputs of its
+    `seqs_per_worker` sequences, all workers start together at a barrier, and
+    the round's time runs from the first start to the last finish.  Returns
+    per round (GB/s, sequences, wall seconds)."""
     import multiprocessing as mp
     ctx = mp.get_context("spawn")
-    per = 1 if budget_s <= 0 else None
     out = []
-    with ctx.Pool(workers) as pool:
-        jobs = lambda r: [(w.name, budget_s, r * workers + i, 1 if per else workers, per)  # noqa
-                          for i in range(workers)]
-        limit = 120.0 + 4 * max(budget_s, 1.0)          # seconds a round may take
+    with ctx.Manager() as mgr, ctx.Pool(workers) as pool:
+        bar = mgr.Barrier(workers)
+
+        def jobs(r, n):
+            first = r * workers * n
+            return [(w.name, [(first + i * n + j) % max(w.num_seqs, 1) for j in range(n)], bar)
+                    for i in range(workers)]
+        limit = 600.0 + 60.0 * seqs_per_worker          # seconds a round may take
         for r in range(warmup_rounds):                # imports and library load in each worker
-            warm = [(w.name, 0.0, r * workers + i, 1, 1) for i in range(workers)]
-            pool.map_async(_oracle_job, warm).get(timeout=limit)
+            pool.map_async(_oracle_job, jobs(r, 1)).get(timeout=limit)
         for r in range(rounds):
-            t0 = time.perf_counter()
-            res = pool.map_async(_oracle_job, jobs(warmup_rounds + r)).get(timeout=limit)
-            wall = time.perf_counter() - t0
+            res = pool.map_async(_oracle_job, jobs(warmup_rounds + r, seqs_per_worker)).get(
+                timeout=limit)
+            wall = max(x[3] for x in res) - min(x[2] for x in res)
             out.append((sum(x[0] for x in res) / wall / 1e9, sum(x[1] for x in res), wall))
     return out
 
@@ -228,24 +275,27 @@ def time_oracle_parallel(w: W.Workload, budget_s: float, workers: int, rounds: i
 def cpu_baseline(w: W.Workload, budget_s: float = 6.0) -> dict:
     """The bench line's `cpu_baseline`: the oracle as it stands on a bounded
     sample of workload `w`, on every host core (spawned processes, disjoint
-    sequences, about budget_s each), with the single-thread figure beside it;
-    the one-core figure, labelled, if the process pool cannot run."""
+    sequences, about budget_s of oracle time each, input draws outside the
+    timed region), with the single-thread figure beside it; the one-core
+    figure, labelled, if the process pool cannot run."""
     gbs1, n1, t1 = time_oracle(w, budget_s=budget_s)
     single = f"{n1} whole-sequence steps, {t1:.1f} s on one core"
     cores = host_cores()
+    per = max(1, int(round(budget_s / (t1 / n1))))
+    what = ("quantize-append of the step token + decode of all heads" if w.append
+            else "decode of all heads")
     try:
-        gbs, n, t = time_oracle_parallel(w, budget_s, cores)[0]
+        gbs, n, t = time_oracle_parallel(w, per, cores)[0]
         return {"value": round(gbs, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                "sample": f"{n} whole-sequence steps over {t:.1f} s of wall time on {cores} "
-                          f"host cores (spawned processes, disjoint sequences), cycling over "
-                          f"the {w.num_seqs} sequences of the {w.name} workload "
-                          f"(quantize-append of the step token + decode of all heads), FP64",
+                "sample": f"{n} whole-sequence steps ({per} per core) over {t:.1f} s of wall "
+                          f"time on {cores} host cores (spawned processes started together, "
+                          f"disjoint sequences, input draws before the start) of the "
+                          f"{w.name} workload ({what}), FP64",
                 "single_thread_value": round(gbs1, 6), "single_thread_sample": single}
     except Exception as e:  # the process pool is unavailable: the one-core figure
         return {"value": round(gbs1, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": f"{single} of the {w.name} workload (quantize-append of the step "
-                          f"token + decode of all heads), FP64; process pool failed: "
-                          f"{type(e).__name__}"}
+                "sample": f"{single} of the {w.name} workload ({what}), FP64; process pool "
+                          f"failed: {type(e).__name__}"}
 
 
 def run_reference(args):
@@ -254,10 +304,10 @@ def run_reference(args):
         return
     w = W.make(args.workload)
     cores = host_cores()
-    how = "one per host core in spawned processes"
+    how = "one per host core in spawned processes started together"
     try:
         # each step: one whole sequence per host core, all cores at once
-        res = time_oracle_parallel(w, 0.0, cores, rounds=args.steps,
+        res = time_oracle_parallel(w, 1, cores, rounds=args.steps,
                                    warmup_rounds=max(args.warmup, 1))
     except Exception as e:  # the process pool is unavailable: one core, labelled as such
         how = f"on one core (process pool failed: {type(e).__name__})"
@@ -269,17 +319,17 @@ def run_reference(args):
     times = [t for _, _, t in res]
     total_bytes = sum(g * t for g, _, t in res)
     value = total_bytes / sum(times)
-    per_step = cores
+    what = ("quantize-append of the step token + decode, all heads" if w.append
+            else "decode, all heads")
     line = {
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "impl": "reference",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, {"sample": f"{per_step} sequences per step"}),
+        "config": config_of(w, {"sample": f"{cores} sequences per step"}),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{per_step} whole sequences of the {w.name} workload per step, "
-                                   f"{how} "
-                                   "(quantize-append of the step token + decode, all heads)"},
+                         "sample": f"{cores} whole sequences of the {w.name} workload per step, "
+                                   f"{how} ({what}; input draws outside the timed region)"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -332,8 +382,9 @@ class ClockSampler:
 
 # ------------------------------------------------------------------- GPU ---
 class GpuWorkload:
-    """A workload resident in HBM: INT8 cache, BF16 twin cache, tables, q and
-    the step's new tokens, plus pinned host copies for the end-to-end arm."""
+    """A workload resident in HBM: INT8 cache, 16-bit twin cache, tables, q and
+    the step's new tokens (K/V drawn on the GPU), plus host copies of the
+    step's inputs for the end-to-end arm."""
 
     def __init__(self, w: W.Workload, dev, arms=("int8", "kv16")):
         import torch
@@ -349,32 +400,30 @@ class GpuWorkload:
         self.int8 = kvq.alloc_int8_cache(nb, w.num_kv_heads, w.head_dim, dev) if "int8" in arms else None
         self.kv16 = (kvq.alloc_kv16_cache(nb, w.num_kv_heads, w.head_dim, tdt, dev)
                      if "kv16" in arms else None)
-        for b in range(w.num_seqs):
-            k, v = w.seq_kv(b)
-            n = int(w.prefix_lens[b])
-            if n == 0:
-                continue
-            s = torch.from_numpy(w.slots(b, 0, n)).to(dev)
-            kd, vd = up(k[:n]), up(v[:n])
-            if self.int8 is not None:
-                kvq.kvq_quantize_append(kd, vd, s, *self.int8)
-            if self.kv16 is not None:
-                kvq.kvq_cache_append_kv16(kd, vd, s, *self.kv16)
         ks, vs, ss = [], [], []
-        if w.append:
-            for b in range(w.num_seqs):
-                k, v = w.seq_kv(b)
-                L = int(w.context_lens[b])
+        for b in range(w.num_seqs):
+            L = int(w.context_lens[b])
+            if L == 0:
+                continue
+            k, v = w.seq_kv_device(b, dev)
+            n = int(w.prefix_lens[b])
+            if n:
+                s = torch.from_numpy(w.slots(b, 0, n)).to(dev)
+                if self.int8 is not None:
+                    kvq.kvq_quantize_append(k[:n], v[:n], s, *self.int8)
+                if self.kv16 is not None:
+                    kvq.kvq_cache_append_kv16(k[:n], v[:n], s, *self.kv16)
+            if w.append:
                 ks.append(k[L - 1:L]); vs.append(v[L - 1:L]); ss.append(w.slots(b, L - 1, L))
         if w.prefill_tokens:
-            pk, pv = w.prefill_kv()
+            pk, pv = w.prefill_kv_device(dev)
             ks.append(pk); vs.append(pv); ss.append(w.prefill_slots())
-        self.k_new_h = np.concatenate(ks) if ks else None
-        self.v_new_h = np.concatenate(vs) if vs else None
+        self.k_new = torch.cat(ks).contiguous() if ks else None
+        self.v_new = torch.cat(vs).contiguous() if vs else None
         self.slots_h = np.concatenate(ss).astype(np.int64) if ss else None
-        self.k_new = up(self.k_new_h) if ks else None
-        self.v_new = up(self.v_new_h) if vs else None
         self.slots = torch.from_numpy(self.slots_h).to(dev) if ss else None
+        self.k_new_h = self.k_new.view(torch.int16).cpu().numpy() if ks else None
+        self.v_new_h = self.v_new.view(torch.int16).cpu().numpy() if vs else None
         self.q_h = w.q_all()
         self.q = up(self.q_h)
         self.bt_h = bt
@@ -408,6 +457,39 @@ class GpuWorkload:
 
     def launches_per_step(self):
         return (1 if self.k_new is not None else 0) + 1 + (1 if self.split else 0)
+
+
+def arm_summary(w: W.Workload, step_ms, dec_ms, step16_ms, dec16_ms, peak) -> dict:
+    """Per-workload figures of one INT8 arm and one 16-bit-twin arm (mean
+    step and decode times in ms)."""
+    dec_gbs = w.decode_bytes_int8() / (dec_ms * 1e-3) / 1e9
+    return {"decode_us": round(1e3 * dec_ms, 3), "decode_gbs": round(dec_gbs, 1),
+            "decode_pct_of_measured_peak": round(100 * dec_gbs / peak, 2),
+            "decode_pct_of_nominal_8tbs": round(100 * dec_gbs / 8000.0, 2),
+            "decode_bytes": w.decode_bytes_int8(),
+            "bytes_per_decoded_token": round(w.decode_bytes_int8() / max(w.num_seqs, 1)),
+            "append_tokens_per_step": w.append_tokens(),
+            "step_us": round(1e3 * step_ms, 3),
+            "step_gbs": round((w.append_bytes_int8() + w.decode_bytes_int8()) /
+                              (step_ms * 1e-3) / 1e9, 1),
+            "bf16_decode_us": round(1e3 * dec16_ms, 3),
+            "bf16_decode_gbs": round(w.decode_bytes_kv16() / (dec16_ms * 1e-3) / 1e9, 1),
+            "bf16_step_us": round(1e3 * step16_ms, 3),
+            "int8_vs_bf16_decode_speed": round(dec16_ms / dec_ms, 3),
+            "int8_vs_bf16_steps_per_s": round(step16_ms / step_ms, 3),
+            "traffic": read_traffic(w.name)}
+
+
+def measure_config(torch, w: W.Workload, dev, flush, steps, warmup, peak) -> dict:
+    """The INT8 step and the twin's step of workload w (resident, L2 flushed
+    between steps)."""
+    g = GpuWorkload(w, dev)
+    t_step, t_dec = time_arm(torch, flush, g.append_int8, g.decode_int8, steps, warmup)
+    t_step16, t_dec16 = time_arm(torch, flush, g.append_kv16, g.decode_kv16, steps, warmup)
+    del g
+    torch.cuda.empty_cache()
+    return arm_summary(w, *[statistics.mean(t) for t in (t_step, t_dec, t_step16, t_dec16)],
+                       peak)
 
 
 def time_arm(torch, flush, append, decode, steps, warmup, settle_s=0.0):
@@ -659,6 +741,18 @@ def main():
     dec_gbs = w.decode_bytes_int8() / (dec_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
     traffic = read_traffic(w.name)
+    launches = args.steps * g.launches_per_step()
+    del g
+    torch.cuda.empty_cache()
+    configs = None
+    if not args.no_configs:
+        configs = {}
+        for name in W.NAMES:
+            if name == w.name:
+                configs[name] = arm_summary(w, step_ms, dec_ms, step16_ms, dec16_ms, peak)
+            else:
+                configs[name] = measure_config(torch, W.make(name), dev, flush, args.steps,
+                                               args.warmup, peak)
     sw = None
     if not args.no_sweep:
         sw = sweep(torch, kvq, dev, flush, max(5, min(args.steps, 20)))
@@ -696,9 +790,10 @@ def main():
         "e2e": {"value": round(job_throughput(world, step_bytes, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": args.steps * g.launches_per_step(),
+        "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "configs": configs,
         "context_sweep": sw,
         "chunked_prefill": pf,
     }

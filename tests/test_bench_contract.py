@@ -44,7 +44,7 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["metric"].startswith("INT8-KV paged decode")
     assert line["unit"] == "GB/s" and line["value"] > 0 and line["higher_is_better"] is True
     assert line["n_gpus"] == 1 and line["steps"] == 1 and line["warmup"] == 0
-    assert line["config"]["workload"] == "canonical"
+    assert line["config"]["workload"] == "mha"          # the headline workload
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -202,7 +202,56 @@ class Workload:
         v = self._draw(n, self.v_std, _STREAM["pv"])
         return to_bits(k, self.dtype), to_bits(v, self.dtype)
 
+    # ---------------------------------------------- device-side draws ---
+    def _torch_draw(self, n: int, std: float, device, *key: int):
+        import torch
+        state = np.random.SeedSequence([self.seed, self.wid, *key]).generate_state(2, np.uint32)
+        g = torch.Generator(device=device)
+        g.manual_seed((int(state[0]) << 31) ^ int(state[1]))
+        x = torch.randn((n, self.num_kv_heads, self.head_dim), generator=g, device=device,
+                        dtype=torch.float32)
+        if std != 1.0:
+            x *= std
+        return x
+
+    def _torch_dtype(self):
+        import torch
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float16
+
+    def seq_kv_device(self, b: int, device):
+        """seq_kv's recipe drawn on the device with torch's generator: the same
+        distribution, outlier channels and all-zero token positions, another
+        stream of N(0, 1) numbers.  Returns (k, v) tensors [L, Hkv, D] of the
+        workload dtype (RNE from float32).  For timing runs, where numpy draws
+        of the large workloads would take a minute."""
+        L = int(self.context_lens[b])
+        k = self._torch_draw(L, self.k_std, device, _STREAM["k"], b)
+        v = self._torch_draw(L, self.v_std, device, _STREAM["v"], b)
+        if self.outlier_channels:
+            idx = self._outlier_idx()
+            for j in range(self.num_kv_heads):
+                k[:, j, list(idx[j])] *= float(self.outlier_gain)
+        if self.zero_token_frac > 0.0 and L > 0:
+            nz = int(math.floor(self.zero_token_frac * L))
+            if nz:
+                zr = _rng(self.seed, self.wid, _STREAM["zero"], b)
+                pos = list(zr.choice(L, nz, replace=False))
+                k[pos] = 0.0
+                v[pos] = 0.0
+        return k.to(self._torch_dtype()), v.to(self._torch_dtype())
+
+    def prefill_kv_device(self, device):
+        n = self.prefill_tokens
+        k = self._torch_draw(n, self.k_std, device, _STREAM["pk"])
+        v = self._torch_draw(n, self.v_std, device, _STREAM["pv"])
+        return k.to(self._torch_dtype()), v.to(self._torch_dtype())
+
     # ---------------------------------------------------- byte accounting ---
+    def decode_bytes_int8_seq(self, L: int) -> int:
+        """decode_bytes_int8's share of one sequence with context L."""
+        return (int(L) * self.num_kv_heads * (2 * self.head_dim + 4) + self.pages(L) * 4 +
+                2 * self.num_q_heads * self.head_dim * 2 + 4)
+
     def decode_bytes_int8(self) -> int:
         """Algorithmic HBM bytes of one INT8 decode: K/V payload + scales of the
         attended tokens, the block-table entries read, q and out."""
