@@ -89,6 +89,8 @@ def parse_args():
                     help="chunked-prefill timing instead of the decode bench line: one JSON "
                          "line per shape (causal attention TFLOP/s against the tensor peak)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--profile-seqs", type=int, default=0,
+                    help="with --profile-arm: only the workload's first N sequences")
     ap.add_argument("--profile-arm", choices=["int8", "kv16"], default=None,
                     help="profiling run: only this decode arm (one cache on the device), "
                          "warm-up + steps with L2 flushes, a short timing line; no bench line")
@@ -562,6 +564,36 @@ def time_e2e(torch, g: GpuWorkload, flush, steps, warmup):
     return [a.elapsed_time(b) for a, b in ev], h2d, d2h
 
 
+def host_cost(torch, g: GpuWorkload, calls: int = 200) -> dict:
+    """CPU time to submit one kvq_paged_decode (argument checks, launcher,
+    tensor maps, launches), timed over back-to-back calls whose GPU work
+    queues up behind each other: through the C ABI with prepared ctypes
+    arguments, and through the Python binding."""
+    import ctypes
+    w, L = g.w, g.kvq.load()
+    kc, vc, ks, vs = g.int8
+    P = ctypes.c_void_p
+    args = [P(g.q.data_ptr()), 1 if w.dtype == "bf16" else 0, w.num_seqs, w.num_q_heads,
+            w.num_kv_heads, w.head_dim, P(kc.data_ptr()), P(vc.data_ptr()), P(ks.data_ptr()),
+            P(vs.data_ptr()), kc.shape[0], 16, P(g.bt.data_ptr()), g.bt.shape[1],
+            P(g.cl.data_ptr()), w.max_context_len, w.sm_scale, P(g.out.data_ptr()),
+            P(g.ws.data_ptr()), g.ws.numel(), P(torch.cuda.current_stream().cuda_stream)]
+    res = {}
+    for name, fn in (("c_abi", lambda: L.kvq_paged_decode(*args)),
+                     ("python_binding", g.decode_int8)):
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn()
+        t = time.perf_counter() - t0
+        torch.cuda.synchronize()
+        res[name] = round(1e6 * t / calls, 2)
+    res["calls"] = calls
+    return res
+
+
 def sweep(torch, kvq, dev, flush, steps):
     """INT8 vs BF16-twin decode at 2K/8K/32K context (16 seqs, 32/8 heads,
     d 128, bf16), inputs drawn on the GPU from a seeded generator."""
@@ -671,6 +703,8 @@ def prefill_measure(torch, kvq, dev, flush, names, steps, warmup):
 
 def profile_arm(torch, w, dev, args):
     """One decode arm alone (for ncu captures of a bounded device footprint)."""
+    if args.profile_seqs:
+        w = W.first_seqs(w, args.profile_seqs)
     g = GpuWorkload(w, dev, arms=(args.profile_arm,))
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.zero_()  # noqa: E731
@@ -733,6 +767,7 @@ def main():
                                  args.warmup)
     t_e2e, h2d, d2h = time_e2e(torch, g, flush, args.steps, args.warmup)
     barrier()
+    host_us = host_cost(torch, g)
 
     step_ms, dec_ms, step16_ms, dec16_ms, e2e_ms = max_over_ranks(
         pg, dev, [statistics.mean(t) for t in (t_step, t_dec, t_step16, t_dec16, t_e2e)])
@@ -790,6 +825,7 @@ def main():
         "e2e": {"value": round(job_throughput(world, step_bytes, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
+        "host_us_per_call": host_us,
         "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -2,6 +2,7 @@
 // decode launcher, TMA descriptor construction, and the device error word.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -35,13 +36,25 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxRangePages = 1 << 24;   // forced range length accepted by the _split calls
 
+// Tensor maps of recently used caches, so that repeated calls on the same
+// cache skip the driver's encode.
+constexpr int kMapCache = 16;
+struct MapEntry {
+  const void* base = nullptr;
+  int64_t rows = 0;
+  int D = 0, eb = 0, box_rows = 0;
+  CUtensorMap map;
+};
+
 struct DeviceState {
-  bool ready = false;
+  std::atomic<bool> ready{false};
   int sms = 0;
   unsigned int* err = nullptr;
-  // occupancy cache: [variant][last smem] -> ctas per SM
-  size_t occ_smem[12] = {};
-  int occ_ctas[12] = {};
+  // occupancy cache: [variant] -> (last smem << 32) | ctas per SM
+  std::atomic<uint64_t> occ[24] = {};
+  std::mutex map_mu;
+  MapEntry maps[kMapCache];
+  int map_next = 0;
 };
 
 std::mutex g_mu;
@@ -54,9 +67,10 @@ kvq_status cuda_fail() { return KVQ_ERR_CUDA; }
 DeviceState* device_state() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& st = g_dev[dev];
-  if (st.ready) return &st;
+  if (st.ready.load(std::memory_order_acquire)) return &st;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st.ready.load(std::memory_order_relaxed)) return &st;
   if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err), g_kvq_error_word) != cudaSuccess)
@@ -71,21 +85,16 @@ DeviceState* device_state() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   // opt every decode variant into the largest shared-memory footprint it can use
-  for (int D : {64, 128}) {
-    for (bool bf : {false, true}) {
-      if (decode_configure_int8(D, bf, decode_smem_bytes_int8(D, kMaxSeqs, kMaxGroup)) !=
-              cudaSuccess ||
-          decode_configure_static(D, bf, decode_smem_bytes_static(D, kMaxSeqs, kMaxGroup)) !=
-              cudaSuccess ||
-          decode_configure_kv16(D, bf, decode_smem_bytes_kv16(D, kMaxSeqs, kMaxGroup)) !=
-              cudaSuccess)
-        return nullptr;
-    }
-  }
+  for (const DecodeOps* ops : {&kDecodeInt8H1, &kDecodeInt8H2, &kDecodeStaticH1,
+                               &kDecodeStaticH2, &kDecodeKv16})
+    for (int D : {64, 128})
+      for (bool bf : {false, true})
+        if (ops->configure(D, bf, ops->smem(D, kMaxSeqs, kMaxGroup)) != cudaSuccess)
+          return nullptr;
   for (int D : {64, 128})
     for (bool bf : {false, true})
       if (prefill_configure(D, bf) != cudaSuccess) return nullptr;
-  st.ready = true;
+  st.ready.store(true, std::memory_order_release);
   return &st;
 }
 
@@ -93,26 +102,33 @@ DeviceState* device_state() {
 // static (per-tensor) scales, and the 16-bit twin.
 enum class Dec { kInt8 = 0, kStatic = 1, kKv16 = 2 };
 
-size_t dec_smem(Dec v, int D, int B, int G) {
-  return v == Dec::kInt8     ? decode_smem_bytes_int8(D, B, G)
-         : v == Dec::kStatic ? decode_smem_bytes_static(D, B, G)
-                             : decode_smem_bytes_kv16(D, B, G);
+static_assert(kMaxHeadGroup == 1 || kMaxHeadGroup == 2, "head groups of 1 or 2 KV heads");
+
+// KV heads one decode warp processes together: the largest power of two H
+// up to kMaxHeadGroup with G H <= 8 (the MMAs' N) that divides Hkv.  The
+// 16-bit twin keeps H = 1.
+int head_group(Dec var, int32_t G, int32_t Hkv) {
+  if (var == Dec::kKv16) return 1;
+  int H = 1;
+  while (2 * H <= kMaxHeadGroup && 2 * H * G <= kMaxGroup && Hkv % (2 * H) == 0) H *= 2;
+  return H;
 }
 
-int ctas_per_sm(DeviceState* st, Dec var, int D, bool bf16, size_t smem) {
-  // cache slots: {int8, static, kv16} x {D128, D64} x {fp16, bf16}
-  const int v = (int)var * 4 + (D == 128 ? 0 : 2) + (bf16 ? 1 : 0);
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (st->occ_smem[v] != smem || st->occ_ctas[v] == 0) {
-    int n = 0;
-    cudaError_t e = var == Dec::kInt8     ? decode_occupancy_int8(D, bf16, smem, &n)
-                    : var == Dec::kStatic ? decode_occupancy_static(D, bf16, smem, &n)
-                                          : decode_occupancy_kv16(D, bf16, smem, &n);
-    if (e != cudaSuccess || n <= 0) return 0;
-    st->occ_smem[v] = smem;
-    st->occ_ctas[v] = n;
-  }
-  return st->occ_ctas[v];
+const DecodeOps& ops_of(Dec var, int H) {
+  if (var == Dec::kInt8) return H == 2 ? kDecodeInt8H2 : kDecodeInt8H1;
+  if (var == Dec::kStatic) return H == 2 ? kDecodeStaticH2 : kDecodeStaticH1;
+  return kDecodeKv16;
+}
+
+int ctas_per_sm(DeviceState* st, Dec var, int H, int D, bool bf16, size_t smem) {
+  // cache slots: {int8, static, kv16} x {H 1, 2} x {D128, D64} x {fp16, bf16}
+  const int v = ((int)var * 2 + (H == 2 ? 1 : 0)) * 4 + (D == 128 ? 0 : 2) + (bf16 ? 1 : 0);
+  const uint64_t c = st->occ[v].load(std::memory_order_relaxed);
+  if ((c >> 32) == (uint64_t)smem && (c & 0xFFFFFFFFu) != 0) return (int)(c & 0xFFFFFFFFu);
+  int n = 0;
+  if (ops_of(var, H).occupancy(D, bf16, smem, &n) != cudaSuccess || n <= 0) return 0;
+  st->occ[v].store(((uint64_t)smem << 32) | (uint32_t)n, std::memory_order_relaxed);
+  return n;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -156,8 +172,11 @@ int64_t ranges_for_bytes(int32_t B, int32_t G, int32_t D, size_t bytes) {
 
 // Warps of a full persistent grid of one decode variant on this device (0
 // on failure).
-int64_t resident_warps(DeviceState* st, Dec var, int D, bool bf16, int32_t B, int32_t G) {
-  return (int64_t)st->sms * ctas_per_sm(st, var, D, bf16, dec_smem(var, D, B, G)) * kWarps;
+int64_t resident_warps(DeviceState* st, Dec var, int D, bool bf16, int32_t B, int32_t G,
+                       int32_t Hkv) {
+  const int H = head_group(var, G, Hkv);
+  const size_t smem = ops_of(var, H).smem(D, B, G * H);
+  return (int64_t)st->sms * ctas_per_sm(st, var, H, D, bf16, smem) * kWarps;
 }
 
 // Work units of the balanced split for a grid of `warps` warps: one range
@@ -169,32 +188,62 @@ int64_t balanced_units(int64_t warps, int32_t Hkv, int64_t cols_max) {
   return (int64_t)Hkv * (groups < by_cols ? groups : by_cols);
 }
 
-// Units kvq_paged_decode's balanced split uses at most on this device: for
-// the full grid of whichever decode variant has the most resident warps.
-int64_t balanced_units_max(DeviceState* st, int32_t B, int32_t Hkv, int32_t G, int32_t D,
-                           int32_t max_ctx) {
-  int64_t w = 0;
+// Workspace bytes kvq_paged_decode's balanced split uses at most on this
+// device: for the full grid of each decode variant (its head group), the
+// largest.
+size_t balanced_bytes_max(DeviceState* st, int32_t B, int32_t Hkv, int32_t G, int32_t D,
+                          int32_t max_ctx) {
+  size_t best = 0;
   for (Dec var : {Dec::kInt8, Dec::kStatic, Dec::kKv16})
     for (bool bf : {false, true}) {
-      const int64_t x = resident_warps(st, var, D, bf, B, G);
-      w = x > w ? x : w;
+      const int H = head_group(var, G, Hkv);
+      const int64_t w = resident_warps(st, var, D, bf, B, G, Hkv);
+      const size_t x =
+          layout_for(B, G * H, D, balanced_units(w, Hkv / H, columns_max(B, max_ctx))).total;
+      best = x > best ? x : best;
     }
-  return balanced_units(w, Hkv, columns_max(B, max_ctx));
+  return best;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int elem_bytes, int D, int64_t rows) {
+// Tensor map over a cache payload seen as `rows` token rows of D elements;
+// a box is one 128-byte (or narrower) column block of box_rows rows.
+bool encode_map(CUtensorMap* m, const void* base, int elem_bytes, int D, int64_t rows,
+                int box_rows) {
   const CUtensorMapDataType dt =
       elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   const int row_bytes = D * elem_bytes;
   const int sub = row_bytes < 128 ? row_bytes : 128;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)(sub / elem_bytes), (cuuint32_t)kBlockSize};
+  cuuint32_t box[2] = {(cuuint32_t)(sub / elem_bytes), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapSwizzle sw = sub == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor map of a cache payload (encoded once per (base, rows, D,
+// element size, box rows) and kept among the device's recent ones).
+bool make_map(DeviceState* st, CUtensorMap* m, const void* base, int elem_bytes, int D,
+              int64_t rows, int box_rows = kBlockSize) {
+  std::lock_guard<std::mutex> lk(st->map_mu);
+  for (const MapEntry& e : st->maps)
+    if (e.base == base && e.rows == rows && e.D == D && e.eb == elem_bytes &&
+        e.box_rows == box_rows) {
+      *m = e.map;
+      return true;
+    }
+  if (!encode_map(m, base, elem_bytes, D, rows, box_rows)) return false;
+  MapEntry& e = st->maps[st->map_next];
+  st->map_next = (st->map_next + 1) % kMapCache;
+  e.base = base;
+  e.rows = rows;
+  e.D = D;
+  e.eb = elem_bytes;
+  e.box_rows = box_rows;
+  e.map = *m;
+  return true;
 }
 
 // Shared validation of the decode arguments (both caches).
@@ -244,9 +293,14 @@ kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int
   DeviceState* st = device_state();
   if (!st) return cuda_fail();
   const bool bf16 = dtype == KVQ_BF16;
-  const int32_t G = Hq / Hkv;
-  const size_t smem = dec_smem(var, D, B, G);
-  const int occ = ctas_per_sm(st, var, D, bf16, smem);
+  const int32_t Gr = Hq / Hkv;
+  // the kernel walks head groups of H KV heads: HU groups of G = Gr H query
+  // heads each (the group's query heads are consecutive)
+  const int H = head_group(var, Gr, Hkv);
+  const int32_t HU = Hkv / H, G = Gr * H;
+  const DecodeOps& ops = ops_of(var, H);
+  const size_t smem = ops.smem(D, B, G);
+  const int occ = ctas_per_sm(st, var, H, D, bf16, smem);
   if (occ <= 0) return cuda_fail();
   const int64_t slots = (int64_t)st->sms * occ;      // CTAs of a full persistent grid
   const int64_t cols = columns_max(B, max_ctx);
@@ -256,32 +310,32 @@ kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int
   WsLayout wl;
   int64_t grid = 0;
   if (R == 0 && (ws == nullptr || ws_bytes == 0 || pages_max <= 1)) {
-    p.R = -1;                                       // one unit per (sequence, KV head)
+    p.R = -1;                                       // one unit per (sequence, head group)
     p.range_cap = 0;
-    grid = cdiv((int64_t)B * Hkv, kWarps);
+    grid = cdiv((int64_t)B * HU, kWarps);
     if (grid > slots) grid = slots;
   } else if (R == 0) {
-    // as many ranges as groups of Hkv warps of the full grid, within the
+    // as many ranges as groups of HU warps of the full grid, within the
     // workspace's slots; with fewer ranges than sequences the per-sequence
     // split (above) keeps more warps busy
     const int64_t cap = ranges_for_bytes(B, G, D, ws_bytes);
-    if (cap < Hkv) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-    const int64_t full = balanced_units(slots * kWarps, Hkv, cols) / Hkv;
-    const int64_t groups = full < cap / Hkv ? full : cap / Hkv;
+    if (cap < HU) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t full = balanced_units(slots * kWarps, HU, cols) / HU;
+    const int64_t groups = full < cap / HU ? full : cap / HU;
     if (groups < B && groups < full) {
       p.R = -1;
       p.range_cap = 0;
-      grid = cdiv((int64_t)B * Hkv, kWarps);
+      grid = cdiv((int64_t)B * HU, kWarps);
     } else {
       p.R = 0;
       p.groups = groups;
-      p.range_cap = groups * Hkv;
+      p.range_cap = groups * HU;
       wl = layout_for(B, G, D, p.range_cap);
       grid = cdiv(p.range_cap, kWarps);
     }
     if (grid > slots) grid = slots;
   } else {
-    p.range_cap = cdiv(cols, R) * Hkv;
+    p.range_cap = cdiv(cols, R) * HU;
     wl = layout_for(B, G, D, p.range_cap);
     if (ws == nullptr || ws_bytes < wl.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
     grid = cdiv(p.range_cap, kWarps);
@@ -290,16 +344,18 @@ kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int
   }
   if (grid < 1) grid = 1;
   // the kernel counts columns and work units in 32 bits
-  if (cols > INT32_MAX || p.range_cap > INT32_MAX || (int64_t)B * Hkv > INT32_MAX)
+  if (cols > INT32_MAX || p.range_cap > INT32_MAX || (int64_t)B * HU > INT32_MAX)
     return KVQ_ERR_UNSUPPORTED;
   const bool split = p.R >= 0;
   if (split && (!ws || !aligned(ws, 256) || ws_bytes < wl.total))
     return KVQ_ERR_INVALID_ARGUMENT;
 
+  // one box = the adjacent (page, head) tiles of a head group
   CUtensorMap maps[2];
   const int64_t rows = (int64_t)num_blocks * Hkv * kBlockSize;
   const int eb = var == Dec::kKv16 ? 2 : 1;
-  if (!make_map(&maps[0], kc, eb, D, rows) || !make_map(&maps[1], vc, eb, D, rows))
+  if (!make_map(st, &maps[0], kc, eb, D, rows, kBlockSize * H) ||
+      !make_map(st, &maps[1], vc, eb, D, rows, kBlockSize * H))
     return cuda_fail();
 
   p.q = q;
@@ -316,20 +372,16 @@ kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int
   p.err = st->err;
   p.B = B;
   p.Hq = Hq;
-  p.Hkv = Hkv;
+  p.Hkv = HU;
   p.G = G;
+  p.Gr = Gr;
   p.max_blocks = max_blocks;
   p.max_ctx = max_ctx;
   p.num_blocks = num_blocks;
   p.scale_log2 = (float)((double)sm_scale * (double)k_static * 1.4426950408889634);
   p.v_static = v_static;
 
-  cudaError_t e = var == Dec::kInt8
-                      ? decode_launch_int8(D, bf16, maps, p, (int)grid, smem, stream)
-                  : var == Dec::kStatic
-                      ? decode_launch_static(D, bf16, maps, p, (int)grid, smem, stream)
-                      : decode_launch_kv16(D, bf16, maps, p, (int)grid, smem, stream);
-  if (e != cudaSuccess) return cuda_fail();
+  if (ops.launch(D, bf16, maps, p, (int)grid, smem, stream) != cudaSuccess) return cuda_fail();
   if (split) {
     CombineParams cp{};
     cp.part_o = p.part_o;
@@ -338,7 +390,7 @@ kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int
     cp.out = out;
     cp.B = B;
     cp.Hq = Hq;
-    cp.Hkv = Hkv;
+    cp.Hkv = HU;
     cp.G = G;
     cp.max_tok = max_blocks * kBlockSize < max_ctx ? max_blocks * kBlockSize : max_ctx;
     cp.R = p.R;
@@ -677,8 +729,8 @@ kvq_status kvq_paged_prefill(const void* q, kvq_dtype dtype, int32_t num_seqs,
   if (tiles > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
   CUtensorMap maps[2];
   const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
-  if (!make_map(&maps[0], k_cache, 1, head_dim, rows) ||
-      !make_map(&maps[1], v_cache, 1, head_dim, rows))
+  if (!make_map(st, &maps[0], k_cache, 1, head_dim, rows) ||
+      !make_map(st, &maps[1], v_cache, 1, head_dim, rows))
     return cuda_fail();
   PrefillParams p{};
   p.q = q;
@@ -714,9 +766,10 @@ int32_t kvq_decode_partition_pages(int32_t num_seqs, int32_t num_q_heads, int32_
   DeviceState* st = device_state();
   if (!st) return 0;
   const int32_t G = num_q_heads / num_kv_heads;
-  const int64_t w = resident_warps(st, Dec::kInt8, head_dim, true, num_seqs, G);
+  const int64_t w = resident_warps(st, Dec::kInt8, head_dim, true, num_seqs, G, num_kv_heads);
   if (w <= 0) return 0;
-  const int64_t groups = w / num_kv_heads > 0 ? w / num_kv_heads : 1;
+  const int64_t HU = num_kv_heads / head_group(Dec::kInt8, G, num_kv_heads);
+  const int64_t groups = w / HU > 0 ? w / HU : 1;
   const int64_t r = cdiv(columns_max(num_seqs, max_context_len), groups);
   return (int32_t)(r > kMinRangePages ? (r < INT32_MAX ? r : INT32_MAX) : kMinRangePages);
 }
@@ -743,9 +796,7 @@ size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
   DeviceState* st = device_state();
   if (!st) return 0;
   const int32_t G = num_q_heads / num_kv_heads;
-  return layout_for(num_seqs, G, head_dim,
-                    balanced_units_max(st, num_seqs, num_kv_heads, G, head_dim, max_context_len))
-      .total;
+  return balanced_bytes_max(st, num_seqs, num_kv_heads, G, head_dim, max_context_len);
 }
 
 kvq_status kvq_selftest_wait_timeout(uint32_t limit_us, kvq_stream_t stream) {

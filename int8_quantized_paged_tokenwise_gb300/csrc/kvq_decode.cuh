@@ -54,20 +54,24 @@
 namespace kvq {
 
 // STATIC: INT8 codes with one binary32 scale per tensor (no scale planes).
-template <int D, bool INT8, bool STATIC = false>
+// H: KV heads processed together (a "head group"): the (page, head) tiles of
+// H consecutive KV heads of a block are adjacent in the cache, so one copy
+// brings the group's H tiles (16 H token rows) and its H scale rows.
+template <int D, bool INT8, bool STATIC = false, int H = 1>
 struct TileCfg {
   static constexpr int kElem = INT8 ? 1 : 2;                 // bytes per cache element
   static constexpr int kRowBytes = D * kElem;                // bytes per token row
   static constexpr int kSubRow = kRowBytes < 128 ? kRowBytes : 128;   // TMA box row bytes
   static constexpr int kSubTiles = kRowBytes / kSubRow;       // TMA copies per tile
-  static constexpr int kSubBytes = kBlockSize * kSubRow;
-  static constexpr int kTile = kBlockSize * kRowBytes;        // bytes of one K (or V) tile
+  static constexpr int kRows = H * kBlockSize;                // token rows of a group tile
+  static constexpr int kSubBytes = kRows * kSubRow;
+  static constexpr int kTile = kRows * kRowBytes;             // bytes of one K (or V) group tile
   static constexpr int kStages = INT8 ? KVQ_INT8_STAGES : 2;  // pages in flight per warp
-  static constexpr int kStageBytes = 2 * kTile;               // K tile then V tile
-  static constexpr int kScaleBytes = INT8 && !STATIC ? 2 * kBlockSize * 2 : 0;  // K, V scale rows
+  static constexpr int kStageBytes = 2 * kTile;               // K tiles then V tiles
+  static constexpr int kScaleBytes = INT8 && !STATIC ? 2 * kRows * 2 : 0;  // K, V scale rows
   static constexpr uint32_t kTxBytes = 2 * kTile + kScaleBytes;
   static constexpr uint32_t kSwzMask = kSubRow == 128 ? 0x70u : 0x30u;
-  static constexpr int kMinCtas = INT8 ? KVQ_INT8_MIN_CTAS : 3;
+  static constexpr int kMinCtas = INT8 ? (H == 1 ? KVQ_INT8_MIN_CTAS : 3) : 3;
 };
 
 // Byte offset inside a (K or V) tile of 16-byte chunk `c` of token row `t`,
@@ -179,20 +183,22 @@ __device__ __forceinline__ Piece next_piece(const WalkConst& w, const int* prefi
 }
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).  Per warp:
-// S page stages, one raw query slot (the TMA target, G*D*2 bytes) and a query
-// fragment buffer ([k-step][lane] pairs of the MMA B operand for the lanes
-// 0..4G-1 of real heads, also G*D*2 bytes; the padded heads read as zeros).
-template <int D, bool INT8, bool STATIC = false>
+// S page stages, one raw query slot (the TMA target, GH*D*2 bytes, GH = query
+// heads of the head group) and the query fragments of the MMA B operand:
+// per KV head h of the group, [k-step][lane] pairs holding the lane's column
+// if that column is one of head h's query heads, else zeros.
+template <int D, bool INT8, bool STATIC = false, int H = 1>
 struct SmemLayout {
-  using C = TileCfg<D, INT8, STATIC>;
+  using C = TileCfg<D, INT8, STATIC, H>;
+  static constexpr uint32_t kFragBytes = (uint32_t)H * (D / 16) * 32 * 8;
   size_t tiles, q, qfrag, scales, bars, stage_blk, misc, walk, seq, total_bytes;
-  uint32_t q_bytes;  // one piece's query rows: G * D * 2
-  __host__ __device__ SmemLayout(int B, int G) {
-    q_bytes = (uint32_t)(G * D * 2);
+  uint32_t q_bytes;  // one piece's query rows: GH * D * 2
+  __host__ __device__ SmemLayout(int B, int GH) {
+    q_bytes = (uint32_t)(GH * D * 2);
     tiles = 0;
     q = tiles + (size_t)kWarps * C::kStages * C::kStageBytes;
     qfrag = q + (size_t)kWarps * q_bytes;
-    scales = qfrag + (size_t)kWarps * q_bytes;
+    scales = qfrag + (size_t)kWarps * kFragBytes;
     bars = (scales + (size_t)kWarps * C::kStages * C::kScaleBytes + 15) & ~(size_t)15;
     stage_blk = bars + (size_t)kWarps * C::kStages * 8;
     misc = stage_blk + (size_t)kWarps * C::kStages * 4;   // 4 ints (scan of warp sums)
@@ -209,13 +215,17 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 }
 
 // INT8: QBF16 = activations are bf16 (converted to FP16 for the tensor cores);
-// twin: QBF16 selects the bf16 MMA, otherwise FP16.
-template <int D, bool INT8, bool QBF16, bool STATIC = false>
-__global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
+// twin: QBF16 selects the bf16 MMA, otherwise FP16.  H: KV heads per head
+// group; the walk sees p.Hkv = Hkv / H groups of p.G = G H query heads each
+// (p.Gr = G), the group's query heads being consecutive.
+template <int D, bool INT8, bool QBF16, bool STATIC = false, int H = 1>
+__global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCtas)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
-  using C = TileCfg<D, INT8, STATIC>;
-  const SmemLayout<D, INT8, STATIC> lay(p.B, p.G);
+  using C = TileCfg<D, INT8, STATIC, H>;
+  using Lay = SmemLayout<D, INT8, STATIC, H>;
+  const Lay lay(p.B, p.G);
+  static_assert(INT8 || H == 1, "head groups are built for the INT8 cache");
   constexpr bool MMA_BF16 = (!INT8) && QBF16;
   constexpr int S = C::kStages;
   constexpr int KSTEPS = D / 16;       // MMA k-steps over the head dim
@@ -346,11 +356,18 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
 
   const uint32_t tiles_u32 = smem_u32(smem + lay.tiles) + warp * S * C::kStageBytes;
   const uint32_t q_u32 = smem_u32(smem + lay.q) + warp * lay.q_bytes;
-  uint2* qfrag = reinterpret_cast<uint2*>(smem + lay.qfrag + (size_t)warp * lay.q_bytes);
-  // lanes of padded heads (g >= G) read a real head's fragment: their
-  // columns of the MMAs are never used, and finite values keep them quiet
-  const uint32_t qfrag_lane_u32 = smem_u32(qfrag) + 8 * (lane % (4 * G));   // + 32 * G * ks
-  const uint32_t qks = 32u * (uint32_t)G;                        // bytes per k-step
+  uint2* qfrag = reinterpret_cast<uint2*>(smem + lay.qfrag + (size_t)warp * Lay::kFragBytes);
+  // this lane's B fragment of (KV head h of the group, k-step ks):
+  // qfrag_lane_u32 + qhs * h + qks * ks; columns of other heads (and the
+  // padded ones, g >= G H) hold zeros there
+  const uint32_t qfrag_lane_u32 = smem_u32(qfrag) + 8 * lane;
+  constexpr uint32_t qks = 32u * 8u;                             // bytes per k-step
+  constexpr uint32_t qhs = qks * KSTEPS;                         // bytes per KV head
+  // KV head (within the group) of this thread's score columns 2c, 2c+1 and
+  // of its B column g
+  const int Gr = H > 1 ? p.Gr : G;
+  const int hc0 = min(2 * c / Gr, H - 1), hc1 = min((2 * c + 1) / Gr, H - 1);
+  const int hg = g / Gr;
   const uint32_t scales_u32 = smem_u32(smem + lay.scales) + warp * S * C::kScaleBytes;
   const uint16_t* scales_w =
       reinterpret_cast<const uint16_t*>(smem + lay.scales) + warp * S * (C::kScaleBytes / 2);
@@ -369,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
   const int cp_x = cp_sub * (C::kSubRow / C::kElem);
   const uint32_t cp_dst = tiles_u32 + (lane < C::kSubTiles ? 0 : C::kTile) + cp_sub * C::kSubBytes;
   const uint16_t* sc_src = lane == kTensorCopies ? p.k_scale : p.v_scale;
-  const uint32_t sc_dst = scales_u32 + (lane == kTensorCopies ? 0 : kBlockSize * 2);
+  const uint32_t sc_dst = scales_u32 + (lane == kTensorCopies ? 0 : C::kRows * 2);
 
   // ---------------------------------------------------------------- issuer
   // Warp-uniform state; lanes 0..5 perform the copies.  The block ids of the
@@ -464,13 +481,13 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
         else mbar_arrive(bar);
       }
       if (blk >= 0) {
-        const int row = blk * Hkv + is_j;             // (block, KV head) tile index
+        const int row = blk * Hkv + is_j;             // (block, head group) tile index
         if (lane < kTensorCopies) {
-          tma_load_2d_evict_first(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * kBlockSize,
+          tma_load_2d_evict_first(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * C::kRows,
                                   bar);
         } else if (INT8 && !STATIC && lane < kTensorCopies + 2) {
-          bulk_load(sc_dst + s * C::kScaleBytes, sc_src + (int64_t)row * kBlockSize,
-                    kBlockSize * 2, bar);
+          bulk_load(sc_dst + s * C::kScaleBytes, sc_src + (int64_t)row * C::kRows,
+                    C::kRows * 2, bar);
         }
       }
       if (qbytes && lane == 4) {
@@ -544,15 +561,14 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
           mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
           const int sh = bf16_fp16_shift(mx);
           qinv = exp2i(-sh);
-          // padded heads mirror the real head whose fragment they read
-          const float qsg = __shfl_sync(0xFFFFFFFFu, exp2i(sh), lane % (4 * G));
+          const float qsg = exp2i(sh);               // 2^-126 for padded columns
           qs0 = __shfl_sync(0xFFFFFFFFu, qsg, 8 * c);
           qs1 = __shfl_sync(0xFFFFFFFFu, qsg, 8 * c + 4);
         }
-        if (has_head) {
 #pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {
-            uint2 f;
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          uint2 f = make_uint2(0u, 0u);
+          if (has_head) {
             if constexpr (INT8) {
               // logical k {2c,2c+1,2c+8,2c+9} of step ks <-> head-dim 16ks+4c+{0..3}
               const uint2 v = *reinterpret_cast<const uint2*>(qs + 16 * ks + 4 * c);
@@ -569,10 +585,13 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
               f.x = *reinterpret_cast<const uint32_t*>(qs + 16 * ks + 2 * c);
               f.y = *reinterpret_cast<const uint32_t*>(qs + 16 * ks + 8 + 2 * c);
             }
-            qfrag[ks * 4 * G + lane] = f;
           }
+          // the fragment goes to its KV head's MMAs; the others see zeros
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+            qfrag[(h * KSTEPS + ks) * 32 + lane] = h == hg ? f : make_uint2(0u, 0u);
         }
-        __syncwarp();   // padded lanes read fragments written by other lanes
+        __syncwarp();   // the raw query slot may be refilled once every lane is done
         q_consumed = ord;
       }
       const int blk = blk_w[s];
@@ -585,14 +604,17 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
         const int lt = (lane & 7) + ((lane >> 3) & 1) * 8;
 
         // ---------- S[token][head] = K Q^T: M = 16 tokens, N = 8 heads ----------
-        // two accumulators (even/odd k-steps) halve the dependent MMA chain
+        // two accumulators (even/odd k-steps) halve the dependent MMA chain;
+        // the KV heads of the group add into the same S, each into its own
+        // columns (the B fragments of the other columns are zero)
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kk = 0; kk < (INT8 ? KSTEPS / 2 : 0); ++kk) {
+        for (int hk = 0; hk < (INT8 ? H * (KSTEPS / 2) : 0); ++hk) {
+          const int h = hk / (KSTEPS / 2), kk = hk % (KSTEPS / 2);
           uint32_t r0, r1, r2, r3;
-          ldsm_x4(kt + tile_off<C>(lt, 2 * kk + (lane >> 4)), r0, r1, r2, r3);
-          const uint2 qa = lds_u2(qfrag_lane_u32 + qks * (2 * kk));
-          const uint2 qb = lds_u2(qfrag_lane_u32 + qks * (2 * kk + 1));
+          ldsm_x4(kt + tile_off<C>(16 * h + lt, 2 * kk + (lane >> 4)), r0, r1, r2, r3);
+          const uint2 qa = lds_u2(qfrag_lane_u32 + qhs * h + qks * (2 * kk));
+          const uint2 qb = lds_u2(qfrag_lane_u32 + qhs * h + qks * (2 * kk + 1));
           if constexpr (INT8) {
             // r0/r1: tokens g / g+8, head-dim 16(2kk)+4c+{0..3}; r2/r3: next chunk
             uint32_t a0, a2, a1, a3;
@@ -619,15 +641,23 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
         }
 
         // scores in log2 units: z0 (token g, head 2c), z1 (g, 2c+1), z2 (g+8, 2c), z3
-        // (static scales: the K scale is folded into scale_log2)
-        float ksg = p.scale_log2, ksg8 = p.scale_log2;
+        // (static scales: the K scale is folded into scale_log2); a column's
+        // K scales are those of its KV head hc0 / hc1
+        float ks0 = p.scale_log2, ks1 = p.scale_log2, ks80 = p.scale_log2, ks81 = p.scale_log2;
         if constexpr (INT8 && !STATIC) {
           const uint16_t* ksc = scales_w + s * (C::kScaleBytes / 2);
-          ksg *= __half2float(__ushort_as_half(ksc[g]));
-          ksg8 *= __half2float(__ushort_as_half(ksc[g + 8]));
+          ks0 *= __half2float(__ushort_as_half(ksc[16 * hc0 + g]));
+          ks80 *= __half2float(__ushort_as_half(ksc[16 * hc0 + g + 8]));
+          if constexpr (H > 1) {
+            ks1 *= __half2float(__ushort_as_half(ksc[16 * hc1 + g]));
+            ks81 *= __half2float(__ushort_as_half(ksc[16 * hc1 + g + 8]));
+          } else {
+            ks1 = ks0;
+            ks81 = ks80;
+          }
         }
-        float z0 = (sa[0] + sb[0]) * ksg, z1 = (sa[1] + sb[1]) * ksg;
-        float z2 = (sa[2] + sb[2]) * ksg8, z3 = (sa[3] + sb[3]) * ksg8;
+        float z0 = (sa[0] + sb[0]) * ks0, z1 = (sa[1] + sb[1]) * ks1;
+        float z2 = (sa[2] + sb[2]) * ks80, z3 = (sa[3] + sb[3]) * ks81;
         if (nvalid < kBlockSize) {
           if (g >= nvalid) z0 = z1 = -INFINITY;
           if (g + 8 >= nvalid) z2 = z3 = -INFINITY;
@@ -653,18 +683,32 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
         // shifts the exponents so that p' = p * 2^lg, and P' = p' * s_v < 2
         float ra = 1.f;     // O's unit change (power of two)
         int lg = 0;
-        float sv_g = 1.f, sv_g8 = 1.f;
+        float sv0 = 1.f, sv1 = 1.f, sv80 = 1.f, sv81 = 1.f;   // V scales of z0..z3
         if constexpr (INT8 && !STATIC) {
-          const uint16_t* vsc = scales_w + s * (C::kScaleBytes / 2) + kBlockSize;
-          const uint32_t vmax = redux_max_u32((lane & 15) < nvalid ? (uint32_t)vsc[lane & 15] : 0u);
+          const uint16_t* vsc = scales_w + s * (C::kScaleBytes / 2) + C::kRows;
+          uint32_t vb = 0;                       // slots (head, token) = (i / 16, i % 16)
+#pragma unroll
+          for (int i = lane & (H == 1 ? 15 : 31); i < C::kRows; i += 32)
+            if ((i & 15) < nvalid) vb = max(vb, (uint32_t)vsc[i]);
+          const uint32_t vmax = redux_max_u32(vb);
           const int eb = max((int)(vmax >> 10), 1);
           if (eb > vfb) {
             if (pg > 0) ra = exp2i(vfb - eb);   // the first page starts from O = 0
             vfb = eb;
           }
           lg = 15 - vfb;
-          sv_g = g < nvalid ? __half2float(__ushort_as_half(vsc[g])) : 0.f;
-          sv_g8 = g + 8 < nvalid ? __half2float(__ushort_as_half(vsc[g + 8])) : 0.f;
+          if (g < nvalid) {
+            sv0 = __half2float(__ushort_as_half(vsc[16 * hc0 + g]));
+            sv1 = H > 1 ? __half2float(__ushort_as_half(vsc[16 * hc1 + g])) : sv0;
+          } else {
+            sv0 = sv1 = 0.f;
+          }
+          if (g + 8 < nvalid) {
+            sv80 = __half2float(__ushort_as_half(vsc[16 * hc0 + g + 8]));
+            sv81 = H > 1 ? __half2float(__ushort_as_half(vsc[16 * hc1 + g + 8])) : sv80;
+          } else {
+            sv80 = sv81 = 0.f;
+          }
         }
         const float o0 = (float)lg - mn0, o1 = (float)lg - mn1;
         float p0, p1, p2, p3;
@@ -683,10 +727,10 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
           const float ul = exp2i(-lg);
           l0 = fmaf(p0 + p2, ul, l0 * al0);
           l1 = fmaf(p1 + p3, ul, l1 * al1);
-          p0 *= sv_g;
-          p1 *= sv_g;
-          p2 *= sv_g8;
-          p3 *= sv_g8;
+          p0 *= sv0;
+          p1 *= sv1;
+          p2 *= sv80;
+          p3 *= sv81;
         } else {
           l0 = l0 * al0 + (p0 + p2);
           l1 = l1 * al1 + (p1 + p3);
@@ -711,21 +755,26 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
         // ---------- O^T[d][head] += V^T P^T: M = 16 head-dims, N = 8 heads ----------
         if constexpr (INT8) {
           // exact codes; the V scales are in P' (tokenwise) or applied once
-          // to the output (static)
+          // to the output (static).  KV head h of the group multiplies only
+          // its own columns of P'^T (the lanes of other columns pass zeros).
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS / 2; ++kk) {
+          for (int hk = 0; hk < H * (KSTEPS / 2); ++hk) {
+            const int h = hk / (KSTEPS / 2), kk = hk % (KSTEPS / 2);
+            const uint32_t bm0 = H == 1 || hg == h ? pb0 : 0u;
+            const uint32_t bm1 = H == 1 || hg == h ? pb1 : 0u;
             uint32_t r[4];
-            ldsm_x4_trans(vt + tile_off<C>(lt, 2 * kk + (lane >> 4)), r[0], r[1], r[2], r[3]);
+            ldsm_x4_trans(vt + tile_off<C>(16 * h + lt, 2 * kk + (lane >> 4)), r[0], r[1], r[2],
+                          r[3]);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              // r[2h]: tokens 2c, 2c+1; r[2h+1]: tokens 2c+8, 2c+9; bytes
+            for (int x = 0; x < 2; ++x) {
+              // r[2x]: tokens 2c, 2c+1; r[2x+1]: tokens 2c+8, 2c+9; bytes
               // {t0 d0, t0 d1, t1 d0, t1 d1} with d0 = 16cb + 2g (row g), d1 = d0 + 1 (row g+8)
               uint32_t ev0, od0, ev1, od1;
-              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h], ev0, od0);
-              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * h + 1], ev1, od1);
-              const int cb = 2 * kk + h;
+              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * x], ev0, od0);
+              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * x + 1], ev1, od1);
+              const int cb = 2 * kk + x;
               float* oq = o + 4 * cb;
-              mma_16816_acc<false>(*reinterpret_cast<float(*)[4]>(oq), ev0, od0, ev1, od1, pb0, pb1);
+              mma_16816_acc<false>(*reinterpret_cast<float(*)[4]>(oq), ev0, od0, ev1, od1, bm0, bm1);
             }
           }
         } else {
@@ -811,5 +860,61 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC>::kMinCtas)
     }
   }
 }
+
+// Host side of one kernel variant: shared-memory size, attributes,
+// occupancy and the launch (programmatic stream serialization, so that the
+// launch may overlap the tail of the previous kernel in the stream; the
+// kernel waits (griddepcontrol) before reading any input).
+template <bool INT8, bool STATIC, int H>
+struct DecodeLaunch {
+  template <int D, bool BF16>
+  static const void* fn() {
+    return reinterpret_cast<const void*>(&paged_decode_kernel<D, INT8, BF16, STATIC, H>);
+  }
+  static const void* pick(int D, bool bf16) {
+    if (D == 128) return bf16 ? fn<128, true>() : fn<128, false>();
+    return bf16 ? fn<64, true>() : fn<64, false>();
+  }
+  static size_t smem(int D, int B, int GH) {
+    return D == 128 ? SmemLayout<128, INT8, STATIC, H>(B, GH).total_bytes
+                    : SmemLayout<64, INT8, STATIC, H>(B, GH).total_bytes;
+  }
+  static cudaError_t configure(int D, bool bf16, size_t bytes) {
+    // all of the unified L1/shared array as shared memory: the kernel's
+    // occupancy is set by its page stages
+    cudaError_t e = cudaFuncSetAttribute(pick(D, bf16), cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(pick(D, bf16), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)bytes);
+  }
+  static cudaError_t occupancy(int D, bool bf16, size_t bytes, int* n) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, pick(D, bf16), kThreads, bytes);
+  }
+  static cudaError_t launch(int D, bool bf16, const CUtensorMap* maps, const DecodeParams& p,
+                            int grid, size_t bytes, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (D == 128) {
+      return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, true, STATIC, H>,
+                                       maps[0], maps[1], p)
+                  : cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, false, STATIC, H>,
+                                       maps[0], maps[1], p);
+    }
+    return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, true, STATIC, H>,
+                                     maps[0], maps[1], p)
+                : cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, false, STATIC, H>,
+                                     maps[0], maps[1], p);
+  }
+  static constexpr DecodeOps ops() { return DecodeOps{&smem, &configure, &occupancy, &launch}; }
+};
 
 }  // namespace kvq

@@ -53,7 +53,8 @@ struct DecodeParams {
   float* part_o;            // [2 * range_cap][G][D]   (unit u, slot k -> rows (2u + k) * G)
   float* part_lse;          // [2 * range_cap][G]      (log2 domain)
   unsigned int* err;
-  int32_t B, Hq, Hkv, G;
+  int32_t B, Hq, Hkv, G;     // Hkv, G: head groups and query heads per group
+  int32_t Gr;               // query heads per KV head (G / KV heads per group)
   int32_t max_blocks;       // block-table row length
   int32_t max_ctx;          // host upper bound on context_lens
   int32_t num_blocks;
@@ -123,23 +124,28 @@ cudaError_t prefill_configure(int D, bool bf16);
 cudaError_t prefill_launch(int D, bool bf16, const CUtensorMap* maps, const PrefillParams& p,
                            int tiles, cudaStream_t s);
 
-// decode (kvq_decode_int8.cu / kvq_decode_kv16.cu); D = head_dim, smem in bytes; maps =
-// {K tiles, V tiles}.
-size_t decode_smem_bytes_int8(int D, int B, int G);
-cudaError_t decode_configure_int8(int D, bool bf16, size_t smem);
-cudaError_t decode_occupancy_int8(int D, bool bf16, size_t smem, int* n);
-cudaError_t decode_launch_int8(int D, bool bf16, const CUtensorMap* maps,
-                               const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
-size_t decode_smem_bytes_static(int D, int B, int G);
-cudaError_t decode_configure_static(int D, bool bf16, size_t smem);
-cudaError_t decode_occupancy_static(int D, bool bf16, size_t smem, int* n);
-cudaError_t decode_launch_static(int D, bool bf16, const CUtensorMap* maps,
-                                 const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
-size_t decode_smem_bytes_kv16(int D, int B, int G);
-cudaError_t decode_configure_kv16(int D, bool bf16, size_t smem);
-cudaError_t decode_occupancy_kv16(int D, bool bf16, size_t smem, int* n);
-cudaError_t decode_launch_kv16(int D, bool bf16, const CUtensorMap* maps,
-                               const DecodeParams& p, int grid, size_t smem, cudaStream_t s);
+// Head groups: KV heads one decode warp processes together (each page step
+// covers their adjacent tiles).  The launcher uses up to kMaxHeadGroup.
+#ifndef KVQ_MAX_HEAD_GROUP
+#define KVQ_MAX_HEAD_GROUP 2
+#endif
+constexpr int kMaxHeadGroup = KVQ_MAX_HEAD_GROUP;
+
+// One decode kernel variant (cache kind x head group), for head_dim 64/128
+// and FP16/BF16 activations.  D = head_dim, GH = query heads per head group,
+// smem in bytes, maps = {K tiles, V tiles}.
+struct DecodeOps {
+  size_t (*smem)(int D, int B, int GH);
+  cudaError_t (*configure)(int D, bool bf16, size_t smem);
+  cudaError_t (*occupancy)(int D, bool bf16, size_t smem, int* n);
+  cudaError_t (*launch)(int D, bool bf16, const CUtensorMap* maps, const DecodeParams& p,
+                        int grid, size_t smem, cudaStream_t s);
+};
+extern const DecodeOps kDecodeInt8H1;    // kvq_decode_int8.cu
+extern const DecodeOps kDecodeInt8H2;    // kvq_decode_int8_h2.cu
+extern const DecodeOps kDecodeStaticH1;  // kvq_decode_static.cu
+extern const DecodeOps kDecodeStaticH2;  // kvq_decode_static_h2.cu
+extern const DecodeOps kDecodeKv16;      // kvq_decode_kv16.cu
 
 // combine (kvq_combine.cu)
 cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, int sms, cudaStream_t s);

@@ -281,6 +281,15 @@ class Workload:
         return n * 2 * (2 * self.head_dim) * 2 + self.append_tokens() * 8
 
 
+def first_seqs(w: Workload, n: int) -> Workload:
+    """The workload restricted to its first n sequences (same values for
+    those sequences; block tables drawn afresh for the smaller pool)."""
+    return Workload(w.name, n, w.num_q_heads, w.num_kv_heads, w.head_dim, w.dtype,
+                    w.context_lens[:n].copy(), w.append, w.prefill_tokens, w.k_std, w.v_std,
+                    w.q_std, w.outlier_channels, w.outlier_gain, w.zero_token_frac,
+                    w.pool_factor, w.seed, w.block_size)
+
+
 def make(name: str, seed: int = 0) -> Workload:
     """The five named workloads."""
     wid = _IDS[name]
