@@ -89,9 +89,13 @@ def parse_args():
                     help="chunked-prefill timing instead of the decode bench line: one JSON "
                          "line per shape (causal attention TFLOP/s against the tensor peak)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--profile-g", type=int, default=0,
+                    help="with --profile-arm: the group-size sweep's workload for G "
+                         "(32 sequences x 4096 tokens, 8 KV heads, 8G query heads)")
+    ap.add_argument("--no-g-sweep", action="store_true")
     ap.add_argument("--profile-seqs", type=int, default=0,
                     help="with --profile-arm: only the workload's first N sequences")
-    ap.add_argument("--profile-arm", choices=["int8", "kv16"], default=None,
+    ap.add_argument("--profile-arm", choices=["int8", "kv16", "int8cc"], default=None,
                     help="profiling run: only this decode arm (one cache on the device), "
                          "warm-up + steps with L2 flushes, a short timing line; no bench line")
     return ap.parse_args()
@@ -452,6 +456,12 @@ class GpuWorkload:
         if self.k_new is not None:
             self.kvq.kvq_cache_append_kv16(self.k_new, self.v_new, self.slots, *self.kv16)
 
+    def decode_int8_cuda_cores(self):
+        w = self.w
+        self.kvq.kvq_paged_decode_cuda_cores(self.q, *self.int8, self.bt, self.cl,
+                                             w.max_context_len, w.sm_scale, out=self.out,
+                                             workspace=self.ws)
+
     def decode_kv16(self):
         w = self.w
         self.kvq.kvq_paged_decode_kv16(self.q, *self.kv16, self.bt, self.cl, w.max_context_len,
@@ -461,11 +471,13 @@ class GpuWorkload:
         return (1 if self.k_new is not None else 0) + 1 + (1 if self.split else 0)
 
 
-def arm_summary(w: W.Workload, step_ms, dec_ms, step16_ms, dec16_ms, peak) -> dict:
+def arm_summary(w: W.Workload, step_ms, dec_ms, step16_ms, dec16_ms, peak, cc_ms=None) -> dict:
     """Per-workload figures of one INT8 arm and one 16-bit-twin arm (mean
-    step and decode times in ms)."""
+    step and decode times in ms); cc_ms: the INT8 decode on the CUDA cores."""
     dec_gbs = w.decode_bytes_int8() / (dec_ms * 1e-3) / 1e9
-    return {"decode_us": round(1e3 * dec_ms, 3), "decode_gbs": round(dec_gbs, 1),
+    return {"group_size": w.group,
+            "cuda_core_decode_us": None if cc_ms is None else round(1e3 * cc_ms, 3),
+            "tensor_core_speedup": None if cc_ms is None else round(cc_ms / dec_ms, 3),"decode_us": round(1e3 * dec_ms, 3), "decode_gbs": round(dec_gbs, 1),
             "decode_pct_of_measured_peak": round(100 * dec_gbs / peak, 2),
             "decode_pct_of_nominal_8tbs": round(100 * dec_gbs / 8000.0, 2),
             "decode_bytes": w.decode_bytes_int8(),
@@ -488,10 +500,11 @@ def measure_config(torch, w: W.Workload, dev, flush, steps, warmup, peak) -> dic
     g = GpuWorkload(w, dev)
     t_step, t_dec = time_arm(torch, flush, g.append_int8, g.decode_int8, steps, warmup)
     t_step16, t_dec16 = time_arm(torch, flush, g.append_kv16, g.decode_kv16, steps, warmup)
+    _, t_cc = time_arm(torch, flush, lambda: None, g.decode_int8_cuda_cores, steps, warmup)
     del g
     torch.cuda.empty_cache()
     return arm_summary(w, *[statistics.mean(t) for t in (t_step, t_dec, t_step16, t_dec16)],
-                       peak)
+                       peak, statistics.mean(t_cc))
 
 
 def time_arm(torch, flush, append, decode, steps, warmup, settle_s=0.0):
@@ -591,6 +604,33 @@ def host_cost(torch, g: GpuWorkload, calls: int = 200) -> dict:
         torch.cuda.synchronize()
         res[name] = round(1e6 * t / calls, 2)
     res["calls"] = calls
+    return res
+
+
+def g_sweep_workload(G: int) -> W.Workload:
+    """The tensor-core A/B's workload for query-group size G: 32 sequences of
+    4096 tokens, 8 KV heads, 8 G query heads, d 128, bf16 (the same 272 MB of
+    INT8 K/V for every G)."""
+    return W.custom(32, 8 * G, 8, 128, "bf16", [4096] * 32, seed=300 + G, pool_factor=1)
+
+
+def g_sweep(torch, dev, flush, steps):
+    """The INT8 decode on the tensor cores (kvq_paged_decode) and on the CUDA
+    cores (kvq_paged_decode_cuda_cores) for G = 1, 2, 4, 8 on the same pages."""
+    res = {}
+    for G in (1, 2, 4, 8):
+        w = g_sweep_workload(G)
+        g = GpuWorkload(w, dev, arms=("int8",))
+        nop = lambda: None  # noqa: E731
+        _, tt = time_arm(torch, flush, nop, g.decode_int8, steps, 3)
+        _, tc = time_arm(torch, flush, nop, g.decode_int8_cuda_cores, steps, 3)
+        mt, mc = statistics.mean(tt), statistics.mean(tc)
+        res[str(G)] = {"tensor_core_us": round(1e3 * mt, 2), "cuda_core_us": round(1e3 * mc, 2),
+                       "tensor_core_speedup": round(mc / mt, 3),
+                       "tensor_core_gbs": round(w.decode_bytes_int8() / (mt * 1e-3) / 1e9, 1),
+                       "cuda_core_gbs": round(w.decode_bytes_int8() / (mc * 1e-3) / 1e9, 1)}
+        del g
+        torch.cuda.empty_cache()
     return res
 
 
@@ -703,15 +743,19 @@ def prefill_measure(torch, kvq, dev, flush, names, steps, warmup):
 
 def profile_arm(torch, w, dev, args):
     """One decode arm alone (for ncu captures of a bounded device footprint)."""
+    if args.profile_g:
+        w = g_sweep_workload(args.profile_g)
     if args.profile_seqs:
         w = W.first_seqs(w, args.profile_seqs)
-    g = GpuWorkload(w, dev, arms=(args.profile_arm,))
+    kv16 = args.profile_arm == "kv16"
+    g = GpuWorkload(w, dev, arms=("kv16",) if kv16 else ("int8",))
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.zero_()  # noqa: E731
     nop = lambda: None  # noqa: E731
-    dec = g.decode_int8 if args.profile_arm == "int8" else g.decode_kv16
+    dec = {"int8": g.decode_int8, "kv16": g.decode_kv16,
+           "int8cc": g.decode_int8_cuda_cores}[args.profile_arm]
     _, t = time_arm(torch, flush, nop, dec, args.steps, args.warmup)
-    nbytes = w.decode_bytes_int8() if args.profile_arm == "int8" else w.decode_bytes_kv16()
+    nbytes = w.decode_bytes_kv16() if kv16 else w.decode_bytes_int8()
     ms = statistics.mean(t)
     print(json.dumps({"profile_arm": args.profile_arm, "workload": w.name,
                       "decode_us": round(1e3 * ms, 2),
@@ -768,6 +812,8 @@ def main():
     t_e2e, h2d, d2h = time_e2e(torch, g, flush, args.steps, args.warmup)
     barrier()
     host_us = host_cost(torch, g)
+    _, t_cc = time_arm(torch, flush, lambda: None, g.decode_int8_cuda_cores, args.steps,
+                       args.warmup)
 
     step_ms, dec_ms, step16_ms, dec16_ms, e2e_ms = max_over_ranks(
         pg, dev, [statistics.mean(t) for t in (t_step, t_dec, t_step16, t_dec16, t_e2e)])
@@ -784,13 +830,17 @@ def main():
         configs = {}
         for name in W.NAMES:
             if name == w.name:
-                configs[name] = arm_summary(w, step_ms, dec_ms, step16_ms, dec16_ms, peak)
+                configs[name] = arm_summary(w, step_ms, dec_ms, step16_ms, dec16_ms, peak,
+                                            statistics.mean(t_cc))
             else:
                 configs[name] = measure_config(torch, W.make(name), dev, flush, args.steps,
                                                args.warmup, peak)
     sw = None
     if not args.no_sweep:
         sw = sweep(torch, kvq, dev, flush, max(5, min(args.steps, 20)))
+    gsw = None
+    if not args.no_g_sweep:
+        gsw = g_sweep(torch, dev, flush, max(5, min(args.steps, 20)))
     pf = None
     if not args.no_prefill:
         pf = prefill_measure(torch, kvq, dev, flush, ["8k_full_gqa8"], max(3, min(args.steps, 10)),
@@ -831,6 +881,7 @@ def main():
         "cpu_baseline": cpu,
         "configs": configs,
         "context_sweep": sw,
+        "tensor_core_ab": gsw,
         "chunked_prefill": pf,
     }
     print(json.dumps(line), flush=True)

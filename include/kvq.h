@@ -355,6 +355,27 @@ kvq_status kvq_trim_front_keep_sink(int8_t* k_cache, int8_t* v_cache, uint16_t* 
                                     const int32_t* trim, int32_t keep, kvq_stream_t stream);
 
 /*
+ * kvq_paged_decode_cuda_cores -- kvq_paged_decode with the page math on the
+ * CUDA cores: FP32 FFMA dot products over the exactly converted codes and
+ * warp-shuffle reductions, in place of the tensor-core MMAs (same pages, same
+ * work split, same arithmetic up to rounding order, same arguments, results
+ * and error behaviour).  The A/B counterpart that measures what the tensor
+ * cores gain for each query-group size; kvq_paged_decode takes the faster
+ * engine.  The computation is that of "feat: opt-in INT8 KV-cache
+ * quantization" (MoE-Infinity PR #183), "What landed".
+ */
+kvq_status kvq_paged_decode_cuda_cores(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, const int8_t* k_cache,
+                                       const int8_t* v_cache, const uint16_t* k_scale,
+                                       const uint16_t* v_scale, int32_t num_blocks,
+                                       int32_t block_size, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t max_context_len, float sm_scale, void* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       kvq_stream_t stream);
+
+/*
  * kvq_paged_decode_noalloc -- kvq_paged_decode for callers that cannot
  * allocate device memory.  The pages have no counterpart of this call; it
  * exists for hosts that own all device memory through their own pool

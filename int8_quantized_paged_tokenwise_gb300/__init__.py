@@ -30,7 +30,7 @@ __all__ = [
     "KvqError", "load", "kvq_quantize_append", "kvq_paged_decode", "kvq_paged_decode_kv16",
     "kvq_cache_append_kv16", "kvq_paged_decode_noalloc", "kvq_dequantize_window",
     "kvq_quantize_append_static", "kvq_paged_decode_static", "kvq_trim_front_keep_sink",
-    "kvq_paged_prefill", "kvq_selftest_wait_timeout",
+    "kvq_paged_prefill", "kvq_selftest_wait_timeout", "kvq_paged_decode_cuda_cores",
     "kvq_decode_workspace_bytes", "kvq_decode_partition_pages",
     "kvq_get_error", "kvq_status_string", "alloc_int8_cache", "alloc_kv16_cache",
     "HEADER_SYMBOLS", "BLOCK_SIZE", "DEVERR_SLOT", "DEVERR_BLOCK", "DEVERR_CONTEXT",
@@ -52,6 +52,7 @@ HEADER_SYMBOLS = (
     "kvq_get_error", "kvq_status_string", "kvq_version", "kvq_paged_decode_noalloc",
     "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static",
     "kvq_trim_front_keep_sink", "kvq_paged_prefill", "kvq_selftest_wait_timeout",
+    "kvq_paged_decode_cuda_cores",
 )
 
 _lib = None
@@ -84,6 +85,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
            sz]
     L.kvq_paged_decode.argtypes = dec + [vp]
     L.kvq_paged_decode_split.argtypes = dec + [i32, vp]
+    L.kvq_paged_decode_cuda_cores.argtypes = dec + [vp]
     L.kvq_paged_decode_noalloc.argtypes = dec[:-2] + [vp]
     L.kvq_paged_decode_noalloc.restype = ctypes.c_int
     dec16 = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz]
@@ -101,6 +103,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.kvq_paged_decode_static.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, f32s, f32s, i32,
                                           i32, vp, i32, vp, i32, f32s, vp, vp, sz, vp]
     for fn in ("kvq_quantize_append", "kvq_cache_append_kv16", "kvq_paged_decode",
+               "kvq_paged_decode_cuda_cores",
                "kvq_paged_decode_split", "kvq_paged_decode_kv16", "kvq_paged_decode_kv16_split",
                "kvq_dequantize_window", "kvq_quantize_append_static", "kvq_paged_decode_static",
                "kvq_trim_front_keep_sink", "kvq_paged_prefill"):
@@ -322,6 +325,29 @@ def kvq_paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_tables, contex
     else:
         st = L.kvq_paged_decode(*args, _stream(stream))
     _check(st, "kvq_paged_decode")
+    return out
+
+
+def kvq_paged_decode_cuda_cores(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                context_lens, max_context_len: int, sm_scale: float, out=None,
+                                workspace=None, stream=None):
+    """kvq_paged_decode with the page math on the CUDA cores (FFMA) instead of
+    the tensor cores: the A/B counterpart, same arguments and results."""
+    L = load()
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check_decode(q, k_cache, v_cache, block_tables, context_lens, out, (torch.int8,))
+    _check_scales(k_scale, v_scale, k_cache)
+    ws, nbytes = _workspace(q, Hkv, max_context_len, 0, workspace)
+    st = L.kvq_paged_decode_cuda_cores(_ptr(q), _dtype_code(q), B, Hq, Hkv, D, _ptr(k_cache),
+                                       _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), NB, bs,
+                                       _ptr(block_tables), block_tables.shape[1],
+                                       _ptr(context_lens), int(max_context_len),
+                                       float(sm_scale), _ptr(out), _ptr(ws), nbytes,
+                                       _stream(stream))
+    _check(st, "kvq_paged_decode_cuda_cores")
     return out
 
 

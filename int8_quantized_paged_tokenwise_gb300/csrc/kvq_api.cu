@@ -51,7 +51,7 @@ struct DeviceState {
   int sms = 0;
   unsigned int* err = nullptr;
   // occupancy cache: [variant] -> (last smem << 32) | ctas per SM
-  std::atomic<uint64_t> occ[24] = {};
+  std::atomic<uint64_t> occ[32] = {};
   std::mutex map_mu;
   MapEntry maps[kMapCache];
   int map_next = 0;
@@ -86,7 +86,7 @@ DeviceState* device_state() {
   }
   // opt every decode variant into the largest shared-memory footprint it can use
   for (const DecodeOps* ops : {&kDecodeInt8H1, &kDecodeInt8H2, &kDecodeStaticH1,
-                               &kDecodeStaticH2, &kDecodeKv16})
+                               &kDecodeStaticH2, &kDecodeKv16, &kDecodeInt8Cc})
     for (int D : {64, 128})
       for (bool bf : {false, true})
         if (ops->configure(D, bf, ops->smem(D, kMaxSeqs, kMaxGroup)) != cudaSuccess)
@@ -99,8 +99,9 @@ DeviceState* device_state() {
 }
 
 // The decode kernel variants: INT8 with per-token scale planes, INT8 with
-// static (per-tensor) scales, and the 16-bit twin.
-enum class Dec { kInt8 = 0, kStatic = 1, kKv16 = 2 };
+// static (per-tensor) scales, the 16-bit twin, and the per-token INT8 decode
+// on the CUDA cores (A/B counterpart of the tensor-core one).
+enum class Dec { kInt8 = 0, kStatic = 1, kKv16 = 2, kInt8Cc = 3 };
 
 static_assert(kMaxHeadGroup == 1 || kMaxHeadGroup == 2, "head groups of 1 or 2 KV heads");
 
@@ -108,7 +109,7 @@ static_assert(kMaxHeadGroup == 1 || kMaxHeadGroup == 2, "head groups of 1 or 2 K
 // up to kMaxHeadGroup with G H <= 8 (the MMAs' N) that divides Hkv.  The
 // 16-bit twin keeps H = 1.
 int head_group(Dec var, int32_t G, int32_t Hkv) {
-  if (var == Dec::kKv16) return 1;
+  if (var == Dec::kKv16 || var == Dec::kInt8Cc) return 1;
   int H = 1;
   while (2 * H <= kMaxHeadGroup && 2 * H * G <= kMaxGroup && Hkv % (2 * H) == 0) H *= 2;
   return H;
@@ -117,11 +118,12 @@ int head_group(Dec var, int32_t G, int32_t Hkv) {
 const DecodeOps& ops_of(Dec var, int H) {
   if (var == Dec::kInt8) return H == 2 ? kDecodeInt8H2 : kDecodeInt8H1;
   if (var == Dec::kStatic) return H == 2 ? kDecodeStaticH2 : kDecodeStaticH1;
+  if (var == Dec::kInt8Cc) return kDecodeInt8Cc;
   return kDecodeKv16;
 }
 
 int ctas_per_sm(DeviceState* st, Dec var, int H, int D, bool bf16, size_t smem) {
-  // cache slots: {int8, static, kv16} x {H 1, 2} x {D128, D64} x {fp16, bf16}
+  // cache slots: {int8, static, kv16, int8 cuda cores} x {H 1, 2} x {D128, D64} x {fp16, bf16}
   const int v = ((int)var * 2 + (H == 2 ? 1 : 0)) * 4 + (D == 128 ? 0 : 2) + (bf16 ? 1 : 0);
   const uint64_t c = st->occ[v].load(std::memory_order_relaxed);
   if ((c >> 32) == (uint64_t)smem && (c & 0xFFFFFFFFu) != 0) return (int)(c & 0xFFFFFFFFu);
@@ -194,7 +196,7 @@ int64_t balanced_units(int64_t warps, int32_t Hkv, int64_t cols_max) {
 size_t balanced_bytes_max(DeviceState* st, int32_t B, int32_t Hkv, int32_t G, int32_t D,
                           int32_t max_ctx) {
   size_t best = 0;
-  for (Dec var : {Dec::kInt8, Dec::kStatic, Dec::kKv16})
+  for (Dec var : {Dec::kInt8, Dec::kStatic, Dec::kKv16, Dec::kInt8Cc})
     for (bool bf : {false, true}) {
       const int H = head_group(var, G, Hkv);
       const int64_t w = resident_warps(st, var, D, bf, B, G, Hkv);
@@ -283,7 +285,8 @@ kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int
                          int32_t max_ctx, float sm_scale, void* out, void* ws, size_t ws_bytes,
                          int32_t R, cudaStream_t stream, float k_static = 1.f,
                          float v_static = 1.f) {
-  kvq_status s = check_decode(q, dtype, B, Hq, Hkv, D, kc, vc, ks, vs, var == Dec::kInt8,
+  kvq_status s = check_decode(q, dtype, B, Hq, Hkv, D, kc, vc, ks, vs,
+                              var == Dec::kInt8 || var == Dec::kInt8Cc,
                               num_blocks, bs, bt, max_blocks, cl, max_ctx, sm_scale, out);
   if (s != KVQ_OK || B == 0) return s;
   // the page prefix over sequences and token counts are 32-bit in the kernels
@@ -572,6 +575,22 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
                             kvq_stream_t stream) {
   return decode_common(Dec::kInt8, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
                        v_cache, k_scale, v_scale, num_blocks, block_size, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
+                       workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_paged_decode_cuda_cores(const void* q, kvq_dtype dtype, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, const int8_t* k_cache,
+                                       const int8_t* v_cache, const uint16_t* k_scale,
+                                       const uint16_t* v_scale, int32_t num_blocks,
+                                       int32_t block_size, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t max_context_len, float sm_scale, void* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       kvq_stream_t stream) {
+  return decode_common(Dec::kInt8Cc, q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       k_cache, v_cache, k_scale, v_scale, num_blocks, block_size, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, sm_scale, out,
                        workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
 }

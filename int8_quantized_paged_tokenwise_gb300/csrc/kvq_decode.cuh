@@ -187,10 +187,12 @@ __device__ __forceinline__ Piece next_piece(const WalkConst& w, const int* prefi
 // heads of the head group) and the query fragments of the MMA B operand:
 // per KV head h of the group, [k-step][lane] pairs holding the lane's column
 // if that column is one of head h's query heads, else zeros.
-template <int D, bool INT8, bool STATIC = false, int H = 1>
+template <int D, bool INT8, bool STATIC = false, int H = 1, bool CC = false>
 struct SmemLayout {
   using C = TileCfg<D, INT8, STATIC, H>;
-  static constexpr uint32_t kFragBytes = (uint32_t)H * (D / 16) * 32 * 8;
+  // CUDA-core variant (CC): FP32 queries [G][D] and P' [G][16] instead
+  static constexpr uint32_t kFragBytes =
+      CC ? (uint32_t)kMaxGroup * (D + kBlockSize) * 4 : (uint32_t)H * (D / 16) * 32 * 8;
   size_t tiles, q, qfrag, scales, bars, stage_blk, misc, walk, seq, total_bytes;
   uint32_t q_bytes;  // one piece's query rows: GH * D * 2
   __host__ __device__ SmemLayout(int B, int GH) {
@@ -214,16 +216,210 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   else return h2_as_u32(__floats2half2_rn(a, b));
 }
 
+// 16 INT8 codes (offset-binary after the XOR) -> 16 exact floats: each byte
+// u = code + 128 goes under the exponent of 2^23 (0x4B000000 + u = 2^23 + u)
+// and 2^23 + 128 is subtracted.
+__device__ __forceinline__ void i8x16_to_f32(const uint4 w, float (&f)[16]) {
+  const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u,
+                         w.w ^ 0x80808080u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      f[4 * i + b] = __uint_as_float(__byte_perm(x[i], 0x4B000000u, 0x7540u + b)) - 8388736.f;
+  }
+}
+
+// The pipeline state one piece's consumer advances.
+struct ConsumerState {
+  int cs_slot;        // stage read next
+  uint32_t cs_phase;  // parity of that wait
+  uint32_t n_done;    // pages consumed
+  int q_consumed;     // last piece whose query rows were read
+};
+
+// One piece on the CUDA cores: the counterpart of the tensor-core path for
+// A/B measurements (same pages, same walk, same outputs).  Lane (t, half)
+// forms the FP32 dot products of token t over half of the head dims for every
+// query head of the group (FFMA over exactly converted codes, the halves
+// joined by a shuffle); the online softmax runs per head over the 16 lanes of
+// a half; for P V lane l owns head dims [l E, l E + E) of every head and
+// reads the page's P' = p s_v (FP32) from shared memory.  Returns false if a
+// wait timed out.
+template <int D, bool QBF16, class Refill>
+__device__ __forceinline__ bool cc_piece(const DecodeParams& p, const Piece& it, int ord,
+                                         int lane, const uint16_t* q_raw, float* q32,
+                                         float* pbuf, uint32_t tiles_u32,
+                                         const uint16_t* scales_w, const int* blk_w,
+                                         uint32_t bars_u32, ConsumerState& cs,
+                                         Refill&& refill) {
+  using C = TileCfg<D, true>;
+  constexpr int S = C::kStages;
+  constexpr int E = D / 32;           // output dims per lane
+  constexpr int QC = D / 32;          // 16-byte K chunks per lane (half a row)
+  const int G = p.G;
+  const int t = lane & 15, half = lane >> 4;
+  float m[kMaxGroup], l[kMaxGroup], o[kMaxGroup][E];
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[g][e] = 0.f;
+  }
+  for (int pg = 0; pg < it.npg; ++pg) {
+    const int s = cs.cs_slot;
+    const uint32_t par = cs.cs_phase;
+    if (++cs.cs_slot == S) {
+      cs.cs_slot = 0;
+      cs.cs_phase ^= 1u;
+    }
+    if (!mbar_wait_bounded(bars_u32 + 8 * s, par)) return false;
+    if (pg == 0) {
+      for (int i = lane; i < G * D; i += 32) {
+        const uint16_t b = q_raw[i];
+        q32[i] = QBF16 ? __uint_as_float((uint32_t)b << 16) : __half2float(__ushort_as_half(b));
+      }
+      __syncwarp();
+      cs.q_consumed = ord;
+    }
+    const int blk = blk_w[s];
+    if (blk >= 0) {
+      const uint32_t kt = tiles_u32 + s * C::kStageBytes;
+      const uint32_t vt = kt + C::kTile;
+      const int nvalid = min(kBlockSize, it.L - (it.pg0 + pg) * kBlockSize);
+      // ---- scores: token t, all heads (the lane's half row converted once) ----
+      float kf[QC * 16];
+#pragma unroll
+      for (int cc = 0; cc < QC; ++cc) {
+        uint4 w;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                     : "r"(kt + tile_off<C>(t, half * QC + cc)));
+        i8x16_to_f32(w, *reinterpret_cast<float(*)[16]>(kf + 16 * cc));
+      }
+      float acc[kMaxGroup];
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g) {
+        acc[g] = 0.f;
+        if (g < G) {
+          const float4* qv = reinterpret_cast<const float4*>(q32 + g * D + half * QC * 16);
+#pragma unroll
+          for (int x = 0; x < QC * 4; ++x) {
+            const float4 q4 = qv[x];
+            acc[g] = fmaf(kf[4 * x], q4.x, acc[g]);
+            acc[g] = fmaf(kf[4 * x + 1], q4.y, acc[g]);
+            acc[g] = fmaf(kf[4 * x + 2], q4.z, acc[g]);
+            acc[g] = fmaf(kf[4 * x + 3], q4.w, acc[g]);
+          }
+        }
+      }
+      const bool valid = t < nvalid;
+      const float ks = p.scale_log2 * __half2float(__ushort_as_half(scales_w[s * (C::kScaleBytes / 2) + t]));
+      const float sv =
+          valid ? __half2float(__ushort_as_half(scales_w[s * (C::kScaleBytes / 2) + kBlockSize + t]))
+                : 0.f;
+      // ---- online softmax per head over the 16 tokens of a half ----
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g) {
+        if (g < G) {
+          const float a = acc[g] + __shfl_xor_sync(0xFFFFFFFFu, acc[g], 16);
+          const float z = valid ? a * ks : -INFINITY;
+          float mx = z;
+#pragma unroll
+          for (int off = 1; off < 16; off <<= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+          const float mn = fmaxf(m[g], mx);
+          const float al = fast_exp2(m[g] - mn);
+          const float pz = fast_exp2(z - mn);
+          float ps = pz;
+#pragma unroll
+          for (int off = 1; off < 16; off <<= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
+          l[g] = l[g] * al + ps;
+          m[g] = mn;
+          if (al != 1.f) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[g][e] *= al;
+          }
+          if (half == 0) pbuf[g * kBlockSize + t] = pz * sv;
+        }
+      }
+      __syncwarp();
+      // ---- P V: head dims [lane E, lane E + E) of every head ----
+      const int d0 = lane * E;
+      for (int tt = 0; tt < nvalid; ++tt) {
+        const uint32_t a = vt + tile_off<C>(tt, d0 / 16) + (d0 % 16);
+        float v[E];
+        if constexpr (E == 4) {
+          uint32_t w;
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(a));
+          w ^= 0x80808080u;
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            v[b] = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + b)) - 8388736.f;
+        } else {
+          uint16_t w;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(w) : "r"(a));
+          const uint32_t x = (uint32_t)w ^ 0x8080u;
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+            v[b] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + b)) - 8388736.f;
+        }
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g) {
+          if (g < G) {
+            const float pp = pbuf[g * kBlockSize + tt];
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[g][e] = fmaf(pp, v[e], o[g][e]);
+          }
+        }
+      }
+      __syncwarp();   // P' is rewritten by the next page
+    }
+    ++cs.n_done;
+    __syncwarp();
+    refill();
+  }
+  // ---- the whole sequence's output, or a partial for the combine ----
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    if (g < G) {
+      const float inv = l[g] > 0.f ? 1.f / l[g] : 0.f;
+      const int64_t hrow = (int64_t)it.b * p.Hq + (int64_t)it.j * G + g;
+      if (it.flags & 1) {
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + hrow * D + lane * E;
+        if constexpr (E == 4)
+          *reinterpret_cast<uint2*>(dst) = make_uint2(pack2<QBF16>(o[g][0] * inv, o[g][1] * inv),
+                                                       pack2<QBF16>(o[g][2] * inv, o[g][3] * inv));
+        else
+          *reinterpret_cast<uint32_t*>(dst) = pack2<QBF16>(o[g][0] * inv, o[g][1] * inv);
+      } else {
+        const int64_t prow = (2 * (int64_t)it.unit + (it.flags >> 1)) * G + g;
+        float* dst = p.part_o + prow * D + lane * E;
+        if constexpr (E == 4)
+          *reinterpret_cast<float4*>(dst) =
+              make_float4(o[g][0] * inv, o[g][1] * inv, o[g][2] * inv, o[g][3] * inv);
+        else
+          *reinterpret_cast<float2*>(dst) = make_float2(o[g][0] * inv, o[g][1] * inv);
+        if (lane == 0) p.part_lse[prow] = l[g] > 0.f ? m[g] + __log2f(l[g]) : -INFINITY;
+      }
+    }
+  }
+  return true;
+}
+
 // INT8: QBF16 = activations are bf16 (converted to FP16 for the tensor cores);
 // twin: QBF16 selects the bf16 MMA, otherwise FP16.  H: KV heads per head
 // group; the walk sees p.Hkv = Hkv / H groups of p.G = G H query heads each
 // (p.Gr = G), the group's query heads being consecutive.
-template <int D, bool INT8, bool QBF16, bool STATIC = false, int H = 1>
-__global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCtas)
+// CC: the page math on the CUDA cores (cc_piece), for A/B measurements.
+template <int D, bool INT8, bool QBF16, bool STATIC = false, int H = 1, bool CC = false>
+__global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>::kMinCtas)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
   using C = TileCfg<D, INT8, STATIC, H>;
-  using Lay = SmemLayout<D, INT8, STATIC, H>;
+  using Lay = SmemLayout<D, INT8, STATIC, H, CC>;
+  static_assert(!CC || (INT8 && !STATIC && H == 1), "the CUDA-core variant is tokenwise INT8");
   const Lay lay(p.B, p.G);
   static_assert(INT8 || H == 1, "head groups are built for the INT8 cache");
   constexpr bool MMA_BF16 = (!INT8) && QBF16;
@@ -393,16 +589,17 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
   // current 32-page chunk live one per lane (blk_cur); the first chunk of the
   // following piece is prefetched into blk_nxt.
   int is_ord = 0, is_pg = 0, is_chunk = 0;
-  int q_issued = -1, q_consumed = -1;   // ordinals: last piece whose query was copied / read
+  int q_issued = -1;                    // ordinal of the last piece whose query was copied
+  // consumer side: next stage and its parity, pages consumed, last piece
+  // whose query rows were read
+  ConsumerState cs{0, 0u, 0u, -1};
   WarpWalk& ww = wwalk[warp];
   // the issuer's piece (the fields the page issue needs); the following
   // piece's descriptor is in ww.ring and its first block-id chunk in blk_nxt
   int is_b = 0, is_j = 0, is_pg0 = 0, is_npg = 0;
   int blk_cur = -1, blk_nxt = -1;
-  uint32_t n_issued = 0, n_done = 0;
+  uint32_t n_issued = 0;
   int is_slot = 0;                       // stage the next issued page goes to
-  int cs_slot = 0;                       // stage the consumer reads next
-  uint32_t cs_phase = 0;                 // parity of that wait (flips each pass over the ring)
 
   auto load_chunk = [&](int b, int pg0, int npg, int base) -> int {
     const int pg = base + lane;
@@ -451,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
   // also copies the piece's query rows into the single raw query slot) waits
   // until the previously copied query rows have been read by the consumer.
   auto refill = [&]() {
-    while (n_issued - n_done < (uint32_t)S) {
+    while (n_issued - cs.n_done < (uint32_t)S) {
       if (is_npg > 0 && is_pg >= is_npg) {   // next piece (pieces have pages)
         ++is_ord;
         const Piece& nx = ww.ring[is_ord & 3];
@@ -464,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
         blk_cur = blk_nxt;
         if (is_npg > 0) blk_nxt = walk_next(is_ord + 1);
       }
-      if (is_npg == 0 || (is_pg == 0 && q_issued > q_consumed)) return;
+      if (is_npg == 0 || (is_pg == 0 && q_issued > cs.q_consumed)) return;
       if (is_pg >= is_chunk + 32) {
         is_chunk += 32;
         blk_cur = load_chunk(is_b, is_pg0, is_npg, is_chunk);
@@ -510,6 +707,18 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
     const int it_npg = ww.ring[ord & 3].npg;
     if (it_npg == 0) break;
     const int it_pg0 = ww.ring[ord & 3].pg0, it_L = ww.ring[ord & 3].L;
+    if constexpr (CC) {
+      const uint16_t* q_raw =
+          reinterpret_cast<const uint16_t*>(smem + lay.q) + (size_t)warp * (lay.q_bytes / 2);
+      float* q32 = reinterpret_cast<float*>(smem + lay.qfrag + (size_t)warp * Lay::kFragBytes);
+      const Piece piece = ww.ring[ord & 3];
+      if (!cc_piece<D, QBF16>(p, piece, ord, lane, q_raw, q32, q32 + kMaxGroup * D, tiles_u32,
+                              scales_w, blk_w, bars_u32, cs, refill)) {
+        aborted = true;
+        break;
+      }
+      continue;
+    }
     // Running softmax state of the two query heads this thread's columns hold
     // (heads 2c and 2c+1 of the KV head's group), and the output accumulator
     // O^T[d][head]: o[4cb + e] for 16-wide head-dim block cb, e = (row, col)
@@ -530,11 +739,11 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
     int vfb = 0;
 
     for (int pg = 0; pg < it_npg; ++pg) {
-      const int s = cs_slot;
-      const uint32_t par = cs_phase;
-      if (++cs_slot == S) {
-        cs_slot = 0;
-        cs_phase ^= 1u;
+      const int s = cs.cs_slot;
+      const uint32_t par = cs.cs_phase;
+      if (++cs.cs_slot == S) {
+        cs.cs_slot = 0;
+        cs.cs_phase ^= 1u;
       }
       if (!mbar_wait_bounded(bars_u32 + 8 * s, par)) {
         aborted = true;
@@ -592,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
             qfrag[(h * KSTEPS + ks) * 32 + lane] = h == hg ? f : make_uint2(0u, 0u);
         }
         __syncwarp();   // the raw query slot may be refilled once every lane is done
-        q_consumed = ord;
+        cs.q_consumed = ord;
       }
       const int blk = blk_w[s];
       if (blk >= 0) {
@@ -790,7 +999,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
           }
         }
       }
-      ++n_done;
+      ++cs.n_done;
       __syncwarp();
       refill();
     }
@@ -848,10 +1057,10 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
     // A wait gave up: record it, then wait (bounded) for this warp's copies
     // still in flight so that none lands after the CTA has exited.
     if (lane == 0) atomicOr(p.err, 0x8u);
-    // the failed wait's stage is the one before cs_slot (cs_slot/cs_phase advanced)
-    int s = cs_slot == 0 ? S - 1 : cs_slot - 1;
-    uint32_t ph = cs_slot == 0 ? (cs_phase ^ 1u) : cs_phase;
-    for (; n_done < n_issued; ++n_done) {
+    // the failed wait's stage is the one before cs.cs_slot (cs.cs_slot/cs.cs_phase advanced)
+    int s = cs.cs_slot == 0 ? S - 1 : cs.cs_slot - 1;
+    uint32_t ph = cs.cs_slot == 0 ? (cs.cs_phase ^ 1u) : cs.cs_phase;
+    for (; cs.n_done < n_issued; ++cs.n_done) {
       mbar_wait_bounded(bars_u32 + 8 * s, ph);
       if (++s == S) {
         s = 0;
@@ -865,19 +1074,19 @@ __global__ void __launch_bounds__(kThreads, TileCfg<D, INT8, STATIC, H>::kMinCta
 // occupancy and the launch (programmatic stream serialization, so that the
 // launch may overlap the tail of the previous kernel in the stream; the
 // kernel waits (griddepcontrol) before reading any input).
-template <bool INT8, bool STATIC, int H>
+template <bool INT8, bool STATIC, int H, bool CC = false>
 struct DecodeLaunch {
   template <int D, bool BF16>
   static const void* fn() {
-    return reinterpret_cast<const void*>(&paged_decode_kernel<D, INT8, BF16, STATIC, H>);
+    return reinterpret_cast<const void*>(&paged_decode_kernel<D, INT8, BF16, STATIC, H, CC>);
   }
   static const void* pick(int D, bool bf16) {
     if (D == 128) return bf16 ? fn<128, true>() : fn<128, false>();
     return bf16 ? fn<64, true>() : fn<64, false>();
   }
   static size_t smem(int D, int B, int GH) {
-    return D == 128 ? SmemLayout<128, INT8, STATIC, H>(B, GH).total_bytes
-                    : SmemLayout<64, INT8, STATIC, H>(B, GH).total_bytes;
+    return D == 128 ? SmemLayout<128, INT8, STATIC, H, CC>(B, GH).total_bytes
+                    : SmemLayout<64, INT8, STATIC, H, CC>(B, GH).total_bytes;
   }
   static cudaError_t configure(int D, bool bf16, size_t bytes) {
     // all of the unified L1/shared array as shared memory: the kernel's
@@ -904,14 +1113,14 @@ struct DecodeLaunch {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (D == 128) {
-      return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, true, STATIC, H>,
+      return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, true, STATIC, H, CC>,
                                        maps[0], maps[1], p)
-                  : cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, false, STATIC, H>,
+                  : cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, false, STATIC, H, CC>,
                                        maps[0], maps[1], p);
     }
-    return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, true, STATIC, H>,
+    return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, true, STATIC, H, CC>,
                                      maps[0], maps[1], p)
-                : cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, false, STATIC, H>,
+                : cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, false, STATIC, H, CC>,
                                      maps[0], maps[1], p);
   }
   static constexpr DecodeOps ops() { return DecodeOps{&smem, &configure, &occupancy, &launch}; }

@@ -146,6 +146,7 @@ extern const DecodeOps kDecodeInt8H2;    // kvq_decode_int8_h2.cu
 extern const DecodeOps kDecodeStaticH1;  // kvq_decode_static.cu
 extern const DecodeOps kDecodeStaticH2;  // kvq_decode_static_h2.cu
 extern const DecodeOps kDecodeKv16;      // kvq_decode_kv16.cu
+extern const DecodeOps kDecodeInt8Cc;    // kvq_decode_int8_cc.cu (CUDA cores, A/B)
 
 // combine (kvq_combine.cu)
 cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, int sms, cudaStream_t s);

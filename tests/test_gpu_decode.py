@@ -111,6 +111,27 @@ def test_decode_ragged_contexts_every_partition_size(Hq, Hkv, D, dtype):
     assert kvq.kvq_get_error() == (0, 0)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [(4, 4, 128, "fp16"), (8, 4, 64, "bf16"),
+                                            (32, 8, 128, "bf16"), (16, 2, 128, "bf16"),
+                                            (12, 4, 64, "fp16")])
+def test_decode_cuda_cores_matches_oracle(Hq, Hkv, D, dtype):
+    """The CUDA-core engine (the tensor cores' A/B counterpart) over ragged
+    contexts, G in {1, 2, 3, 4, 8}: split-K with the recommended workspace and
+    one range per sequence without one."""
+    w = W.custom(len(RAGGED), Hq, Hkv, D, dtype, RAGGED, seed=Hq * 11 + D + 5)
+    case = Case(w)
+    case.write_prefix()
+    out = kvq.kvq_paged_decode_cuda_cores(case.q, *case.int8, case.bt, case.cl,
+                                          w.max_context_len, w.sm_scale)
+    _check_all(case, out, what="cuda cores")
+    assert bool((out[0] == 0).all())
+    none = torch.empty(0, dtype=torch.uint8, device="cuda")
+    out = kvq.kvq_paged_decode_cuda_cores(case.q, *case.int8, case.bt, case.cl,
+                                          w.max_context_len, w.sm_scale, workspace=none)
+    _check_all(case, out, what="cuda cores, no workspace")
+    assert kvq.kvq_get_error() == (0, 0)
+
+
 def test_decode_single_token_returns_v():
     w = W.custom(3, 8, 2, 128, "bf16", [1, 1, 1], seed=3)
     case = Case(w)

@@ -49,6 +49,10 @@ def _decode_vs_oracle(w, seqs, q_bits, sm_scale, v_scale=1.0, parts=(0, 4), what
                                            sm_scale, partition_pages=P))
         for b in range(w.num_seqs):
             assert_attention_close(ob[b], refs[b], w.dtype, f"{what} P={P} seq {b}", v_scale)
+    ob = out_bits(kvq.kvq_paged_decode_cuda_cores(q, *case.int8, case.bt, case.cl,
+                                                  w.max_context_len, sm_scale))
+    for b in range(w.num_seqs):
+        assert_attention_close(ob[b], refs[b], w.dtype, f"{what} cuda cores seq {b}", v_scale)
     assert kvq.kvq_get_error() == (0, 0)
 
 
