@@ -53,7 +53,8 @@ UNIT = "GB/s"
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
 # the kernels whose DRAM traffic the committed ncu summaries measured
-DECODE_SOURCES = ("kvq_decode.cuh", "kvq_decode_int8.cu", "kvq_ptx.cuh", "kvq_combine.cu")
+DECODE_SOURCES = ("kvq_decode.cuh", "kvq_decode_int8.cu", "kvq_decode_int8_h2.cu",
+                  "kvq_decode_int8_t2.cu", "kvq_ptx.cuh", "kvq_combine.cu")
 HEADLINE = "mha"
 
 

@@ -86,7 +86,7 @@ DeviceState* device_state() {
   }
   // opt every decode variant into the largest shared-memory footprint it can use
   for (const DecodeOps* ops : {&kDecodeInt8H1, &kDecodeInt8H2, &kDecodeStaticH1,
-                               &kDecodeStaticH2, &kDecodeKv16, &kDecodeInt8Cc})
+                               &kDecodeStaticH2, &kDecodeKv16, &kDecodeInt8Cc, &kDecodeInt8T2})
     for (int D : {64, 128})
       for (bool bf : {false, true})
         if (ops->configure(D, bf, ops->smem(D, kMaxSeqs, kMaxGroup)) != cudaSuccess)
@@ -115,20 +115,41 @@ int head_group(Dec var, int32_t G, int32_t Hkv) {
   return H;
 }
 
-const DecodeOps& ops_of(Dec var, int H) {
-  if (var == Dec::kInt8) return H == 2 ? kDecodeInt8H2 : kDecodeInt8H1;
-  if (var == Dec::kStatic) return H == 2 ? kDecodeStaticH2 : kDecodeStaticH1;
-  if (var == Dec::kInt8Cc) return kDecodeInt8Cc;
-  return kDecodeKv16;
+// Pages one decode warp step covers: two for the per-token INT8 decode with
+// one KV head per step (G > 4), so that each step's fixed work covers two
+// page tiles there too; else one.
+int pages_per_step(Dec var, int H) {
+  return var == Dec::kInt8 && H == 1 && kMaxPageStep >= 2 ? 2 : 1;
 }
 
-int ctas_per_sm(DeviceState* st, Dec var, int H, int D, bool bf16, size_t smem) {
-  // cache slots: {int8, static, kv16, int8 cuda cores} x {H 1, 2} x {D128, D64} x {fp16, bf16}
-  const int v = ((int)var * 2 + (H == 2 ? 1 : 0)) * 4 + (D == 128 ? 0 : 2) + (bf16 ? 1 : 0);
+// The kernel variant of (cache kind, head group, pages per step), and its
+// index among the variants (occupancy cache).
+const DecodeOps& ops_of(Dec var, int H, int T, int* vid = nullptr) {
+  int v = 4;
+  const DecodeOps* o = &kDecodeKv16;
+  if (var == Dec::kInt8) {
+    v = T == 2 ? 6 : (H == 2 ? 1 : 0);
+    o = T == 2 ? &kDecodeInt8T2 : (H == 2 ? &kDecodeInt8H2 : &kDecodeInt8H1);
+  } else if (var == Dec::kStatic) {
+    v = H == 2 ? 3 : 2;
+    o = H == 2 ? &kDecodeStaticH2 : &kDecodeStaticH1;
+  } else if (var == Dec::kInt8Cc) {
+    v = 5;
+    o = &kDecodeInt8Cc;
+  }
+  if (vid) *vid = v;
+  return *o;
+}
+
+int ctas_per_sm(DeviceState* st, Dec var, int H, int T, int D, bool bf16, size_t smem) {
+  // cache slots: 7 variants x {D128, D64} x {fp16, bf16}
+  int vid = 0;
+  const DecodeOps& ops = ops_of(var, H, T, &vid);
+  const int v = vid * 4 + (D == 128 ? 0 : 2) + (bf16 ? 1 : 0);
   const uint64_t c = st->occ[v].load(std::memory_order_relaxed);
   if ((c >> 32) == (uint64_t)smem && (c & 0xFFFFFFFFu) != 0) return (int)(c & 0xFFFFFFFFu);
   int n = 0;
-  if (ops_of(var, H).occupancy(D, bf16, smem, &n) != cudaSuccess || n <= 0) return 0;
+  if (ops.occupancy(D, bf16, smem, &n) != cudaSuccess || n <= 0) return 0;
   st->occ[v].store(((uint64_t)smem << 32) | (uint32_t)n, std::memory_order_relaxed);
   return n;
 }
@@ -176,9 +197,9 @@ int64_t ranges_for_bytes(int32_t B, int32_t G, int32_t D, size_t bytes) {
 // on failure).
 int64_t resident_warps(DeviceState* st, Dec var, int D, bool bf16, int32_t B, int32_t G,
                        int32_t Hkv) {
-  const int H = head_group(var, G, Hkv);
-  const size_t smem = ops_of(var, H).smem(D, B, G * H);
-  return (int64_t)st->sms * ctas_per_sm(st, var, H, D, bf16, smem) * kWarps;
+  const int H = head_group(var, G, Hkv), T = pages_per_step(var, H);
+  const size_t smem = ops_of(var, H, T).smem(D, B, G * H);
+  return (int64_t)st->sms * ctas_per_sm(st, var, H, T, D, bf16, smem) * kWarps;
 }
 
 // Work units of the balanced split for a grid of `warps` warps: one range
@@ -299,11 +320,11 @@ kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int
   const int32_t Gr = Hq / Hkv;
   // the kernel walks head groups of H KV heads: HU groups of G = Gr H query
   // heads each (the group's query heads are consecutive)
-  const int H = head_group(var, Gr, Hkv);
+  const int H = head_group(var, Gr, Hkv), T = pages_per_step(var, H);
   const int32_t HU = Hkv / H, G = Gr * H;
-  const DecodeOps& ops = ops_of(var, H);
+  const DecodeOps& ops = ops_of(var, H, T);
   const size_t smem = ops.smem(D, B, G);
-  const int occ = ctas_per_sm(st, var, H, D, bf16, smem);
+  const int occ = ctas_per_sm(st, var, H, T, D, bf16, smem);
   if (occ <= 0) return cuda_fail();
   const int64_t slots = (int64_t)st->sms * occ;      // CTAs of a full persistent grid
   const int64_t cols = columns_max(B, max_ctx);

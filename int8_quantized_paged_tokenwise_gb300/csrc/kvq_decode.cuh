@@ -57,21 +57,26 @@ namespace kvq {
 // H: KV heads processed together (a "head group"): the (page, head) tiles of
 // H consecutive KV heads of a block are adjacent in the cache, so one copy
 // brings the group's H tiles (16 H token rows) and its H scale rows.
-template <int D, bool INT8, bool STATIC = false, int H = 1>
+// T: pages processed together (a step covers T consecutive pages of the
+// group, each brought by its own copies).  H T <= 2.
+template <int D, bool INT8, bool STATIC = false, int H = 1, int T = 1>
 struct TileCfg {
   static constexpr int kElem = INT8 ? 1 : 2;                 // bytes per cache element
   static constexpr int kRowBytes = D * kElem;                // bytes per token row
   static constexpr int kSubRow = kRowBytes < 128 ? kRowBytes : 128;   // TMA box row bytes
-  static constexpr int kSubTiles = kRowBytes / kSubRow;       // TMA copies per tile
-  static constexpr int kRows = H * kBlockSize;                // token rows of a group tile
+  static constexpr int kSubTiles = kRowBytes / kSubRow;       // TMA copies per page tile
+  static constexpr int kPageRows = H * kBlockSize;            // token rows of one page's tiles
+  static constexpr int kRows = T * kPageRows;                 // token rows of a step
   static constexpr int kSubBytes = kRows * kSubRow;
-  static constexpr int kTile = kRows * kRowBytes;             // bytes of one K (or V) group tile
-  static constexpr int kStages = INT8 ? KVQ_INT8_STAGES : 2;  // pages in flight per warp
+  static constexpr int kTile = kRows * kRowBytes;             // bytes of a step's K (or V) tiles
+  static constexpr int kStages = INT8 ? KVQ_INT8_STAGES : 2;  // steps in flight per warp
   static constexpr int kStageBytes = 2 * kTile;               // K tiles then V tiles
   static constexpr int kScaleBytes = INT8 && !STATIC ? 2 * kRows * 2 : 0;  // K, V scale rows
-  static constexpr uint32_t kTxBytes = 2 * kTile + kScaleBytes;
+  // bytes one page brings: its K and V tiles and scale rows
+  static constexpr uint32_t kPageTx = 2 * kPageRows * kRowBytes + kScaleBytes / T;
   static constexpr uint32_t kSwzMask = kSubRow == 128 ? 0x70u : 0x30u;
-  static constexpr int kMinCtas = INT8 ? (H == 1 ? KVQ_INT8_MIN_CTAS : 3) : 3;
+  static constexpr int kMinCtas = INT8 ? (H * T == 1 ? KVQ_INT8_MIN_CTAS : 3) : 3;
+  static_assert(H * T <= 2, "steps of at most two page tiles");
 };
 
 // Byte offset inside a (K or V) tile of 16-byte chunk `c` of token row `t`,
@@ -187,9 +192,9 @@ __device__ __forceinline__ Piece next_piece(const WalkConst& w, const int* prefi
 // heads of the head group) and the query fragments of the MMA B operand:
 // per KV head h of the group, [k-step][lane] pairs holding the lane's column
 // if that column is one of head h's query heads, else zeros.
-template <int D, bool INT8, bool STATIC = false, int H = 1, bool CC = false>
+template <int D, bool INT8, bool STATIC = false, int H = 1, bool CC = false, int T = 1>
 struct SmemLayout {
-  using C = TileCfg<D, INT8, STATIC, H>;
+  using C = TileCfg<D, INT8, STATIC, H, T>;
   // CUDA-core variant (CC): FP32 queries [G][D] and P' [G][16] instead
   static constexpr uint32_t kFragBytes =
       CC ? (uint32_t)kMaxGroup * (D + kBlockSize) * 4 : (uint32_t)H * (D / 16) * 32 * 8;
@@ -203,7 +208,7 @@ struct SmemLayout {
     scales = qfrag + (size_t)kWarps * kFragBytes;
     bars = (scales + (size_t)kWarps * C::kStages * C::kScaleBytes + 15) & ~(size_t)15;
     stage_blk = bars + (size_t)kWarps * C::kStages * 8;
-    misc = stage_blk + (size_t)kWarps * C::kStages * 4;   // 4 ints (scan of warp sums)
+    misc = stage_blk + (size_t)kWarps * C::kStages * T * 4;   // 4 ints (scan of warp sums)
     walk = (misc + 16 + 15) & ~(size_t)15;                 // WalkConst, then per warp WarpWalk
     seq = walk + sizeof(WalkConst) + (size_t)kWarps * sizeof(WarpWalk);   // page prefix, lengths
     total_bytes = seq + (size_t)B * 8 + 1024;        // + alignment slack of the base
@@ -413,13 +418,16 @@ __device__ __forceinline__ bool cc_piece(const DecodeParams& p, const Piece& it,
 // group; the walk sees p.Hkv = Hkv / H groups of p.G = G H query heads each
 // (p.Gr = G), the group's query heads being consecutive.
 // CC: the page math on the CUDA cores (cc_piece), for A/B measurements.
-template <int D, bool INT8, bool QBF16, bool STATIC = false, int H = 1, bool CC = false>
-__global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>::kMinCtas)
+// T: pages per step (1, or 2 with H = 1).
+template <int D, bool INT8, bool QBF16, bool STATIC = false, int H = 1, bool CC = false,
+          int T = 1>
+__global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H, T>::kMinCtas)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
-  using C = TileCfg<D, INT8, STATIC, H>;
-  using Lay = SmemLayout<D, INT8, STATIC, H, CC>;
-  static_assert(!CC || (INT8 && !STATIC && H == 1), "the CUDA-core variant is tokenwise INT8");
+  using C = TileCfg<D, INT8, STATIC, H, T>;
+  using Lay = SmemLayout<D, INT8, STATIC, H, CC, T>;
+  static_assert(!CC || (INT8 && !STATIC && H == 1 && T == 1),
+                "the CUDA-core variant is tokenwise INT8, one page per step");
   const Lay lay(p.B, p.G);
   static_assert(INT8 || H == 1, "head groups are built for the INT8 cache");
   constexpr bool MMA_BF16 = (!INT8) && QBF16;
@@ -568,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
   const uint16_t* scales_w =
       reinterpret_cast<const uint16_t*>(smem + lay.scales) + warp * S * (C::kScaleBytes / 2);
   const uint32_t bars_u32 = smem_u32(&bars[warp * S]);
-  int* blk_w = stage_blk + warp * S;
+  int* blk_w = stage_blk + warp * S * T;   // per stage: the T pages' block ids
 
   // Each page arrives as copies issued together by lanes 0..3: 2-D tensor TMA
   // of the K and V tiles (16-bit tiles in 128-byte-wide sub-tiles; a tiled
@@ -576,13 +584,24 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
   // and, for INT8, 1-D bulk copies of the K and V scale rows (16-byte aligned
   // destinations).  Per lane: tensor map, x coordinate and destination (+ the
   // per-stage stride), or the scale plane and destination.
+  // Lanes [0, T * kTensorCopies): page lane / kTensorCopies, copy lane %
+  // kTensorCopies (K sub-tiles, then V sub-tiles); the next 2 T lanes: page
+  // (lane - base) / 2, K or V scale row; lane kQLane: the query rows.
   constexpr int kTensorCopies = 2 * C::kSubTiles;
-  const CUtensorMap* cp_map = lane < C::kSubTiles ? &tmK : &tmV;
-  const int cp_sub = lane % C::kSubTiles;               // 128-byte column block
+  constexpr int kScaleLanes = INT8 && !STATIC ? 2 * T : 0;
+  constexpr int kQLane = T * kTensorCopies + kScaleLanes;
+  const int cp_i = lane % kTensorCopies;
+  const int cp_page = lane < T * kTensorCopies ? lane / kTensorCopies
+                      : (lane - T * kTensorCopies) / 2;       // page of this lane's copy
+  const CUtensorMap* cp_map = cp_i < C::kSubTiles ? &tmK : &tmV;
+  const int cp_sub = cp_i % C::kSubTiles;               // 128-byte column block
   const int cp_x = cp_sub * (C::kSubRow / C::kElem);
-  const uint32_t cp_dst = tiles_u32 + (lane < C::kSubTiles ? 0 : C::kTile) + cp_sub * C::kSubBytes;
-  const uint16_t* sc_src = lane == kTensorCopies ? p.k_scale : p.v_scale;
-  const uint32_t sc_dst = scales_u32 + (lane == kTensorCopies ? 0 : C::kRows * 2);
+  const uint32_t cp_dst = tiles_u32 + (cp_i < C::kSubTiles ? 0 : C::kTile) + cp_sub * C::kSubBytes +
+                          cp_page * C::kPageRows * C::kSubRow;
+  const int sc_kind = (lane - T * kTensorCopies) & 1;   // 0: K scales, 1: V scales
+  const uint16_t* sc_src = sc_kind == 0 ? p.k_scale : p.v_scale;
+  const uint32_t sc_dst =
+      scales_u32 + (sc_kind == 0 ? 0 : C::kRows * 2) + cp_page * C::kPageRows * 2;
 
   // ---------------------------------------------------------------- issuer
   // Warp-uniform state; lanes 0..5 perform the copies.  The block ids of the
@@ -666,35 +685,45 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
         is_chunk += 32;
         blk_cur = load_chunk(is_b, is_pg0, is_npg, is_chunk);
       }
-      const int blk = __shfl_sync(0xFFFFFFFFu, blk_cur, is_pg - is_chunk);
+      // the step's T pages (T divides 32, so they share the chunk); a page
+      // past the piece reads as -1 from load_chunk
+      int blk_p[T];
+#pragma unroll
+      for (int pp = 0; pp < T; ++pp)
+        blk_p[pp] = __shfl_sync(0xFFFFFFFFu, blk_cur, is_pg + pp - is_chunk);
       const int s = is_slot;
       is_slot = is_slot + 1 == S ? 0 : is_slot + 1;
       const uint32_t bar = bars_u32 + 8 * s;
       const uint32_t qbytes = is_pg == 0 ? lay.q_bytes : 0u;
       if (lane == 0) {
-        blk_w[s] = blk;
-        if (blk >= 0) mbar_arrive_expect_tx(bar, C::kTxBytes + qbytes);
-        else if (qbytes) mbar_arrive_expect_tx(bar, qbytes);
+        uint32_t tx = qbytes;
+#pragma unroll
+        for (int pp = 0; pp < T; ++pp) {
+          blk_w[T * s + pp] = blk_p[pp];
+          if (blk_p[pp] >= 0) tx += C::kPageTx;
+        }
+        if (tx) mbar_arrive_expect_tx(bar, tx);
         else mbar_arrive(bar);
       }
+      const int blk = T == 1 || cp_page != 1 ? blk_p[0] : blk_p[T - 1];
       if (blk >= 0) {
         const int row = blk * Hkv + is_j;             // (block, head group) tile index
-        if (lane < kTensorCopies) {
-          tma_load_2d_evict_first(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * C::kRows,
+        if (lane < T * kTensorCopies) {
+          tma_load_2d_evict_first(cp_dst + s * C::kStageBytes, cp_map, cp_x, row * C::kPageRows,
                                   bar);
-        } else if (INT8 && !STATIC && lane < kTensorCopies + 2) {
-          bulk_load(sc_dst + s * C::kScaleBytes, sc_src + (int64_t)row * C::kRows,
-                    C::kRows * 2, bar);
+        } else if (lane < kQLane) {
+          bulk_load(sc_dst + s * C::kScaleBytes, sc_src + (int64_t)row * C::kPageRows,
+                    C::kPageRows * 2, bar);
         }
       }
-      if (qbytes && lane == 4) {
+      if (qbytes && lane == kQLane) {
         const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) +
                                ((int64_t)is_b * p.Hq + (int64_t)is_j * G) * D;
         bulk_load(q_u32, qsrc, qbytes, bar);
       }
       if (is_pg == 0) q_issued = is_ord;
       ++n_issued;
-      ++is_pg;
+      is_pg += T;
     }
   };
   refill();
@@ -738,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
     // O accumulates in units of 2^(vfb - 15) and is rescaled when vfb grows.
     int vfb = 0;
 
-    for (int pg = 0; pg < it_npg; ++pg) {
+    for (int pg = 0; pg < it_npg; pg += T) {
       const int s = cs.cs_slot;
       const uint32_t par = cs.cs_phase;
       if (++cs.cs_slot == S) {
@@ -803,36 +832,52 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
         __syncwarp();   // the raw query slot may be refilled once every lane is done
         cs.q_consumed = ord;
       }
-      const int blk = blk_w[s];
-      if (blk >= 0) {
+      // the step's T pages: valid tokens of each (0 when the page is absent)
+      int nv[T];
+      bool any = false;
+#pragma unroll
+      for (int pp = 0; pp < T; ++pp) {
+        nv[pp] = blk_w[T * s + pp] >= 0
+                     ? min(kBlockSize, it_L - (it_pg0 + pg + pp) * kBlockSize) : 0;
+        any |= nv[pp] > 0;
+      }
+      if (any) {
         const uint32_t kt = tiles_u32 + s * C::kStageBytes;
         const uint32_t vt = kt + C::kTile;
-        const int nvalid = min(kBlockSize, it_L - (it_pg0 + pg) * kBlockSize);
         // ldmatrix row address: matrices (tokens 0-7, chunk 2i), (8-15, 2i),
         // (0-7, 2i+1), (8-15, 2i+1) for lanes 0-7, 8-15, 16-23, 24-31
         const int lt = (lane & 7) + ((lane >> 3) & 1) * 8;
 
         // ---------- S[token][head] = K Q^T: M = 16 tokens, N = 8 heads ----------
-        // two accumulators (even/odd k-steps) halve the dependent MMA chain;
-        // the KV heads of the group add into the same S, each into its own
-        // columns (the B fragments of the other columns are zero)
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        // per page two accumulators (even/odd k-steps) halve the dependent MMA
+        // chain; the KV heads of a group add into the same S, each into its own
+        // columns (the B fragments of the other columns are zero).  Tile rows:
+        // page pp, head h -> rows 16 (pp H + h) ..
+        float sa[T][4], sb[T][4];
 #pragma unroll
-        for (int hk = 0; hk < (INT8 ? H * (KSTEPS / 2) : 0); ++hk) {
-          const int h = hk / (KSTEPS / 2), kk = hk % (KSTEPS / 2);
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4(kt + tile_off<C>(16 * h + lt, 2 * kk + (lane >> 4)), r0, r1, r2, r3);
-          const uint2 qa = lds_u2(qfrag_lane_u32 + qhs * h + qks * (2 * kk));
-          const uint2 qb = lds_u2(qfrag_lane_u32 + qhs * h + qks * (2 * kk + 1));
-          if constexpr (INT8) {
-            // r0/r1: tokens g / g+8, head-dim 16(2kk)+4c+{0..3}; r2/r3: next chunk
-            uint32_t a0, a2, a1, a3;
-            i8x4_to_h2x2<0x4140u, 0x4342u>(r0, a0, a2);
-            i8x4_to_h2x2<0x4140u, 0x4342u>(r1, a1, a3);
-            mma_16816_acc<false>(sa, a0, a1, a2, a3, qa.x, qa.y);
-            i8x4_to_h2x2<0x4140u, 0x4342u>(r2, a0, a2);
-            i8x4_to_h2x2<0x4140u, 0x4342u>(r3, a1, a3);
-            mma_16816_acc<false>(sb, a0, a1, a2, a3, qb.x, qb.y);
+        for (int pp = 0; pp < T; ++pp)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sa[pp][e] = sb[pp][e] = 0.f;
+#pragma unroll
+        for (int pp = 0; pp < T; ++pp) {
+#pragma unroll
+          for (int hk = 0; hk < (INT8 ? H * (KSTEPS / 2) : 0); ++hk) {
+            const int h = hk / (KSTEPS / 2), kk = hk % (KSTEPS / 2);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kt + tile_off<C>(16 * (pp * H + h) + lt, 2 * kk + (lane >> 4)), r0, r1, r2,
+                    r3);
+            const uint2 qa = lds_u2(qfrag_lane_u32 + qhs * h + qks * (2 * kk));
+            const uint2 qb = lds_u2(qfrag_lane_u32 + qhs * h + qks * (2 * kk + 1));
+            if constexpr (INT8) {
+              // r0/r1: tokens g / g+8, head-dim 16(2kk)+4c+{0..3}; r2/r3: next chunk
+              uint32_t a0, a2, a1, a3;
+              i8x4_to_h2x2<0x4140u, 0x4342u>(r0, a0, a2);
+              i8x4_to_h2x2<0x4140u, 0x4342u>(r1, a1, a3);
+              mma_16816_acc<false>(sa[pp], a0, a1, a2, a3, qa.x, qa.y);
+              i8x4_to_h2x2<0x4140u, 0x4342u>(r2, a0, a2);
+              i8x4_to_h2x2<0x4140u, 0x4342u>(r3, a1, a3);
+              mma_16816_acc<false>(sb[pp], a0, a1, a2, a3, qb.x, qb.y);
+            }
           }
         }
         if constexpr (!INT8) {
@@ -844,38 +889,50 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
             ldsm_x4(kt + tile_off<C>(lt, 2 * ks + (lane >> 4)), r0, r1, r2, r3);
             const uint2 qa = lds_u2(qfrag_lane_u32 + qks * ks);
             // a0: token g, d 16ks+2c..; a1: token g+8; a2: token g, d 16ks+8+2c..; a3: g+8
-            if (ks & 1) mma_16816_acc<MMA_BF16>(sb, r0, r1, r2, r3, qa.x, qa.y);
-            else mma_16816_acc<MMA_BF16>(sa, r0, r1, r2, r3, qa.x, qa.y);
+            if (ks & 1) mma_16816_acc<MMA_BF16>(sb[0], r0, r1, r2, r3, qa.x, qa.y);
+            else mma_16816_acc<MMA_BF16>(sa[0], r0, r1, r2, r3, qa.x, qa.y);
           }
         }
 
-        // scores in log2 units: z0 (token g, head 2c), z1 (g, 2c+1), z2 (g+8, 2c), z3
-        // (static scales: the K scale is folded into scale_log2); a column's
-        // K scales are those of its KV head hc0 / hc1
-        float ks0 = p.scale_log2, ks1 = p.scale_log2, ks80 = p.scale_log2, ks81 = p.scale_log2;
-        if constexpr (INT8 && !STATIC) {
-          const uint16_t* ksc = scales_w + s * (C::kScaleBytes / 2);
-          ks0 *= __half2float(__ushort_as_half(ksc[16 * hc0 + g]));
-          ks80 *= __half2float(__ushort_as_half(ksc[16 * hc0 + g + 8]));
-          if constexpr (H > 1) {
-            ks1 *= __half2float(__ushort_as_half(ksc[16 * hc1 + g]));
-            ks81 *= __half2float(__ushort_as_half(ksc[16 * hc1 + g + 8]));
-          } else {
-            ks1 = ks0;
-            ks81 = ks80;
+        // scores in log2 units, per page: z[pp][0] (token g, head 2c), [1] (g,
+        // 2c+1), [2] (g+8, 2c), [3] (g+8, 2c+1) (static scales: the K scale is
+        // folded into scale_log2); a column's K scales are those of its KV
+        // head hc0 / hc1 (scale slots: page pp, head h, token t -> 16 (pp H + h) + t)
+        float z[T][4];
+#pragma unroll
+        for (int pp = 0; pp < T; ++pp) {
+          float ks0 = p.scale_log2, ks1 = p.scale_log2, ks80 = p.scale_log2, ks81 = p.scale_log2;
+          if constexpr (INT8 && !STATIC) {
+            const uint16_t* ksc = scales_w + s * (C::kScaleBytes / 2) + 16 * pp * H;
+            ks0 *= __half2float(__ushort_as_half(ksc[16 * hc0 + g]));
+            ks80 *= __half2float(__ushort_as_half(ksc[16 * hc0 + g + 8]));
+            if constexpr (H > 1) {
+              ks1 *= __half2float(__ushort_as_half(ksc[16 * hc1 + g]));
+              ks81 *= __half2float(__ushort_as_half(ksc[16 * hc1 + g + 8]));
+            } else {
+              ks1 = ks0;
+              ks81 = ks80;
+            }
           }
-        }
-        float z0 = (sa[0] + sb[0]) * ks0, z1 = (sa[1] + sb[1]) * ks1;
-        float z2 = (sa[2] + sb[2]) * ks80, z3 = (sa[3] + sb[3]) * ks81;
-        if (nvalid < kBlockSize) {
-          if (g >= nvalid) z0 = z1 = -INFINITY;
-          if (g + 8 >= nvalid) z2 = z3 = -INFINITY;
+          z[pp][0] = (sa[pp][0] + sb[pp][0]) * ks0;
+          z[pp][1] = (sa[pp][1] + sb[pp][1]) * ks1;
+          z[pp][2] = (sa[pp][2] + sb[pp][2]) * ks80;
+          z[pp][3] = (sa[pp][3] + sb[pp][3]) * ks81;
+          if (nv[pp] < kBlockSize) {
+            if (g >= nv[pp]) z[pp][0] = z[pp][1] = -INFINITY;
+            if (g + 8 >= nv[pp]) z[pp][2] = z[pp][3] = -INFINITY;
+          }
         }
 
         // ---------- online softmax per head column (reduce over the 8 g-lanes) ----------
         // true scores are z * qs (BF16 queries); the factor enters the max
         // once and each exponent through an FMA
-        float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
+        float mx0 = fmaxf(z[0][0], z[0][2]), mx1 = fmaxf(z[0][1], z[0][3]);
+#pragma unroll
+        for (int pp = 1; pp < T; ++pp) {
+          mx0 = fmaxf(mx0, fmaxf(z[pp][0], z[pp][2]));
+          mx1 = fmaxf(mx1, fmaxf(z[pp][1], z[pp][3]));
+        }
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
@@ -887,62 +944,76 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
         }
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-        // tokenwise V scales: the page's largest V scale (valid tokens) moves
+        // tokenwise V scales: the step's largest V scale (valid tokens) moves
         // the O unit up when it exceeds the running one; lg = 15 - vfb
         // shifts the exponents so that p' = p * 2^lg, and P' = p' * s_v < 2
         float ra = 1.f;     // O's unit change (power of two)
         int lg = 0;
-        float sv0 = 1.f, sv1 = 1.f, sv80 = 1.f, sv81 = 1.f;   // V scales of z0..z3
+        float sv[T][4];     // V scales of z[pp][0..3]
+#pragma unroll
+        for (int pp = 0; pp < T; ++pp)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sv[pp][e] = 1.f;
         if constexpr (INT8 && !STATIC) {
           const uint16_t* vsc = scales_w + s * (C::kScaleBytes / 2) + C::kRows;
-          uint32_t vb = 0;                       // slots (head, token) = (i / 16, i % 16)
+          uint32_t vb = 0;                       // slots (page, head, token)
 #pragma unroll
-          for (int i = lane & (H == 1 ? 15 : 31); i < C::kRows; i += 32)
-            if ((i & 15) < nvalid) vb = max(vb, (uint32_t)vsc[i]);
+          for (int i = lane & (C::kRows == 16 ? 15 : 31); i < C::kRows; i += 32)
+            if ((i & 15) < (i < 16 * H ? nv[0] : nv[T - 1])) vb = max(vb, (uint32_t)vsc[i]);
           const uint32_t vmax = redux_max_u32(vb);
           const int eb = max((int)(vmax >> 10), 1);
           if (eb > vfb) {
-            if (pg > 0) ra = exp2i(vfb - eb);   // the first page starts from O = 0
+            if (pg > 0) ra = exp2i(vfb - eb);   // the first step starts from O = 0
             vfb = eb;
           }
           lg = 15 - vfb;
-          if (g < nvalid) {
-            sv0 = __half2float(__ushort_as_half(vsc[16 * hc0 + g]));
-            sv1 = H > 1 ? __half2float(__ushort_as_half(vsc[16 * hc1 + g])) : sv0;
-          } else {
-            sv0 = sv1 = 0.f;
-          }
-          if (g + 8 < nvalid) {
-            sv80 = __half2float(__ushort_as_half(vsc[16 * hc0 + g + 8]));
-            sv81 = H > 1 ? __half2float(__ushort_as_half(vsc[16 * hc1 + g + 8])) : sv80;
-          } else {
-            sv80 = sv81 = 0.f;
+#pragma unroll
+          for (int pp = 0; pp < T; ++pp) {
+            const uint16_t* vp = vsc + 16 * pp * H;
+            if (g < nv[pp]) {
+              sv[pp][0] = __half2float(__ushort_as_half(vp[16 * hc0 + g]));
+              sv[pp][1] = H > 1 ? __half2float(__ushort_as_half(vp[16 * hc1 + g])) : sv[pp][0];
+            } else {
+              sv[pp][0] = sv[pp][1] = 0.f;
+            }
+            if (g + 8 < nv[pp]) {
+              sv[pp][2] = __half2float(__ushort_as_half(vp[16 * hc0 + g + 8]));
+              sv[pp][3] = H > 1 ? __half2float(__ushort_as_half(vp[16 * hc1 + g + 8])) : sv[pp][2];
+            } else {
+              sv[pp][2] = sv[pp][3] = 0.f;
+            }
           }
         }
         const float o0 = (float)lg - mn0, o1 = (float)lg - mn1;
-        float p0, p1, p2, p3;
-        if constexpr (INT8 && QBF16) {
-          p0 = fast_exp2(fmaf(z0, qs0, o0));
-          p1 = fast_exp2(fmaf(z1, qs1, o1));
-          p2 = fast_exp2(fmaf(z2, qs0, o0));
-          p3 = fast_exp2(fmaf(z3, qs1, o1));
-        } else {
-          p0 = fast_exp2(z0 + o0);
-          p1 = fast_exp2(z1 + o1);
-          p2 = fast_exp2(z2 + o0);
-          p3 = fast_exp2(z3 + o1);
+        float pr[T][4];
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int pp = 0; pp < T; ++pp) {
+          if constexpr (INT8 && QBF16) {
+            pr[pp][0] = fast_exp2(fmaf(z[pp][0], qs0, o0));
+            pr[pp][1] = fast_exp2(fmaf(z[pp][1], qs1, o1));
+            pr[pp][2] = fast_exp2(fmaf(z[pp][2], qs0, o0));
+            pr[pp][3] = fast_exp2(fmaf(z[pp][3], qs1, o1));
+          } else {
+            pr[pp][0] = fast_exp2(z[pp][0] + o0);
+            pr[pp][1] = fast_exp2(z[pp][1] + o1);
+            pr[pp][2] = fast_exp2(z[pp][2] + o0);
+            pr[pp][3] = fast_exp2(z[pp][3] + o1);
+          }
+          ps0 += pr[pp][0] + pr[pp][2];
+          ps1 += pr[pp][1] + pr[pp][3];
         }
         if constexpr (INT8 && !STATIC) {
           const float ul = exp2i(-lg);
-          l0 = fmaf(p0 + p2, ul, l0 * al0);
-          l1 = fmaf(p1 + p3, ul, l1 * al1);
-          p0 *= sv0;
-          p1 *= sv1;
-          p2 *= sv80;
-          p3 *= sv81;
+          l0 = fmaf(ps0, ul, l0 * al0);
+          l1 = fmaf(ps1, ul, l1 * al1);
+#pragma unroll
+          for (int pp = 0; pp < T; ++pp)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pr[pp][e] *= sv[pp][e];
         } else {
-          l0 = l0 * al0 + (p0 + p2);
-          l1 = l1 * al1 + (p1 + p3);
+          l0 = l0 * al0 + ps0;
+          l1 = l1 * al1 + ps1;
         }
         m0 = mn0;
         m1 = mn1;
@@ -957,45 +1028,48 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
           }
         }
 
-        // P'^T as the B operand: b0 = P'[tokens 2c, 2c+1][head g], b1 = tokens 2c+8, 2c+9
-        const uint32_t pb0 = movmatrix_trans(pack2<MMA_BF16>(p0, p1));
-        const uint32_t pb1 = movmatrix_trans(pack2<MMA_BF16>(p2, p3));
-
         // ---------- O^T[d][head] += V^T P^T: M = 16 head-dims, N = 8 heads ----------
-        if constexpr (INT8) {
-          // exact codes; the V scales are in P' (tokenwise) or applied once
-          // to the output (static).  KV head h of the group multiplies only
-          // its own columns of P'^T (the lanes of other columns pass zeros).
 #pragma unroll
-          for (int hk = 0; hk < H * (KSTEPS / 2); ++hk) {
-            const int h = hk / (KSTEPS / 2), kk = hk % (KSTEPS / 2);
-            const uint32_t bm0 = H == 1 || hg == h ? pb0 : 0u;
-            const uint32_t bm1 = H == 1 || hg == h ? pb1 : 0u;
-            uint32_t r[4];
-            ldsm_x4_trans(vt + tile_off<C>(16 * h + lt, 2 * kk + (lane >> 4)), r[0], r[1], r[2],
-                          r[3]);
+        for (int pp = 0; pp < T; ++pp) {
+          // P'^T as the B operand: b0 = P'[tokens 2c, 2c+1][head g], b1 = tokens 2c+8, 2c+9
+          const uint32_t pb0 = movmatrix_trans(pack2<MMA_BF16>(pr[pp][0], pr[pp][1]));
+          const uint32_t pb1 = movmatrix_trans(pack2<MMA_BF16>(pr[pp][2], pr[pp][3]));
+          if constexpr (INT8) {
+            // exact codes; the V scales are in P' (tokenwise) or applied once
+            // to the output (static).  KV head h of a group multiplies only
+            // its own columns of P'^T (the lanes of other columns pass zeros).
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              // r[2x]: tokens 2c, 2c+1; r[2x+1]: tokens 2c+8, 2c+9; bytes
-              // {t0 d0, t0 d1, t1 d0, t1 d1} with d0 = 16cb + 2g (row g), d1 = d0 + 1 (row g+8)
-              uint32_t ev0, od0, ev1, od1;
-              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * x], ev0, od0);
-              i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * x + 1], ev1, od1);
-              const int cb = 2 * kk + x;
-              float* oq = o + 4 * cb;
-              mma_16816_acc<false>(*reinterpret_cast<float(*)[4]>(oq), ev0, od0, ev1, od1, bm0, bm1);
+            for (int hk = 0; hk < H * (KSTEPS / 2); ++hk) {
+              const int h = hk / (KSTEPS / 2), kk = hk % (KSTEPS / 2);
+              const uint32_t bm0 = H == 1 || hg == h ? pb0 : 0u;
+              const uint32_t bm1 = H == 1 || hg == h ? pb1 : 0u;
+              uint32_t r[4];
+              ldsm_x4_trans(vt + tile_off<C>(16 * (pp * H + h) + lt, 2 * kk + (lane >> 4)), r[0],
+                            r[1], r[2], r[3]);
+#pragma unroll
+              for (int x = 0; x < 2; ++x) {
+                // r[2x]: tokens 2c, 2c+1; r[2x+1]: tokens 2c+8, 2c+9; bytes
+                // {t0 d0, t0 d1, t1 d0, t1 d1} with d0 = 16cb + 2g (row g), d1 = d0 + 1 (row g+8)
+                uint32_t ev0, od0, ev1, od1;
+                i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * x], ev0, od0);
+                i8x4_to_h2x2<0x4240u, 0x4341u>(r[2 * x + 1], ev1, od1);
+                const int cb = 2 * kk + x;
+                float* oq = o + 4 * cb;
+                mma_16816_acc<false>(*reinterpret_cast<float(*)[4]>(oq), ev0, od0, ev1, od1, bm0,
+                                     bm1);
+              }
             }
-          }
-        } else {
-          // matrices: (tokens 0-7, chunk 2pp), (0-7, 2pp+1), (8-15, 2pp), (8-15, 2pp+1)
-          const int vtk = (lane & 7) + (lane >> 4) * 8;
+          } else {
+            // matrices: (tokens 0-7, chunk 2q), (0-7, 2q+1), (8-15, 2q), (8-15, 2q+1)
+            const int vtk = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
-          for (int pp = 0; pp < D / 16; ++pp) {
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(vt + tile_off<C>(vtk, 2 * pp + ((lane >> 3) & 1)), r0, r1, r2, r3);
-            // rows g: d = 16pp + g; rows g+8: d = 16pp + 8 + g
-            float* oq = o + 4 * pp;
-            mma_16816_acc<MMA_BF16>(*reinterpret_cast<float(*)[4]>(oq), r0, r1, r2, r3, pb0, pb1);
+            for (int qq = 0; qq < D / 16; ++qq) {
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4_trans(vt + tile_off<C>(vtk, 2 * qq + ((lane >> 3) & 1)), r0, r1, r2, r3);
+              // rows g: d = 16qq + g; rows g+8: d = 16qq + 8 + g
+              float* oq = o + 4 * qq;
+              mma_16816_acc<MMA_BF16>(*reinterpret_cast<float(*)[4]>(oq), r0, r1, r2, r3, pb0, pb1);
+            }
           }
         }
       }
@@ -1074,19 +1148,19 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H>
 // occupancy and the launch (programmatic stream serialization, so that the
 // launch may overlap the tail of the previous kernel in the stream; the
 // kernel waits (griddepcontrol) before reading any input).
-template <bool INT8, bool STATIC, int H, bool CC = false>
+template <bool INT8, bool STATIC, int H, bool CC = false, int T = 1>
 struct DecodeLaunch {
   template <int D, bool BF16>
   static const void* fn() {
-    return reinterpret_cast<const void*>(&paged_decode_kernel<D, INT8, BF16, STATIC, H, CC>);
+    return reinterpret_cast<const void*>(&paged_decode_kernel<D, INT8, BF16, STATIC, H, CC, T>);
   }
   static const void* pick(int D, bool bf16) {
     if (D == 128) return bf16 ? fn<128, true>() : fn<128, false>();
     return bf16 ? fn<64, true>() : fn<64, false>();
   }
   static size_t smem(int D, int B, int GH) {
-    return D == 128 ? SmemLayout<128, INT8, STATIC, H, CC>(B, GH).total_bytes
-                    : SmemLayout<64, INT8, STATIC, H, CC>(B, GH).total_bytes;
+    return D == 128 ? SmemLayout<128, INT8, STATIC, H, CC, T>(B, GH).total_bytes
+                    : SmemLayout<64, INT8, STATIC, H, CC, T>(B, GH).total_bytes;
   }
   static cudaError_t configure(int D, bool bf16, size_t bytes) {
     // all of the unified L1/shared array as shared memory: the kernel's
@@ -1113,14 +1187,14 @@ struct DecodeLaunch {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (D == 128) {
-      return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, true, STATIC, H, CC>,
+      return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, true, STATIC, H, CC, T>,
                                        maps[0], maps[1], p)
-                  : cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, false, STATIC, H, CC>,
+                  : cudaLaunchKernelEx(&cfg, paged_decode_kernel<128, INT8, false, STATIC, H, CC, T>,
                                        maps[0], maps[1], p);
     }
-    return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, true, STATIC, H, CC>,
+    return bf16 ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, true, STATIC, H, CC, T>,
                                      maps[0], maps[1], p)
-                : cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, false, STATIC, H, CC>,
+                : cudaLaunchKernelEx(&cfg, paged_decode_kernel<64, INT8, false, STATIC, H, CC, T>,
                                      maps[0], maps[1], p);
   }
   static constexpr DecodeOps ops() { return DecodeOps{&smem, &configure, &occupancy, &launch}; }

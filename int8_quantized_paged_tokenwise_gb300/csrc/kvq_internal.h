@@ -130,6 +130,11 @@ cudaError_t prefill_launch(int D, bool bf16, const CUtensorMap* maps, const Pref
 #define KVQ_MAX_HEAD_GROUP 2
 #endif
 constexpr int kMaxHeadGroup = KVQ_MAX_HEAD_GROUP;
+// Pages one warp step covers when the head group is one KV head.
+#ifndef KVQ_MAX_PAGE_STEP
+#define KVQ_MAX_PAGE_STEP 2
+#endif
+constexpr int kMaxPageStep = KVQ_MAX_PAGE_STEP;
 
 // One decode kernel variant (cache kind x head group), for head_dim 64/128
 // and FP16/BF16 activations.  D = head_dim, GH = query heads per head group,
@@ -147,6 +152,7 @@ extern const DecodeOps kDecodeStaticH1;  // kvq_decode_static.cu
 extern const DecodeOps kDecodeStaticH2;  // kvq_decode_static_h2.cu
 extern const DecodeOps kDecodeKv16;      // kvq_decode_kv16.cu
 extern const DecodeOps kDecodeInt8Cc;    // kvq_decode_int8_cc.cu (CUDA cores, A/B)
+extern const DecodeOps kDecodeInt8T2;    // kvq_decode_int8_t2.cu (two pages per step)
 
 // combine (kvq_combine.cu)
 cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, int sms, cudaStream_t s);
