@@ -45,28 +45,36 @@ constexpr int kTcRows = 128;                    // M: (query, head) rows per hal
 constexpr int kTcHalves = 2;                    // row tiles per CTA
 constexpr int kTcKv = 64;                       // tokens per KV tile
 constexpr int kTcPages = kTcKv / kBlockSize;     // pages per KV tile
-constexpr int kTcRaw = 3;                       // INT8 staging ring depth
-constexpr int kTcConv = 3;                      // converted (FP16) operand buffers
+#ifndef KVQ_PF_RAW
+#define KVQ_PF_RAW 3
+#endif
+#ifndef KVQ_PF_CONV
+#define KVQ_PF_CONV 3
+#endif
+constexpr int kTcRaw = KVQ_PF_RAW;              // INT8 staging ring depth
+constexpr int kTcConv = KVQ_PF_CONV;            // converted (FP16) operand buffers
 constexpr int kTcWarps = 14;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpCvt = 10;
 constexpr uint32_t kTcCols = 512;
 
-// TMEM columns of half h: O at h D, S at 2 D + 64 h, P (64 FP16 = 32 columns)
-// at 2 D + 128 + 32 h; 2 D + 192 <= 448 < 512.
+// TMEM columns of half h: O at h D, S at 2 D + 64 h, whose first 32 columns
+// also hold P' (64 FP16) once the softmax has read S, and the half's Q tile
+// (the A operand of S = Q K^T, D FP16 = D / 2 columns) at 2 D + 128 + D h / 2;
+// 3 D + 128 <= 512.
 
 // barrier indices
-constexpr int kBarRawFull = 0, kBarRawEmpty = 3, kBarCvtFull = 6, kBarCvtEmpty = 9,
-              kBarSFull = 12, kBarPFull = 14, kBarODone = 16, kBarFin = 18, kNumBars = 19;
+constexpr int kBarRawFull = 0, kBarRawEmpty = kTcRaw, kBarCvtFull = 2 * kTcRaw,
+              kBarCvtEmpty = 2 * kTcRaw + kTcConv, kBarSFull = 2 * kTcRaw + 2 * kTcConv,
+              kBarPFull = kBarSFull + 2, kBarODone = kBarPFull + 2, kBarFin = kBarODone + 2,
+              kNumBars = kBarFin + 1;
 
 // Shared memory (offsets from a 1024-aligned base; every operand tile starts
 // on a 1024-byte boundary).
 template <int D>
 struct TcLayout {
-  static constexpr int kQBytes = kTcRows * D * 2;        // [128][D] FP16, D/64 tiles of 16 KB
-  static constexpr int kQ = 0;                            // one per half
   static constexpr int kConvBytes = kTcKv * D * 2;        // [64][D] FP16, D/64 tiles of 8 KB
-  static constexpr int kKc = kQ + kTcHalves * kQBytes;   // kTcConv K buffers
+  static constexpr int kKc = 0;                          // kTcConv K buffers
   static constexpr int kVc = kKc + kTcConv * kConvBytes; // kTcConv V buffers
   static constexpr int kTile = kBlockSize * D;           // one page's INT8 K (or V) tile
   static constexpr int kRawBytes = 2 * kTcPages * kTile; // K tiles of 4 pages, then V tiles
@@ -74,8 +82,7 @@ struct TcLayout {
   static constexpr int kRawSc = kRaw + kTcRaw * kRawBytes;         // per page: K 32 B, V 32 B
   static constexpr int kColSc = kRawSc + kTcRaw * kTcPages * 64;   // per buffer: K 64, V 64 floats
   static constexpr int kVmax = kColSc + kTcConv * 2 * kTcKv * 4;  // per buffer: 2 floats
-  static constexpr int kQsh = kVmax + kTcConv * 2 * 4;             // per half and row: shift
-  static constexpr int kBars = kQsh + kTcHalves * kTcRows * 4;
+  static constexpr int kBars = kVmax + kTcConv * 2 * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;     // TMEM base, abort flag
   static constexpr size_t kTotal = (size_t)kMisc + 16 + 1024;      // + base alignment slack
 };
@@ -96,6 +103,30 @@ __device__ __forceinline__ void convert_chunk(const uint8_t* src, uint8_t* dst, 
   i8x4_to_h2x2<0x4140u, 0x4342u>(w.y, lo.z, lo.w);
   i8x4_to_h2x2<0x4140u, 0x4342u>(w.z, hi.x, hi.y);
   i8x4_to_h2x2<0x4140u, 0x4342u>(w.w, hi.z, hi.w);
+  uint8_t* row = dst + (c >> 2) * (kTcKv * 128) + t * 128;
+  const int c0 = (2 * c) & 7;
+  *reinterpret_cast<uint4*>(row + ((c0 ^ (t & 7)) << 4)) = lo;
+  *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (t & 7)) << 4)) = hi;
+}
+
+// The same for V, each exact code pair then multiplied by the token's scale
+// factor `f` (an FP16 pair): V' = code * s_v * 2^(127 - F) <= 254.
+template <int D>
+__device__ __forceinline__ void convert_chunk_scaled(const uint8_t* src, uint8_t* dst, int t, int c,
+                                                     __half2 f) {
+  const uint4 w = *reinterpret_cast<const uint4*>(src);
+  uint4 lo, hi;
+  i8x4_to_h2x2<0x4140u, 0x4342u>(w.x, lo.x, lo.y);
+  i8x4_to_h2x2<0x4140u, 0x4342u>(w.y, lo.z, lo.w);
+  i8x4_to_h2x2<0x4140u, 0x4342u>(w.z, hi.x, hi.y);
+  i8x4_to_h2x2<0x4140u, 0x4342u>(w.w, hi.z, hi.w);
+  uint32_t* l4 = reinterpret_cast<uint32_t*>(&lo);
+  uint32_t* h4 = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    l4[i] = h2_as_u32(__hmul2(u32_as_h2(l4[i]), f));
+    h4[i] = h2_as_u32(__hmul2(u32_as_h2(h4[i]), f));
+  }
   uint8_t* row = dst + (c >> 2) * (kTcKv * 128) + t * 128;
   const int c0 = (2 * c) & 7;
   *reinterpret_cast<uint4*>(row + ((c0 ^ (t & 7)) << 4)) = lo;
@@ -156,51 +187,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          n_it * kTcPages);
 
   if (warp == kWarpMma) tc_alloc(smem_u32(&misc[0]), kTcCols);
-
-  // ---- Q tiles: row r of half h = (query i_begin + h TH + r / G, head j G + r % G), FP16 ----
-  // BF16 rows enter as q * 2^-sh (exact: the row's largest |q| lands in
-  // [2^14, 2^15)); the row's softmax multiplies its scores by 2^sh.  The D/8
-  // chunks of a row are handled by D/8 consecutive lanes of one warp (the
-  // loop's stride is a multiple of 32, so a warp runs an iteration whole).
-  int* qsh = reinterpret_cast<int*>(smem + Ly::kQsh);
-  for (int e = tid; e < kTcHalves * kTcRows * (D / 8); e += kTcThreads) {
-    const int hr = e / (D / 8), c8 = e - hr * (D / 8);  // 16-byte chunk c8 of row hr
-    const int h = hr / kTcRows, r = hr - h * kTcRows;
-    const int i = i_begin + h * TH + r / G;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < TH * G && i < n) {
-      const uint16_t* src = static_cast<const uint16_t*>(p.q) +
-                            ((int64_t)(q0 + i) * p.Hq + (int64_t)j * G + r % G) * D + 8 * c8;
-      v = __ldg(reinterpret_cast<const uint4*>(src));
-    }
-    if constexpr (BF16) {
-      uint32_t mx = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                             __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-      mx = max(mx & 0xFFFFu, mx >> 16);
-#pragma unroll
-      for (int o = 1; o < D / 8; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-      const int sh = bf16_fp16_shift(mx);
-      if (c8 == 0) qsh[hr] = sh;
-      const float inv = exp2i(-sh);
-      v.x = bf2_to_h2(v.x, inv);
-      v.y = bf2_to_h2(v.y, inv);
-      v.z = bf2_to_h2(v.z, inv);
-      v.w = bf2_to_h2(v.w, inv);
-    } else if (c8 == 0) {
-      qsh[hr] = 0;
-    }
-    *reinterpret_cast<uint4*>(smem + Ly::kQ + h * Ly::kQBytes + (c8 >> 3) * (kTcRows * 128) +
-                              r * 128 + (((c8 & 7) ^ (r & 7)) << 4)) = v;
-  }
-  fence_proxy_async_smem();
-  fence_mbar_init();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
   auto tO = [&](int h) { return tmem + (uint32_t)(h * D); };
   auto tS = [&](int h) { return tmem + (uint32_t)(2 * D + kTcKv * h); };
-  auto tP = [&](int h) { return tmem + (uint32_t)(2 * D + 2 * kTcKv + (kTcKv / 2) * h); };
+  auto tP = [&](int h) { return tS(h); };
+  auto tQ = [&](int h) { return tmem + (uint32_t)(2 * D + 2 * kTcKv + (D / 2) * h); };
+
+  // ---- Q tiles into TMEM: row r of half h = TMEM lane r = (query i_begin +
+  // h TH + r / G, head j G + r % G), FP16, written by that row's softmax
+  // thread.  BF16 rows enter as q * 2^-sh (exact: the row's largest |q| lands
+  // in [2^14, 2^15)); the softmax multiplies the row's scores by qf = 2^sh.
+  float qf = 1.f;
+  if (warp < 2 * 4) {
+    const int h = warp >> 2, r = 32 * (warp & 3) + lane;
+    const int i = i_begin + h * TH + r / G;
+    uint4 v[D / 8];
+    const bool row = r < TH * G && i < n;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        static_cast<const uint16_t*>(p.q) +
+        ((int64_t)(q0 + (row ? i : 0)) * p.Hq + (int64_t)j * G + r % G) * D);
+#pragma unroll
+    for (int c8 = 0; c8 < D / 8; ++c8) v[c8] = row ? __ldg(src + c8) : make_uint4(0, 0, 0, 0);
+    if constexpr (BF16) {
+      uint32_t mx = 0;
+#pragma unroll
+      for (int c8 = 0; c8 < D / 8; ++c8)
+        mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(v[c8].x & 0x7FFF7FFFu, v[c8].y & 0x7FFF7FFFu),
+                                   __vmaxu2(v[c8].z & 0x7FFF7FFFu, v[c8].w & 0x7FFF7FFFu)));
+      const int sh = bf16_fp16_shift(max(mx & 0xFFFFu, mx >> 16));
+      qf = exp2i(sh);
+      const float inv = exp2i(-sh);
+#pragma unroll
+      for (int c8 = 0; c8 < D / 8; ++c8) {
+        v[c8].x = bf2_to_h2(v[c8].x, inv);
+        v[c8].y = bf2_to_h2(v[c8].y, inv);
+        v[c8].z = bf2_to_h2(v[c8].z, inv);
+        v[c8].w = bf2_to_h2(v[c8].w, inv);
+      }
+    }
+    // column c holds elements 2c (low half) and 2c + 1 of the row
+    const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
+#pragma unroll
+    for (int c0 = 0; c0 < D / 2; c0 += 32) {
+      uint32_t w[32];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const uint4 u = v[(c0 + 4 * x) / 4];
+        w[4 * x] = u.x;
+        w[4 * x + 1] = u.y;
+        w[4 * x + 2] = u.z;
+        w[4 * x + 3] = u.w;
+      }
+      tc_st32(tQ(h) + c0 + lanes, w);
+    }
+    tc_wait_st();
+  }
+  fence_mbar_init();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   auto fail = [&]() {
     atomicOr(p.err, 0x8u);
     *abort_flag = 1;
@@ -268,6 +316,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp >= kWarpCvt) {
     // ---------------------------------------------------------- converters
     const int ct = tid - kWarpCvt * 32;           // 0..127
+    int cvt_f = 0;                                // running V exponent F
     for (int it = 0; it < n_it; ++it) {
       const int s = it % kTcRaw, cb = it % kTcConv;
       if (!mbar_wait_bounded(bar(kBarRawFull + s), (it / kTcRaw) & 1) ||
@@ -281,34 +330,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint8_t* rawV = rawK + kTcPages * Ly::kTile;
       uint8_t* kc = smem + Ly::kKc + cb * Ly::kConvBytes;
       uint8_t* vc = smem + Ly::kVc + cb * Ly::kConvBytes;
-      // 16 codes (chunk c of token t) -> FP16 chunks 2c, 2c+1 of row t, K then V
+      const uint16_t* rs =
+          reinterpret_cast<const uint16_t*>(smem + Ly::kRawSc) + s * kTcPages * 32;
+      // the tile's largest V scale over the tokens that were copied and
+      // belong to the sequence (other slots may hold anything), reduced by
+      // every converter warp itself; F = its running maximum's FP32 exponent
+      // (the softmax tracks the same F from vmax)
+      const int vlim = min(L, npages * kBlockSize) - it * kTcKv;   // valid tokens of the tile
+      uint32_t vb = 0;
+#pragma unroll
+      for (int t = lane; t < kTcKv; t += 32)
+        if (t < vlim)
+          vb = max(vb, __float_as_uint(__half2float(__ushort_as_half(rs[(t >> 4) * 32 + 16 + (t & 15)]))));
+      vb = redux_max_u32(vb);
+      cvt_f = max(cvt_f, (int)(vb >> 23));
+      const float vsf = exp2i(127 - cvt_f);
+      if (warp == kWarpCvt && lane == 0) {
+        float* vm = reinterpret_cast<float*>(smem + Ly::kVmax) + 2 * cb;
+        vm[0] = __uint_as_float(vb);
+        vm[1] = 0.f;
+      }
+      // 16 codes (chunk c of token t) -> FP16 chunks 2c, 2c+1 of row t; K
+      // exact, V times its token's s_v 2^(127 - F)
 #pragma unroll
       for (int pass = 0; pass < kTcKv * (D / 16) / 128; ++pass) {
         const int e = ct + 128 * pass;
         const int t = e / (D / 16), c = e - t * (D / 16);
         const int src = (t >> 4) * Ly::kTile + tile_off<C>(t & 15, c);
         convert_chunk<D>(rawK + src, kc, t, c);
-        convert_chunk<D>(rawV + src, vc, t, c);
+        const float f =
+            t < vlim ? __half2float(__ushort_as_half(rs[(t >> 4) * 32 + 16 + (t & 15)])) * vsf : 0.f;
+        convert_chunk_scaled<D>(rawV + src, vc, t, c, __float2half2_rn(f));
       }
-      // scale columns: K (times sm_scale log2 e) for ct < 64, V for the others
-      {
-        const uint16_t* rs =
-            reinterpret_cast<const uint16_t*>(smem + Ly::kRawSc) + s * kTcPages * 32;
+      // K scale column (times sm_scale log2 e)
+      if (ct < kTcKv) {
         float* cs = reinterpret_cast<float*>(smem + Ly::kColSc) + cb * 2 * kTcKv;
-        const int t = ct & (kTcKv - 1), kind = ct >> 6;
-        const float sv = __half2float(__ushort_as_half(rs[(t >> 4) * 32 + kind * 16 + (t & 15)]));
-        cs[kind * kTcKv + t] = kind == 0 ? sv * p.scale_log2 : sv;
-        if (kind == 1) {
-          // the largest V scale of the tile's tokens that were copied and
-          // belong to the sequence (other slots may hold anything): one per
-          // V warp
-          const int tg = it * kTcKv + t;
-          const uint32_t vm =
-              redux_max_u32(tg < L && tg < npages * kBlockSize ? __float_as_uint(sv) : 0u);
-          if (lane == 0)
-            reinterpret_cast<float*>(smem + Ly::kVmax)[2 * cb + (warp - kWarpCvt - 2)] =
-                __uint_as_float(vm);
-        }
+        cs[ct] = __half2float(__ushort_as_half(rs[(ct >> 4) * 32 + (ct & 15)])) * p.scale_log2;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -351,13 +408,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (it == n_half[h]) tc_commit(bar(kBarODone + h));   // the half's O is final
           }
           if (it < n_half[h]) {
-            const uint32_t qa = smem_u32(smem + Ly::kQ + h * Ly::kQBytes);
             const uint32_t kbase = smem_u32(smem + Ly::kKc + cb * Ly::kConvBytes);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-              tc_mma_f16(tS(h), tc_desc_sw128(qa + (ks >> 2) * (kTcRows * 128) + 32 * (ks & 3)),
-                         tc_desc_sw128(kbase + (ks >> 2) * (kTcKv * 128) + 32 * (ks & 3)), idS,
-                         ks > 0);
+              tc_mma_f16_tmem_a(tS(h), tQ(h) + 8 * ks,
+                                tc_desc_sw128(kbase + (ks >> 2) * (kTcKv * 128) + 32 * (ks & 3)),
+                                idS, ks > 0);
             tc_commit(bar(kBarSFull + h));         // also covers the P V above
           }
         }
@@ -378,7 +434,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nh = n_half[h];
     float m_use = -INFINITY, l = 0.f;
     // the row's scores are (S * K scale) * qf (BF16 queries entered as q / qf)
-    const float qf = exp2i(qsh[h * kTcRows + r]);
     // V scales go onto P: P' = P s_v 2^(127 - vfb) with vfb the FP32 biased
     // exponent of the largest V scale so far (all rows see the same tokens,
     // so it moves for all rows at once); O accumulates in units of
@@ -395,7 +450,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      // scale columns of the tile: K (times sm_scale log2 e) at [0, 64), V at [64, 128)
+      // the tile's K scale column (times sm_scale log2 e)
       const float4* cs4 = reinterpret_cast<const float4*>(smem + Ly::kColSc) + cb * (kTcKv / 2);
       const int t0 = it * kTcKv;
       const bool masked = t0 + kTcKv - 1 > pos;    // some token of the tile is past the row
@@ -420,14 +475,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       float mx;
       {
-        float mr[kTcKv / 2];                       // pairwise tree: short dependency chains
+        // three-way tree (64 -> 22 -> 8 -> 3 -> 1): short dependency chains
+        static_assert(kTcKv == 64, "the max tree is laid out for 64 tokens");
+        float m1[22], m2[8];
 #pragma unroll
-        for (int t = 0; t < kTcKv / 2; ++t) mr[t] = fmaxf(z[t], z[t + kTcKv / 2]);
+        for (int t = 0; t < 21; ++t) m1[t] = fmax3(z[t], z[t + 21], z[t + 42]);
+        m1[21] = z[63];
 #pragma unroll
-        for (int w = kTcKv / 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int t = 0; t < w; ++t) mr[t] = fmaxf(mr[t], mr[t + w]);
-        mx = mr[0] * qf;
+        for (int t = 0; t < 7; ++t) m2[t] = fmax3(m1[t], m1[t + 7], m1[t + 14]);
+        m2[7] = m1[21];
+        mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+        mx *= qf;
       }
       const bool grow = mx > m_use + 8.f;
       const float m_new = grow ? mx : m_use;
@@ -444,13 +502,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           vfb = eb;
         }
       }
-      const int lg = 127 - vfb;
-      // P = 2^(z qf - m) scaled by 2^lg: the row sum takes P, the P V operand
-      // P' = P 2^lg s_v (0 for tokens past the row, whose scale slots may
-      // hold anything)
-      const float off = (float)lg - ref;
+      // P = 2^(z qf - m): the row sum and the P V operand (the V scales are
+      // in the converted V tile; 0 for tokens past the row)
 #pragma unroll
-      for (int t = 0; t < kTcKv; ++t) z[t] = fast_exp2(fmaf(z[t], qf, off));
+      for (int t = 0; t < kTcKv; ++t) z[t] = fast_exp2(fmaf(z[t], qf, -ref));
       float lsum;
       {
         float sr2[kTcKv / 2];
@@ -462,14 +517,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int t = 0; t < w; ++t) sr2[t] += sr2[t + w];
         lsum = sr2[0];
       }
-      l = fmaf(lsum, exp2i(-lg), l * alpha);
-      uint32_t pk[kTcKv / 2];                     // P' packed two FP16 per TMEM column
+      l = fmaf(l, alpha, lsum);
+      uint32_t pk[kTcKv / 2];                     // P packed two FP16 per TMEM column
 #pragma unroll
       for (int cc = 0; cc < kTcKv / 8; ++cc) {
-        const float4 v0 = cs4[kTcKv / 4 + 2 * cc], v1 = cs4[kTcKv / 4 + 2 * cc + 1];
-        float a8[8] = {z[8 * cc] * v0.x,     z[8 * cc + 1] * v0.y, z[8 * cc + 2] * v0.z,
-                       z[8 * cc + 3] * v0.w, z[8 * cc + 4] * v1.x, z[8 * cc + 5] * v1.y,
-                       z[8 * cc + 6] * v1.z, z[8 * cc + 7] * v1.w};
+        float a8[8] = {z[8 * cc],     z[8 * cc + 1], z[8 * cc + 2], z[8 * cc + 3],
+                       z[8 * cc + 4], z[8 * cc + 5], z[8 * cc + 6], z[8 * cc + 7]};
         if (masked) {
 #pragma unroll
           for (int e2 = 0; e2 < 8; ++e2)

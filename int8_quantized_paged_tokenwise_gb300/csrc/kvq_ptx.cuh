@@ -221,6 +221,13 @@ __device__ __forceinline__ uint32_t redux_max_u32(uint32_t x) {
 }
 
 // ------------------------------------------------------------ numerics ---
+// The largest of three floats in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^e as a float, for e in [-126, 127] (exact; built from the exponent field).
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 
