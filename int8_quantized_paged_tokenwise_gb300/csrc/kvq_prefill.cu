@@ -354,8 +354,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // exact, V times its token's s_v 2^(127 - F)
 #pragma unroll
       for (int pass = 0; pass < kTcKv * (D / 16) / 128; ++pass) {
+        // D = 128: a quarter-warp takes 4 chunks of each of two adjacent
+        // tokens, so that its 16-byte reads (raw rows) and writes (converted
+        // rows, swizzled) each cover all eight bank groups
         const int e = ct + 128 * pass;
-        const int t = e / (D / 16), c = e - t * (D / 16);
+        const int t = D == 128 ? 16 * pass + 4 * (warp - kWarpCvt) + 2 * (lane >> 4) +
+                                     (((lane >> 2) ^ (lane >> 3)) & 1)
+                               : e / (D / 16);
+        const int c = D == 128 ? (lane & 7) : e - t * (D / 16);
         const int src = (t >> 4) * Ly::kTile + tile_off<C>(t & 15, c);
         convert_chunk<D>(rawK + src, kc, t, c);
         const float f =
@@ -455,17 +461,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int t0 = it * kTcKv;
       const bool masked = t0 + kTcKv - 1 > pos;    // some token of the tile is past the row
       float z[kTcKv];
+      {
+        uint32_t sr[kTcKv];
+        tc_ld64(tS(h) + lanes, sr);
 #pragma unroll
-      for (int hc = 0; hc < kTcKv / 32; ++hc) {
-        uint32_t sr[32];
-        tc_ld32(tS(h) + 32 * hc + lanes, sr);
-#pragma unroll
-        for (int x = 0; x < 32; x += 4) {
-          const float4 k4 = cs4[(32 * hc + x) / 4];
-          z[32 * hc + x] = __uint_as_float(sr[x]) * k4.x;
-          z[32 * hc + x + 1] = __uint_as_float(sr[x + 1]) * k4.y;
-          z[32 * hc + x + 2] = __uint_as_float(sr[x + 2]) * k4.z;
-          z[32 * hc + x + 3] = __uint_as_float(sr[x + 3]) * k4.w;
+        for (int x = 0; x < kTcKv; x += 4) {
+          const float4 k4 = cs4[x / 4];
+          const float2 a = __fmul2_rn(make_float2(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])),
+                                      make_float2(k4.x, k4.y));
+          const float2 c = __fmul2_rn(
+              make_float2(__uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3])),
+              make_float2(k4.z, k4.w));
+          z[x] = a.x;
+          z[x + 1] = a.y;
+          z[x + 2] = c.x;
+          z[x + 3] = c.y;
         }
       }
       if (masked) {
@@ -503,19 +513,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       // P = 2^(z qf - m): the row sum and the P V operand (the V scales are
-      // in the converted V tile; 0 for tokens past the row)
-#pragma unroll
-      for (int t = 0; t < kTcKv; ++t) z[t] = fast_exp2(fmaf(z[t], qf, -ref));
+      // in the converted V tile; 0 for tokens past the row); FP32 pairs go
+      // through the packed (two-lane) FMA instructions
       float lsum;
       {
-        float sr2[kTcKv / 2];
+        const float2 qf2 = make_float2(qf, qf), nref2 = make_float2(-ref, -ref);
+        float2 acc[kTcKv / 4];
 #pragma unroll
-        for (int t = 0; t < kTcKv / 2; ++t) sr2[t] = z[t] + z[t + kTcKv / 2];
+        for (int t = 0; t < kTcKv; t += 2) {
+          float2 e = __ffma2_rn(make_float2(z[t], z[t + 1]), qf2, nref2);
+          e.x = fast_exp2(e.x);
+          e.y = fast_exp2(e.y);
+          z[t] = e.x;
+          z[t + 1] = e.y;
+          acc[t >> 2] = (t & 2) ? __fadd2_rn(acc[t >> 2], e) : e;
+        }
 #pragma unroll
-        for (int w = kTcKv / 4; w >= 1; w >>= 1)
+        for (int w = kTcKv / 8; w >= 1; w >>= 1)
 #pragma unroll
-          for (int t = 0; t < w; ++t) sr2[t] += sr2[t + w];
-        lsum = sr2[0];
+          for (int t = 0; t < w; ++t) acc[t] = __fadd2_rn(acc[t], acc[t + w]);
+        lsum = acc[0].x + acc[0].y;
       }
       l = fmaf(l, alpha, lsum);
       uint32_t pk[kTcKv / 2];                     // P packed two FP16 per TMEM column
