@@ -762,6 +762,10 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H,
     // head's largest |q| lands in [2^14, 2^15)); qs0/qs1 = 2^sh of the heads
     // 2c, 2c+1 of this thread's score columns multiply their scores.
     float qs0 = 1.f, qs1 = 1.f;
+    // INT8 K codes enter the QK MMAs as 1152 + code (no subtraction in the
+    // conversion): the score of head column n then carries 1152 * sum_d q[n][d],
+    // kb0 / kb1 for this thread's columns 2c / 2c + 1, removed before scaling.
+    float kb0 = 0.f, kb1 = 0.f;
     // Tokenwise V scales go onto P: P' = p * s_v * 2^(15 - vfb), vfb the FP16
     // biased exponent of the largest V scale of the piece so far (so P' < 2);
     // O accumulates in units of 2^(vfb - 15) and is rescaled when vfb grows.
@@ -803,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H,
           qs0 = __shfl_sync(0xFFFFFFFFu, qsg, 8 * c);
           qs1 = __shfl_sync(0xFFFFFFFFu, qsg, 8 * c + 4);
         }
+        float qsum = 0.f;            // head g's query sum, over this lane's elements
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
           uint2 f = make_uint2(0u, 0u);
@@ -824,10 +829,20 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H,
               f.y = *reinterpret_cast<const uint32_t*>(qs + 16 * ks + 8 + 2 * c);
             }
           }
+          if constexpr (INT8) {
+            const float2 a = __half22float2(u32_as_h2(f.x)), b = __half22float2(u32_as_h2(f.y));
+            qsum += (a.x + a.y) + (b.x + b.y);
+          }
           // the fragment goes to its KV head's MMAs; the others see zeros
 #pragma unroll
           for (int h = 0; h < H; ++h)
             qfrag[(h * KSTEPS + ks) * 32 + lane] = h == hg ? f : make_uint2(0u, 0u);
+        }
+        if constexpr (INT8) {
+          qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 1);
+          qsum += __shfl_xor_sync(0xFFFFFFFFu, qsum, 2);
+          kb0 = 1152.f * __shfl_sync(0xFFFFFFFFu, qsum, 8 * c);
+          kb1 = 1152.f * __shfl_sync(0xFFFFFFFFu, qsum, 8 * c + 4);
         }
         __syncwarp();   // the raw query slot may be refilled once every lane is done
         cs.q_consumed = ord;
@@ -871,11 +886,11 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H,
             if constexpr (INT8) {
               // r0/r1: tokens g / g+8, head-dim 16(2kk)+4c+{0..3}; r2/r3: next chunk
               uint32_t a0, a2, a1, a3;
-              i8x4_to_h2x2<0x4140u, 0x4342u>(r0, a0, a2);
-              i8x4_to_h2x2<0x4140u, 0x4342u>(r1, a1, a3);
+              i8x4_to_h2x2_b1152<0x4140u, 0x4342u>(r0, a0, a2);
+              i8x4_to_h2x2_b1152<0x4140u, 0x4342u>(r1, a1, a3);
               mma_16816_acc<false>(sa[pp], a0, a1, a2, a3, qa.x, qa.y);
-              i8x4_to_h2x2<0x4140u, 0x4342u>(r2, a0, a2);
-              i8x4_to_h2x2<0x4140u, 0x4342u>(r3, a1, a3);
+              i8x4_to_h2x2_b1152<0x4140u, 0x4342u>(r2, a0, a2);
+              i8x4_to_h2x2_b1152<0x4140u, 0x4342u>(r3, a1, a3);
               mma_16816_acc<false>(sb[pp], a0, a1, a2, a3, qb.x, qb.y);
             }
           }
@@ -914,10 +929,10 @@ __global__ void __launch_bounds__(kThreads, CC ? 2 : TileCfg<D, INT8, STATIC, H,
               ks81 = ks80;
             }
           }
-          z[pp][0] = (sa[pp][0] + sb[pp][0]) * ks0;
-          z[pp][1] = (sa[pp][1] + sb[pp][1]) * ks1;
-          z[pp][2] = (sa[pp][2] + sb[pp][2]) * ks80;
-          z[pp][3] = (sa[pp][3] + sb[pp][3]) * ks81;
+          z[pp][0] = ((sa[pp][0] - kb0) + sb[pp][0]) * ks0;
+          z[pp][1] = ((sa[pp][1] - kb1) + sb[pp][1]) * ks1;
+          z[pp][2] = ((sa[pp][2] - kb0) + sb[pp][2]) * ks80;
+          z[pp][3] = ((sa[pp][3] - kb1) + sb[pp][3]) * ks81;
           if (nv[pp] < kBlockSize) {
             if (g >= nv[pp]) z[pp][0] = z[pp][1] = -INFINITY;
             if (g + 8 >= nv[pp]) z[pp][2] = z[pp][3] = -INFINITY;

@@ -270,4 +270,15 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
   hi = h2_as_u32(__hsub2(u32_as_h2(__byte_perm(u, 0x64646464u, SEL_HI)), bias));
 }
 
+// The same without the subtraction: each FP16 value is 1152 + code, exactly.
+// Used where the bias is removed after the MMA (a dot product with such a row
+// is the dot product with the codes plus 1152 times the sum of the other
+// operand).
+template <uint32_t SEL_LO, uint32_t SEL_HI>
+__device__ __forceinline__ void i8x4_to_h2x2_b1152(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, SEL_LO);
+  hi = __byte_perm(u, 0x64646464u, SEL_HI);
+}
+
 }  // namespace kvq
