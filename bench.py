@@ -537,31 +537,54 @@ def time_arm(torch, flush, append, decode, steps, warmup, settle_s=0.0):
 
 
 def time_e2e(torch, g: GpuWorkload, flush, steps, warmup):
-    """Through the public API with host buffers: pinned H2D of the step's
-    inputs (q, new K/V rows, slots, block tables, context lengths), the two
-    calls, D2H of the output -- all inside the timed region."""
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    q_h = pin(g.q_h.view(np.int16))
-    k_h = pin(g.k_new_h.view(np.int16)) if g.k_new is not None else None
-    v_h = pin(g.v_new_h.view(np.int16)) if g.k_new is not None else None
-    s_h = pin(g.slots_h) if g.k_new is not None else None
-    bt_h, cl_h = pin(g.bt_h), pin(g.cl_h)
+    """Through the C ABI with host buffers, the way a serving engine drives
+    it: the step's inputs (q, block tables, context lengths, and the new K/V
+    rows with their slots when the workload appends) sit in one pinned host
+    staging buffer and go to the GPU in one H2D copy; the calls take prepared
+    arguments (pointers into the device copy of that buffer); the output comes
+    back in one D2H copy.  All of it inside the timed region, every step."""
+    import ctypes
+    L = g.kvq.load()
+    w = g.w
+    parts = [("q", g.q_h.view(np.int16)), ("bt", np.ascontiguousarray(g.bt_h, dtype=np.int32)),
+             ("cl", np.ascontiguousarray(g.cl_h, dtype=np.int32))]
+    if g.k_new is not None:
+        parts += [("k", g.k_new_h), ("v", g.v_new_h), ("s", g.slots_h.astype(np.int64))]
+    offs, total = {}, 0
+    for name, a in parts:
+        offs[name] = total
+        total += (a.nbytes + 255) // 256 * 256
+    stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    sh = stage_h.numpy()
+    for name, a in parts:
+        sh[offs[name]:offs[name] + a.nbytes] = np.ascontiguousarray(a).view(np.uint8).ravel()
+    stage_d = torch.empty(total, dtype=torch.uint8, device=g.dev)
+    h2d = sum(a.nbytes for _, a in parts)
     out_h = torch.empty(g.out.shape, dtype=torch.int16).pin_memory()
-    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + cl_h.numel() * 4
-    if k_h is not None:
-        h2d += k_h.numel() * 2 * 2 + s_h.numel() * 8
     d2h = out_h.numel() * 2
+    base = stage_d.data_ptr()
+    P = ctypes.c_void_p
+    kc, vc, ksc, vsc = g.int8
+    stream = P(torch.cuda.current_stream().cuda_stream)
+    dt = 1 if w.dtype == "bf16" else 0
+    dec_args = [P(base + offs["q"]), dt, w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                P(kc.data_ptr()), P(vc.data_ptr()), P(ksc.data_ptr()), P(vsc.data_ptr()),
+                kc.shape[0], 16, P(base + offs["bt"]), g.bt.shape[1], P(base + offs["cl"]),
+                w.max_context_len, w.sm_scale, P(g.out.data_ptr()), P(g.ws.data_ptr()),
+                g.ws.numel(), stream]
+    app_args = None
+    if g.k_new is not None:
+        T, Hkv, D = g.k_new.shape
+        app_args = [P(base + offs["k"]), P(base + offs["v"]), Hkv * D, Hkv * D, T, Hkv, D, dt,
+                    P(base + offs["s"]), P(kc.data_ptr()), P(vc.data_ptr()), P(ksc.data_ptr()),
+                    P(vsc.data_ptr()), kc.shape[0], 16, stream]
 
     def step():
-        g.q.view(torch.int16).copy_(q_h, non_blocking=True)
-        if k_h is not None:
-            g.k_new.view(torch.int16).copy_(k_h, non_blocking=True)
-            g.v_new.view(torch.int16).copy_(v_h, non_blocking=True)
-            g.slots.copy_(s_h, non_blocking=True)
-        g.bt.copy_(bt_h, non_blocking=True)
-        g.cl.copy_(cl_h, non_blocking=True)
-        g.append_int8()
-        g.decode_int8()
+        stage_d.copy_(stage_h, non_blocking=True)
+        if app_args is not None and L.kvq_quantize_append(*app_args) != 0:
+            raise RuntimeError("kvq_quantize_append failed")
+        if L.kvq_paged_decode(*dec_args) != 0:
+            raise RuntimeError("kvq_paged_decode failed")
         out_h.copy_(g.out.view(torch.int16), non_blocking=True)
 
     for _ in range(warmup):
@@ -575,6 +598,12 @@ def time_e2e(torch, g: GpuWorkload, flush, steps, warmup):
         step()
         ev[i][1].record()
     torch.cuda.synchronize()
+    # the staged call computes what the device-resident one (Python binding,
+    # separate input tensors) does, bit for bit
+    g.decode_int8()
+    torch.cuda.synchronize()
+    if not torch.equal(out_h, g.out.view(torch.int16).cpu()):
+        raise RuntimeError("the end-to-end call's output differs from the device-resident call's")
     return [a.elapsed_time(b) for a, b in ev], h2d, d2h
 
 

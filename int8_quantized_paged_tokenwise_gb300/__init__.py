@@ -136,13 +136,22 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()     # an int; the argtypes make it a void*
 
 
-def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device=None):
+    """The stream handle to launch on: `stream`, else the current stream of
+    `device` (a torch.device of a CUDA tensor), else of the current device."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        idx = device.index if device is not None and device.index is not None else \
+            torch.cuda.current_device()
+        return _raw_stream(idx)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _check(status: int, what: str):
@@ -291,9 +300,17 @@ def _check_decode(q, k_cache, v_cache, block_tables, context_lens, out, cache_dt
           "out must match q")
 
 
+_ws_need = {}
+
+
 def _workspace(q, Hkv, max_context_len, partition_pages, workspace):
     B, Hq, D = q.shape
-    need = kvq_decode_workspace_bytes(B, Hq, Hkv, D, max_context_len, partition_pages)
+    key = (B, Hq, Hkv, D, int(max_context_len), int(partition_pages))
+    need = _ws_need.get(key)
+    if need is None:
+        need = kvq_decode_workspace_bytes(B, Hq, Hkv, D, max_context_len, partition_pages)
+        if len(_ws_need) < 4096:
+            _ws_need[key] = need
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
