@@ -141,7 +141,9 @@ kvq_status kvq_quantize_append(const void* k, const void* v, int64_t k_token_str
  *                   GPU.  NULL (or 0 bytes): no split-K -- one warp per
  *                   (sequence, KV head), correct but unbalanced.  A smaller
  *                   non-zero size is accepted down to four work ranges and
- *                   only lowers the number of warps used.
+ *                   only lowers the number of warps used.  Calls whose
+ *                   sequences all fit in four pages (max_context_len <= 64)
+ *                   never split and do not touch it.
  * Work distribution: the (sequence, KV head, page) tiles form one stream,
  * cut into ranges of R = max(4, ceil(tiles / warps)) pages from the exact
  * context lengths, one range per resident warp, so every warp reads the same
@@ -160,8 +162,9 @@ kvq_status kvq_paged_decode(const void* q, kvq_dtype dtype, int32_t num_seqs,
 
 /* Scratch bytes for kvq_paged_decode (and kvq_paged_decode_kv16) with these
  * sizes on the current device: two partial slots of G rows per work range,
- * one range per resident warp.  0 when no sequence can span two pages or on
- * invalid sizes. */
+ * one range per resident warp.  0 when no sequence can hold more than four
+ * pages (max_context_len <= 64: the call then never splits) or on invalid
+ * sizes. */
 size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len);
 

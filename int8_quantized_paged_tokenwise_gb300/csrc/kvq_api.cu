@@ -333,7 +333,10 @@ kvq_status decode_common(Dec var, const void* q, kvq_dtype dtype, int32_t B, int
   DecodeParams p{};
   WsLayout wl;
   int64_t grid = 0;
-  if (R == 0 && (ws == nullptr || ws_bytes == 0 || pages_max <= 1)) {
+  // no split without a workspace, or when no sequence has more pages than the
+  // shortest range: such a sequence would gain at most a few pieces, less
+  // than the merge launch costs
+  if (R == 0 && (ws == nullptr || ws_bytes == 0 || pages_max <= kMinRangePages)) {
     p.R = -1;                                       // one unit per (sequence, head group)
     p.range_cap = 0;
     grid = cdiv((int64_t)B * HU, kWarps);
@@ -832,7 +835,7 @@ size_t kvq_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
       num_q_heads % num_kv_heads || (head_dim != 64 && head_dim != 128) ||
       num_q_heads / num_kv_heads > kMaxGroup || num_seqs > kMaxSeqs)
     return 0;
-  if (cdiv(max_context_len, kBlockSize) <= 1) return 0;   // nothing can be split
+  if (cdiv(max_context_len, kBlockSize) <= kMinRangePages) return 0;   // never split
   DeviceState* st = device_state();
   if (!st) return 0;
   const int32_t G = num_q_heads / num_kv_heads;

@@ -139,13 +139,15 @@ def test_noalloc_serving_mix_beyond_the_recommended_workspace():
 def test_noalloc_refuses_shapes_without_one_range_per_kv_head():
     """8 (G) x 2100 KV heads at D = 128 need 2100 ranges of 8,256 bytes
     (17.3 MB) even at one range per KV head: refused before anything runs
-    (the small tensors below are never read)."""
+    (the small tensors below are never read).  The context bound (1024
+    tokens, 64 pages) is past the no-split limit of four pages, so the call
+    takes the split path that needs the scratch."""
     L = kvq.load()
     x = torch.zeros(4096, dtype=torch.uint8, device="cuda")
     p = P(x.data_ptr())
     Hkv, G = 2100, 8
-    st = L.kvq_paged_decode_noalloc(p, 1, 1, G * Hkv, Hkv, 128, p, p, p, p, 4, 16, p, 4, p, 64,
-                                    0.1, p, None)
+    st = L.kvq_paged_decode_noalloc(p, 1, 1, G * Hkv, Hkv, 128, p, p, p, p, 64, 16, p, 64, p,
+                                    1024, 0.1, p, None)
     assert st == 4                            # KVQ_ERR_WORKSPACE_TOO_SMALL
     torch.cuda.synchronize()
     assert kvq.kvq_get_error() == (0, 0)
