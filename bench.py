@@ -14,8 +14,10 @@ kvq_paged_decode_kv16) for the steps/s A/B, and through the C ABI with host
 buffers (pinned H2D of the step's inputs and D2H of the output inside the
 timed region) for the end-to-end figure.  ``configs`` repeats the INT8 and
 twin timings on all five workloads (tiny, canonical, long, mha, serving).
-L2 is flushed (512 MB write) between timed steps; each step is timed with
-CUDA events on the launching stream.  A context sweep (2K/8K/32K, 16
+L2 is flushed between timed steps (a 512 MB write, then a 512 MB read of
+another buffer, so that the write's dirty lines are written back before the
+step rather than inside it); each step is timed with CUDA events on the
+launching stream.  A context sweep (2K/8K/32K, 16
 sequences) compares the INT8 decode with the twin, and the chunked prefill
 over the INT8 cache is timed on an 8K-token causal chunk (GQA 8).  The FP64
 CPU oracle is timed on a bounded sample of the headline workload as the CPU
@@ -51,10 +53,25 @@ import workloads as W  # noqa: E402
 METRIC = "INT8-KV paged decode HBM GB/s (% of GB300 peak); decode steps/s vs BF16 KV"
 UNIT = "GB/s"
 FLUSH_BYTES = 512 << 20
+
+
+def make_flush(torch, dev):
+    """The L2 flush between timed steps: write a buffer four times the L2,
+    then read another as large.  The write alone would leave the L2 full of
+    dirty lines whose write-back then lands inside the next timed kernel;
+    after the read the L2 holds clean lines of neither the workload nor the
+    write."""
+    wbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        wbuf.zero_()
+        rbuf.max()
+    return flush
 FALLBACK_HBM_GBS = 6800.0
 # the kernels whose DRAM traffic the committed ncu summaries measured
 DECODE_SOURCES = ("kvq_decode.cuh", "kvq_decode_int8.cu", "kvq_decode_int8_h2.cu",
-                  "kvq_decode_int8_t2.cu", "kvq_ptx.cuh", "kvq_combine.cu")
+                  "kvq_decode_int8_t2.cu", "kvq_ptx.cuh", "kvq_combine.cu", "kvq_api.cu")
 HEADLINE = "mha"
 
 
@@ -166,7 +183,7 @@ def config_of(w: W.Workload, extra=None):
          "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
          "kv_dtype": "int8+fp16-scale", "act_dtype": w.dtype,
          "context_tokens": int(w.context_lens.sum()), "max_context": w.max_context_len,
-         "append_tokens_per_step": w.append_tokens(), "l2": "flushed (512 MB write) between steps"}
+         "append_tokens_per_step": w.append_tokens(), "l2": "flushed between steps: 512 MB written, then 512 MB of another buffer read"}
     if extra:
         c.update(extra)
     return c
@@ -779,8 +796,7 @@ def profile_arm(torch, w, dev, args):
         w = W.first_seqs(w, args.profile_seqs)
     kv16 = args.profile_arm == "kv16"
     g = GpuWorkload(w, dev, arms=("kv16",) if kv16 else ("int8",))
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush = lambda: flush_buf.zero_()  # noqa: E731
+    flush = make_flush(torch, dev)
     nop = lambda: None  # noqa: E731
     dec = {"int8": g.decode_int8, "kv16": g.decode_kv16,
            "int8cc": g.decode_int8_cuda_cores}[args.profile_arm]
@@ -812,9 +828,8 @@ def main():
     kvq.load(build_if_missing=False)
 
     if args.prefill:
-        flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
         names = list(PREFILL_SHAPES) if args.prefill == "all" else [args.prefill]
-        for r in prefill_measure(torch, kvq, dev, lambda: flush_buf.zero_(), names,
+        for r in prefill_measure(torch, kvq, dev, make_flush(torch, dev), names,
                                  args.steps, args.warmup):
             print(json.dumps({"prefill": r}), flush=True)
         return
@@ -823,8 +838,7 @@ def main():
         profile_arm(torch, w, dev, args)
         return
     g = GpuWorkload(w, dev)
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush = lambda: flush_buf.zero_()  # noqa: E731
+    flush = make_flush(torch, dev)
 
     def barrier():
         torch.cuda.synchronize()

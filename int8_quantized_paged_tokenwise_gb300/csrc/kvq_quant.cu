@@ -13,9 +13,8 @@
 // exact quotient of a 16-bit value by 127 is either an FP16 value or at least
 // 2^-17 (relative) away from every FP16 value, far above the 2^-24 FP32
 // rounding error, so __float2half_ru gives the exact upward rounding.
-// x / s is also __fdiv_rn: away from an exact tie the exact quotient is at
-// least ~2^-12 from any k + 1/2, and an exact tie is representable, so
-// rintf (round half to even) of the FP32 quotient equals the exact rounding.
+// The code is the exact quotient x / s rounded half to even, found from an
+// approximate reciprocal and an exact FMA remainder (quant_code below).
 // No fast-math and no flush-to-zero: bf16 subnormal rows must keep a > 0.
 #include "kvq_internal.h"
 #include "kvq_ptx.cuh"
@@ -45,19 +44,56 @@ __device__ __forceinline__ uint16_t row_scale_bits(uint32_t amax_bits) {
   return s;
 }
 
-// Four 16-bit values -> four int8 codes packed little-endian.
+// The code of x: the exact quotient x / s rounded half to even, clamped to
+// +-127, without a division.  x * inv (inv ~ 1/s) is limited to +-256 (only a
+// saturated scale lets the quotient leave +-127 by more than rounding) and
+// rounded to an integer k by adding M = 1.5 * 2^23, which leaves k in the low
+// mantissa bits of t; k is within one of the answer.  The remainder x - k s
+// is exact in one FMA (for |k| <= 128, k s has at most 19 significant bits
+// and x - k s at most 12), and the quotient is k + r/s: k moves by one when
+// |r| > s/2, and on an exact tie |r| = s/2 towards the even neighbour.  For
+// |k| > 128 only the clamp to +-127 matters.
+// SAT: the scale saturated at 65504, so |x / s| may exceed 127 (else the
+// row's largest magnitude maps to at most 127 and neither clamp is needed).
+template <bool SAT>
+__device__ __forceinline__ int quant_code(float x, float s, float h, float inv) {
+  constexpr float kM = 12582912.0f;              // 1.5 * 2^23
+  float q = x * inv;
+  if constexpr (SAT) q = fminf(fmaxf(q, -256.0f), 256.0f);
+  const float t = q + kM;
+  const float k = t - kM;
+  int ki = (int)(__float_as_uint(t) - 0x4B400000u);   // k as an integer (|k| < 2^22)
+  const float r = fmaf(-k, s, x);
+  const bool odd = (ki & 1) != 0;
+  ki += (r > h || (r == h && odd)) ? 1 : 0;
+  ki -= (r < -h || (r == -h && odd)) ? 1 : 0;
+  if constexpr (SAT) ki = min(max(ki, -127), 127);
+  return ki;
+}
+
+template <bool BF16, bool SAT>
+__device__ __forceinline__ uint32_t quantize4_as(uint2 x, float s, float inv) {
+  const float h = 0.5f * s;
+  const uint32_t c0 = (uint32_t)quant_code<SAT>(bits_to_float<BF16>(x.x & 0xFFFFu), s, h, inv);
+  const uint32_t c1 = (uint32_t)quant_code<SAT>(bits_to_float<BF16>(x.x >> 16), s, h, inv);
+  const uint32_t c2 = (uint32_t)quant_code<SAT>(bits_to_float<BF16>(x.y & 0xFFFFu), s, h, inv);
+  const uint32_t c3 = (uint32_t)quant_code<SAT>(bits_to_float<BF16>(x.y >> 16), s, h, inv);
+  return __byte_perm(__byte_perm(c0, c1, 0x0040u), __byte_perm(c2, c3, 0x0040u), 0x5410u);
+}
+
+// Four 16-bit values -> four int8 codes packed little-endian (scale bits sb).
 template <bool BF16>
-__device__ __forceinline__ uint32_t quantize4(uint2 x, float s) {
-  uint32_t out = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const uint32_t w = (e < 2) ? x.x : x.y;
-    const uint32_t b = (e & 1) ? (w >> 16) : (w & 0xFFFFu);
-    float r = rintf(__fdiv_rn(bits_to_float<BF16>(b), s));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    out |= (uint32_t)((int)r & 0xFF) << (8 * e);
-  }
-  return out;
+__device__ __forceinline__ uint32_t quantize4(uint2 x, uint16_t sb, float s, float inv) {
+  return sb == 0x7BFFu ? quantize4_as<BF16, true>(x, s, inv)
+                       : quantize4_as<BF16, false>(x, s, inv);
+}
+
+// An approximate reciprocal is enough for quant_code: its error (a few ulp)
+// moves x * inv by far less than one for |x / s| <= 128.
+__device__ __forceinline__ float approx_rcp(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t mag_max4(uint2 x) {
@@ -69,61 +105,100 @@ __device__ __forceinline__ uint32_t mag_max4(uint2 x) {
 // One group of D/4 lanes per (token, KV head) row; each lane owns four
 // consecutive elements (one 8-byte load of K and of V, one 4-byte store of
 // codes each).  Rows of one warp are adjacent heads of a token, so the
-// 16-bit loads and the int8 stores of a warp are contiguous runs.
+// 16-bit loads and the int8 stores of a warp are contiguous runs.  Each warp
+// takes kRowPasses such passes and issues every load of them (slots, K and V
+// rows) before it uses any, so that a warp keeps several rows' loads in
+// flight instead of waiting for one row's slot, then its values.
+constexpr int kRowPasses = 4;
+
+template <int D>
+struct RowTask {
+  static constexpr int LPR = D / 4;               // lanes per row
+  static constexpr int RPW = 32 / LPR;            // rows per warp pass
+  int64_t row[kRowPasses], t[kRowPasses], slot[kRowPasses];
+  int j[kRowPasses];
+  int sub;
+  // this thread's rows and their slots, K and V words, all loads in flight
+  __device__ __forceinline__ void load(const QuantParams& p, uint2 (&kx)[kRowPasses],
+                                       uint2 (&vx)[kRowPasses]) {
+    const int lane = threadIdx.x & 31;
+    sub = lane % LPR;
+    const int64_t wg = ((int64_t)blockIdx.x * kQuantThreads + threadIdx.x) / 32;
+    const int64_t row0 = wg * (kRowPasses * RPW) + lane / LPR;
+    // (token, head) of the first row by one division, the next ones by steps
+    int64_t tt = row0 / p.num_kv_heads;
+    int jj = (int)(row0 - tt * p.num_kv_heads);
+#pragma unroll
+    for (int i = 0; i < kRowPasses; ++i) {
+      row[i] = row0 + i * RPW;
+      slot[i] = -1;
+      t[i] = tt;
+      j[i] = jj;
+      kx[i] = vx[i] = make_uint2(0, 0);
+      jj += RPW;
+      while (jj >= p.num_kv_heads) {              // RPW <= 2: at most two turns
+        jj -= p.num_kv_heads;
+        ++tt;
+      }
+      if (row[i] < p.num_rows) {
+        slot[i] = p.slots[t[i]];
+        const uint16_t* kr =
+            static_cast<const uint16_t*>(p.k) + t[i] * p.k_stride + (int64_t)j[i] * D;
+        const uint16_t* vr =
+            static_cast<const uint16_t*>(p.v) + t[i] * p.v_stride + (int64_t)j[i] * D;
+        kx[i] = __ldg(reinterpret_cast<const uint2*>(kr) + sub);
+        vx[i] = __ldg(reinterpret_cast<const uint2*>(vr) + sub);
+      }
+    }
+  }
+  // whether row i is written; a slot past the cache sets the error bit
+  __device__ __forceinline__ bool active(const QuantParams& p, int i) const {
+    if (row[i] >= p.num_rows || slot[i] < 0) return false;
+    if (slot[i] >= p.num_slots) {
+      if (sub == 0) atomicOr(p.err, 0x1u);
+      return false;
+    }
+    return true;
+  }
+  // payload row of row i in the cache [NB][Hkv][bs]
+  __device__ __forceinline__ int64_t cache_row(const QuantParams& p, int i) const {
+    const int64_t blk = slot[i] / kBlockSize, off = slot[i] % kBlockSize;
+    return (blk * p.num_kv_heads + j[i]) * kBlockSize + off;
+  }
+};
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const QuantParams p) {
-  constexpr int LPR = D / 4;  // lanes per row
-  const int lane = threadIdx.x & 31;
-  const int64_t gthread = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
-  const int64_t row = gthread / LPR;
-  const int sub = lane % LPR;
-  const bool in_range = row < p.num_rows;
+  constexpr int LPR = D / 4;
   // the next kernel in the stream (a decode launched with programmatic stream
   // serialization) may be scheduled now; it waits for this grid's completion
   griddep_launch_dependents();
-
-  int64_t t = 0, slot = -1;
-  int j = 0;
-  if (in_range) {
-    t = row / p.num_kv_heads;
-    j = (int)(row - t * p.num_kv_heads);
-    slot = p.slots[t];
-    if (slot >= p.num_slots) {
-      if (sub == 0) atomicOr(p.err, 0x1u);
-      slot = -1;
-    }
-  }
-  const bool active = slot >= 0;
-
-  uint2 kx = make_uint2(0, 0), vx = make_uint2(0, 0);
-  if (active) {
-    const uint16_t* kr = static_cast<const uint16_t*>(p.k) + t * p.k_stride + (int64_t)j * D;
-    const uint16_t* vr = static_cast<const uint16_t*>(p.v) + t * p.v_stride + (int64_t)j * D;
-    kx = __ldg(reinterpret_cast<const uint2*>(kr) + sub);
-    vx = __ldg(reinterpret_cast<const uint2*>(vr) + sub);
-  }
-  uint32_t km = mag_max4(kx), vm = mag_max4(vx);
+  RowTask<D> rt;
+  uint2 kx[kRowPasses], vx[kRowPasses];
+  rt.load(p, kx, vx);
 #pragma unroll
-  for (int off = LPR / 2; off > 0; off >>= 1) {
-    km = max(km, __shfl_xor_sync(0xFFFFFFFFu, km, off));
-    vm = max(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, off));
-  }
-  if (!active) return;
-
-  const uint16_t ks = row_scale_bits<BF16>(km);
-  const uint16_t vs = row_scale_bits<BF16>(vm);
-  const float ksf = __half2float(__ushort_as_half(ks));
-  const float vsf = __half2float(__ushort_as_half(vs));
-
-  const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-  const int64_t crow = (blk * p.num_kv_heads + j) * kBlockSize + off;  // [NB][Hkv][bs]
-  reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.k_cache) + crow * D)[sub] =
-      quantize4<BF16>(kx, ksf);
-  reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.v_cache) + crow * D)[sub] =
-      quantize4<BF16>(vx, vsf);
-  if (sub == 0) {
-    p.k_scale[crow] = ks;
-    p.v_scale[crow] = vs;
+  for (int i = 0; i < kRowPasses; ++i) {
+    const bool act = rt.active(p, i);
+    uint32_t km = mag_max4(kx[i]), vm = mag_max4(vx[i]);
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) {
+      km = max(km, __shfl_xor_sync(0xFFFFFFFFu, km, off));
+      vm = max(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, off));
+    }
+    if (!act) continue;
+    const uint16_t ks = row_scale_bits<BF16>(km);
+    const uint16_t vs = row_scale_bits<BF16>(vm);
+    const float ksf = __half2float(__ushort_as_half(ks));
+    const float vsf = __half2float(__ushort_as_half(vs));
+    const int64_t crow = rt.cache_row(p, i);
+    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.k_cache) + crow * D)[rt.sub] =
+        quantize4<BF16>(kx[i], ks, ksf, approx_rcp(ksf));
+    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.v_cache) + crow * D)[rt.sub] =
+        quantize4<BF16>(vx[i], vs, vsf, approx_rcp(vsf));
+    if (rt.sub == 0) {
+      p.k_scale[crow] = ks;
+      p.v_scale[crow] = vs;
+    }
   }
 }
 
@@ -137,68 +212,50 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kQuantThreads) quantize_static_kernel(const QuantParams p,
                                                                          float inv_k,
                                                                          float inv_v) {
-  constexpr int LPR = D / 4;  // lanes per row
-  const int64_t gthread = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
-  const int64_t row = gthread / LPR;
-  const int sub = (threadIdx.x & 31) % LPR;
   griddep_launch_dependents();
-  if (row >= p.num_rows) return;
-  const int64_t t = row / p.num_kv_heads;
-  const int j = (int)(row - t * p.num_kv_heads);
-  const int64_t slot = p.slots[t];
-  if (slot < 0) return;
-  if (slot >= p.num_slots) {
-    if (sub == 0) atomicOr(p.err, 0x1u);
-    return;
-  }
-  const uint16_t* kr = static_cast<const uint16_t*>(p.k) + t * p.k_stride + (int64_t)j * D;
-  const uint16_t* vr = static_cast<const uint16_t*>(p.v) + t * p.v_stride + (int64_t)j * D;
-  const uint2 kx = __ldg(reinterpret_cast<const uint2*>(kr) + sub);
-  const uint2 vx = __ldg(reinterpret_cast<const uint2*>(vr) + sub);
-  const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-  const int64_t crow = (blk * p.num_kv_heads + j) * kBlockSize + off;
-  uint32_t kq = 0, vq = 0;
+  RowTask<D> rt;
+  uint2 kx[kRowPasses], vx[kRowPasses];
+  rt.load(p, kx, vx);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const uint32_t kw = (e < 2) ? kx.x : kx.y, vw = (e < 2) ? vx.x : vx.y;
-    const uint32_t kb = (e & 1) ? (kw >> 16) : (kw & 0xFFFFu);
-    const uint32_t vb = (e & 1) ? (vw >> 16) : (vw & 0xFFFFu);
-    const float kr8 = fminf(fmaxf(rintf(__fmul_rn(bits_to_float<BF16>(kb), inv_k)), -127.f), 127.f);
-    const float vr8 = fminf(fmaxf(rintf(__fmul_rn(bits_to_float<BF16>(vb), inv_v)), -127.f), 127.f);
-    kq |= (uint32_t)((int)kr8 & 0xFF) << (8 * e);
-    vq |= (uint32_t)((int)vr8 & 0xFF) << (8 * e);
+  for (int i = 0; i < kRowPasses; ++i) {
+    if (!rt.active(p, i)) continue;
+    const int64_t crow = rt.cache_row(p, i);
+    uint32_t kq = 0, vq = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t kw = (e < 2) ? kx[i].x : kx[i].y, vw = (e < 2) ? vx[i].x : vx[i].y;
+      const uint32_t kb = (e & 1) ? (kw >> 16) : (kw & 0xFFFFu);
+      const uint32_t vb = (e & 1) ? (vw >> 16) : (vw & 0xFFFFu);
+      const float kr8 =
+          fminf(fmaxf(rintf(__fmul_rn(bits_to_float<BF16>(kb), inv_k)), -127.f), 127.f);
+      const float vr8 =
+          fminf(fmaxf(rintf(__fmul_rn(bits_to_float<BF16>(vb), inv_v)), -127.f), 127.f);
+      kq |= (uint32_t)((int)kr8 & 0xFF) << (8 * e);
+      vq |= (uint32_t)((int)vr8 & 0xFF) << (8 * e);
+    }
+    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.k_cache) + crow * D)[rt.sub] = kq;
+    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.v_cache) + crow * D)[rt.sub] = vq;
   }
-  reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.k_cache) + crow * D)[sub] = kq;
-  reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.v_cache) + crow * D)[sub] = vq;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) append_kv16_kernel(const QuantParams p) {
-  constexpr int LPR = D / 4;
-  const int64_t gthread = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x;
-  const int64_t row = gthread / LPR;
-  const int sub = (threadIdx.x & 31) % LPR;
-  if (row >= p.num_rows) return;
-  const int64_t t = row / p.num_kv_heads;
-  const int j = (int)(row - t * p.num_kv_heads);
-  const int64_t slot = p.slots[t];
-  if (slot < 0) return;
-  if (slot >= p.num_slots) {
-    if (sub == 0) atomicOr(p.err, 0x1u);
-    return;
+  RowTask<D> rt;
+  uint2 kx[kRowPasses], vx[kRowPasses];
+  rt.load(p, kx, vx);
+#pragma unroll
+  for (int i = 0; i < kRowPasses; ++i) {
+    if (!rt.active(p, i)) continue;
+    const int64_t crow = rt.cache_row(p, i);
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.k_cache) + crow * D)[rt.sub] = kx[i];
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.v_cache) + crow * D)[rt.sub] = vx[i];
   }
-  const uint16_t* kr = static_cast<const uint16_t*>(p.k) + t * p.k_stride + (int64_t)j * D;
-  const uint16_t* vr = static_cast<const uint16_t*>(p.v) + t * p.v_stride + (int64_t)j * D;
-  const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-  const int64_t crow = (blk * p.num_kv_heads + j) * kBlockSize + off;
-  reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.k_cache) + crow * D)[sub] =
-      __ldg(reinterpret_cast<const uint2*>(kr) + sub);
-  reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.v_cache) + crow * D)[sub] =
-      __ldg(reinterpret_cast<const uint2*>(vr) + sub);
 }
 
+// CTAs for `rows` rows: warps of kRowPasses passes of 32 / (D / 4) rows each.
 inline int grid_for(int64_t rows, int D) {
-  const int64_t threads = rows * (D / 4);
+  const int64_t per_warp = (int64_t)kRowPasses * (32 / (D / 4));
+  const int64_t threads = (rows + per_warp - 1) / per_warp * 32;
   return (int)((threads + kQuantThreads - 1) / kQuantThreads);
 }
 

@@ -17,6 +17,11 @@
   biased exponent in the decode, FP32 in the prefill) stays below 2 (times
   the prefill's 2^8 lazy-rescale slack), far inside FP16, for every FP16
   scale, where code * s_v itself can exceed 65504.
+- The quantizer rounds x / s half to even without a division: k = rint(x
+  times an approximate reciprocal of s) is within one of the answer, the
+  remainder x - k s is exact in one FMA, and its comparison with s / 2 (ties
+  to the even neighbour) gives the answer; checked for every fp16 and bf16
+  value against scales from the smallest subnormal to 65504.
 - The static-scale decode folds the K scale into the score scale and the V
   scale into the output; the tokenwise one multiplies the scale after the
   integer dot product: both are re-associations of the same product, checked
@@ -103,3 +108,57 @@ def test_v_scale_on_p_stays_inside_fp16():
     with np.errstate(over="ignore"):
         big = (127.0 * s).astype(np.float16)
     assert np.isinf(big).sum() > 0 and not np.isinf(r16.astype(np.float16)).any()
+
+
+
+def _quant_code_f32(x, s, inv, sat=True):
+    """The quantizer's division-free code, step by step in float32: q = x *
+    inv limited to +-256, k = rint(q) by adding 1.5 * 2^23 (k read back as an
+    integer from the sum's bits), the remainder x - k s (one FMA: exact while
+    |k| <= 128), one step towards the exact quotient's round-half-even
+    neighbour, and the clamp to +-127."""
+    x = x.astype(np.float32)
+    s, inv = np.float32(s), np.float32(inv)
+    q = (x * inv).astype(np.float32)
+    if sat:                                   # a saturated scale: the quotient may pass 127
+        q = np.clip(q, -256, 256).astype(np.float32)
+    big = np.float32(12582912.0)
+    t = (q + big).astype(np.float32)
+    k = (t - big).astype(np.float32)
+    ki = t.view(np.uint32).astype(np.int64) - 0x4B400000
+    r64 = x.astype(np.float64) - k.astype(np.float64) * np.float64(s)
+    inb = np.abs(k) <= 128
+    assert np.all(r64[inb].astype(np.float32).astype(np.float64) == r64[inb])   # FMA exact
+    r = r64.astype(np.float32)
+    h = np.float32(0.5) * s
+    odd = (ki & 1) != 0
+    ki = ki + ((r > h) | ((r == h) & odd)) - ((r < -h) | ((r == -h) & odd))
+    return np.clip(ki, -127, 127) if sat else ki
+
+
+def test_quantizer_rounding_without_division_is_exact():
+    # every finite fp16 and bf16 value against FP16 scales from subnormal to
+    # saturated, with the reciprocal off by up to two ulp (the kernel takes an
+    # approximate one)
+    bits = np.arange(0, 1 << 16, dtype=np.uint32)
+    f16 = bits.astype(np.uint16).view(np.float16).astype(np.float32)
+    b16 = (bits << 16).view(np.float32)
+    scales = [np.float16(v) for v in (2.0 ** -24, 2.0 ** -14, 0.0372, 0.5, 1.0, 3.0, 258.0,
+                                      4097.0, 65504.0)]
+    for xs in (f16, b16):
+        xs = xs[np.isfinite(xs)]
+        for sc in scales:
+            s = np.float32(sc)
+            want = np.clip(np.rint(xs.astype(np.float64) / np.float64(s)), -127, 127)
+            for ulps in (-2, 0, 2):
+                inv = np.float32(1) / s
+                for _ in range(abs(ulps)):
+                    inv = np.nextafter(inv, np.float32(np.inf if ulps > 0 else -np.inf),
+                                       dtype=np.float32)
+                with np.errstate(over="ignore", invalid="ignore"):
+                    got = _quant_code_f32(xs, s, inv)
+                assert np.array_equal(got, want), (float(s), ulps)
+                # an unsaturated scale bounds the row's quotients by 127: no clamps
+                inside = np.abs(xs.astype(np.float64)) <= 127 * np.float64(s)
+                got = _quant_code_f32(xs[inside], s, inv, sat=False)
+                assert np.array_equal(got, want[inside]), (float(s), ulps, "unsaturated")

@@ -326,3 +326,27 @@ def test_decode_without_workspace_and_with_a_small_one():
                                    w.sm_scale, workspace=small)
         _check_all(case, out, what=f"small workspace ({nbytes} B)")
     assert kvq.kvq_get_error() == (0, 0)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [(8, 2, 128, "bf16"), (4, 4, 64, "fp16")])
+def test_decode_short_contexts_take_the_unsplit_path(Hq, Hkv, D, dtype):
+    """Contexts of at most four pages (64 tokens) are never split: with the
+    recommended workspace (0 bytes for such calls) and with a large one the
+    output is the no-workspace output bit for bit, and every sequence matches
+    the oracle; a 65-token bound goes back to the split path."""
+    lens = [0, 1, 15, 16, 17, 33, 48, 63, 64] * 3
+    w = W.custom(len(lens), Hq, Hkv, D, dtype, lens, seed=91 + Hq)
+    assert w.max_context_len <= 64
+    case = Case(w)
+    case.write_prefix()
+    assert kvq.kvq_decode_workspace_bytes(w.num_seqs, Hq, Hkv, D, w.max_context_len) == 0
+    none = torch.empty(0, dtype=torch.uint8, device="cuda")
+    ref = kvq.kvq_paged_decode(case.q, *case.int8, case.bt, case.cl, w.max_context_len,
+                               w.sm_scale, workspace=none)
+    _check_all(case, ref, what="short contexts")
+    big = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    out = kvq.kvq_paged_decode(case.q, *case.int8, case.bt, case.cl, w.max_context_len,
+                               w.sm_scale, workspace=big)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert kvq.kvq_decode_workspace_bytes(w.num_seqs, Hq, Hkv, D, 65) > 0
+    assert kvq.kvq_get_error() == (0, 0)
