@@ -42,7 +42,7 @@ COS_MIN = 0.9999     # cosine similarity bound
 
 
 def assert_attention_close(gpu_bits: np.ndarray, ref: np.ndarray, dtype: str, what="",
-                           v_scale: float = 1.0):
+                           v_scale: float = 1.0, atol_extra: float = 0.0):
     """|gpu - oracle| <= 2e-3 * v_scale + half an output ulp elementwise,
     cosine >= 0.9999.
 
@@ -51,11 +51,13 @@ def assert_attention_close(gpu_bits: np.ndarray, ref: np.ndarray, dtype: str, wh
     magnitude ~1 it alone is up to 3.9e-3.  ``v_scale``: the values V were
     multiplied by a power of two v_scale (the workloads' V is N(0,1)-sized);
     attention is linear in V and such a factor leaves every code unchanged
-    and multiplies every scale by it, so the absolute bound scales with it."""
+    and multiplies every scale by it, so the absolute bound scales with it.
+    ``atol_extra``: a further absolute allowance a caller derives for its own
+    arithmetic (the BF16 twin's BF16 softmax weights)."""
     g = bits_f64(gpu_bits, dtype)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
     err = np.abs(g - ref)
-    tol = ATOL * v_scale + 0.5 * ulp(ref, dtype)
+    tol = ATOL * v_scale + atol_extra + 0.5 * ulp(ref, dtype)
     bad = err > tol
     assert not bad.any(), (f"{what}: {int(bad.sum())} elements out of tolerance, "
                            f"max err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}")
