@@ -15,7 +15,12 @@ namespace {
 
 constexpr int kCombineWarps = 8;
 constexpr int kCombineThreads = kCombineWarps * 32;
-constexpr int kCombineBatch = 16;  // pieces a lane loads before using any
+constexpr int kCombineBatch = 8;   // pieces a lane loads before using any
+// CTAs resident per SM the register budget is set for (64 registers): the
+// merge is a chain of dependent L2 loads per pair, so the number of warps in
+// flight sets its speed (measured on GB300: 8 pieces per batch and 4 CTAs per
+// SM took the serving mix's merge from ~11 to ~7 us after the decode)
+constexpr int kCombineMinCtas = 4;
 
 // Every CTA first rebuilds, from context_lens, the page prefix and range
 // length the decode kernel used (this overlaps the decode's tail: the launch
@@ -91,7 +96,8 @@ __device__ __forceinline__ void store_out(const CombineParams& p, int b, int h, 
   else *reinterpret_cast<uint32_t*>(dst) = pk[0];
 }
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kCombineThreads, kCombineMinCtas)
+    combine_kernel(const CombineParams p) {
   constexpr int E = D / 32;                      // dims per lane
   __shared__ int s_prefix[kMaxSeqs];
   __shared__ int s_warp[kCombineWarps];
@@ -208,7 +214,7 @@ cudaError_t combine_launch(int D, bool bf16, const CombineParams& p, int sms, cu
   if (p.B == 0 || p.Hq == 0) return cudaSuccess;
   const int64_t pairs = (int64_t)p.B * p.Hq;
   const int64_t want = p.per_cta ? pairs : (pairs + kCombineWarps - 1) / kCombineWarps;
-  const int64_t cap = 2 * (int64_t)sms;
+  const int64_t cap = 2 * kCombineMinCtas * (int64_t)sms;   // two waves at most
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(want < cap ? want : cap));
   cfg.blockDim = dim3(kCombineThreads);
