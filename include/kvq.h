@@ -211,7 +211,8 @@ size_t kvq_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
  * rows of one KV head, so the grid is ceil(max_query_len / (256 / G)) x
  * num_kv_heads x num_seqs.
  *
- *   q, out          [total_q][num_q_heads][head_dim] of `dtype`, 16-byte aligned.
+ *   q, out          [total_q][num_q_heads][head_dim] of `dtype`, 16-byte aligned
+ *                   (may be null when total_q == 0: nothing is launched).
  *   query_start     device int32 [num_seqs + 1], non-decreasing, from 0.
  *   total_q         rows of q and out; a sequence whose queries fall outside
  *                   them is flagged (KVQ_DEVERR_CONTEXT) and skipped.

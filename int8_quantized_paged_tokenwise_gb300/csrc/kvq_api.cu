@@ -269,12 +269,14 @@ bool make_map(DeviceState* st, CUtensorMap* m, const void* base, int elem_bytes,
   return true;
 }
 
-// Shared validation of the decode arguments (both caches).
+// Shared validation of the decode arguments (both caches).  `rows`: q and
+// out hold at least one row (a prefill without queries passes false, and
+// its q and out may be null).
 kvq_status check_decode(const void* q, kvq_dtype dtype, int32_t B, int32_t Hq, int32_t Hkv,
                         int32_t D, const void* kc, const void* vc, const void* ks,
                         const void* vs, bool planes, int32_t num_blocks, int32_t bs,
                         const int32_t* bt, int32_t max_blocks, const int32_t* cl,
-                        int32_t max_ctx, float sm_scale, const void* out) {
+                        int32_t max_ctx, float sm_scale, const void* out, bool rows = true) {
   if (dtype != KVQ_FP16 && dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARGUMENT;
   if (B < 0 || Hq <= 0 || Hkv <= 0 || num_blocks <= 0 || max_ctx < 0)
     return KVQ_ERR_INVALID_ARGUMENT;
@@ -288,10 +290,11 @@ kvq_status check_decode(const void* q, kvq_dtype dtype, int32_t B, int32_t Hq, i
   if (B == 0) return KVQ_OK;
   if (max_blocks <= 0) return KVQ_ERR_INVALID_ARGUMENT;
   if ((int64_t)max_ctx > (int64_t)max_blocks * kBlockSize) return KVQ_ERR_INVALID_ARGUMENT;
-  if (!q || !kc || !vc || !bt || !cl || !out) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!kc || !vc || !bt || !cl) return KVQ_ERR_INVALID_ARGUMENT;
+  if (rows && (!q || !out || !aligned(q, 16) || !aligned(out, 16)))
+    return KVQ_ERR_INVALID_ARGUMENT;
   if (planes && (!ks || !vs)) return KVQ_ERR_INVALID_ARGUMENT;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(kc, 16) || !aligned(vc, 16) ||
-      !aligned(bt, 4) || !aligned(cl, 4))
+  if (!aligned(kc, 16) || !aligned(vc, 16) || !aligned(bt, 4) || !aligned(cl, 4))
     return KVQ_ERR_INVALID_ARGUMENT;
   if (planes && (!aligned(ks, 16) || !aligned(vs, 16))) return KVQ_ERR_INVALID_ARGUMENT;
   return KVQ_OK;
@@ -754,13 +757,13 @@ kvq_status kvq_paged_prefill(const void* q, kvq_dtype dtype, int32_t num_seqs,
                              const int32_t* context_lens, int32_t max_context_len,
                              const int32_t* query_start, int32_t total_q, int32_t max_query_len,
                              float sm_scale, void* out, kvq_stream_t stream) {
+  if (max_query_len < 0 || total_q < 0) return KVQ_ERR_INVALID_ARGUMENT;
   kvq_status s = check_decode(q, dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, k_cache,
                               v_cache, k_scale, v_scale, true, num_blocks, block_size,
                               block_tables, max_blocks_per_seq, context_lens, max_context_len,
-                              sm_scale, out);
+                              sm_scale, out, total_q > 0);
   if (s != KVQ_OK || num_seqs == 0) return s;
-  if (!query_start || !aligned(query_start, 4) || max_query_len < 0 || total_q < 0)
-    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!query_start || !aligned(query_start, 4)) return KVQ_ERR_INVALID_ARGUMENT;
   if (max_query_len == 0 || total_q == 0) return KVQ_OK;
   if (num_kv_heads > 65535 || num_seqs > 65535 || max_blocks_per_seq > INT32_MAX / kBlockSize)
     return KVQ_ERR_UNSUPPORTED;

@@ -1,10 +1,12 @@
-"""Seeded random shapes against the FP64 oracle: for each case a random
+"""Seeded random shapes against the FP64 oracle.  Decode: for each case a random
 batch, GQA ratio, head dim, dtype and ragged context lengths (including empty
 and single-token sequences), appended (codes and scales read back through the
 block tables, bit-exact), decoded by the tensor-core engine with the
 launcher's balanced split, a random forced range length and no workspace, by
 the CUDA-core engine, and by the 16-bit twin (against the oracle's native
-attention); every (sequence, head) checked."""
+attention); every (sequence, head) checked.  Chunked prefill: random shapes
+and chunk lengths (empty, one query, the whole sequence, across CTA tiles),
+every query row checked."""
 import numpy as np
 import pytest
 import torch
@@ -73,4 +75,55 @@ def test_decode_random_shapes(seed):
             extra = 2.0 ** -9 * vmax
         assert_attention_close(ob[b], refs16[b], w.dtype, f"{what} 16-bit twin seq {b}",
                                atol_extra=extra)
+    assert kvq.kvq_get_error() == (0, 0)
+
+
+def _chunk(rng, L):
+    """A chunk length for a sequence of L tokens: empty, one query, the whole
+    sequence, or a random length around the 64-token tile and the CTA edges."""
+    pick = int(rng.integers(0, 5))
+    if pick == 0 or L == 0:
+        return 0 if pick == 0 else min(L, 1)
+    if pick == 1:
+        return 1
+    if pick == 2:
+        return L
+    return int(rng.integers(1, L + 1))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_prefill_random_shapes(seed):
+    """Chunked prefill on seeded random shapes: every query row of every
+    sequence against the oracle's causal attention over the dequantized
+    tokens ("fix(cuda/kv): correct Int8 KV per-token scale ..." (mlxcel
+    PR #717), "Server integration")."""
+    rng = np.random.default_rng(3000 + seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8]))
+    D = int(rng.choice([64, 128]))
+    dtype = str(rng.choice(["fp16", "bf16"]))
+    B = int(rng.integers(1, 5))
+    lens = [int(x) for x in rng.choice([1, 2, 15, 16, 17, 63, 64, 65, 130, 300, 700], B)]
+    chunks = [_chunk(rng, L) for L in lens]
+    w = W.custom(B, G * Hkv, Hkv, D, dtype, lens, seed=4000 + seed)
+    case = Case(w)
+    case.write_prefix()
+    x = rng.standard_normal((sum(chunks), w.num_q_heads, D)).astype(np.float32)
+    qb = (x.astype(np.float16).view(np.uint16) if dtype == "fp16" else
+          torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    qs = torch.tensor(np.concatenate([[0], np.cumsum(chunks)]), dtype=torch.int32, device="cuda")
+    q = torch.from_numpy(qb.view(np.int16)).to("cuda").view(
+        torch.float16 if dtype == "fp16" else torch.bfloat16)
+    out = kvq.kvq_paged_prefill(q, *case.int8, case.bt, case.cl, qs, w.max_context_len,
+                                max(max(chunks), 1), w.sm_scale)
+    ob = out_bits(out)
+    what = f"Hkv={Hkv} G={G} D={D} {dtype} lens={lens} chunks={chunks}"
+    start = 0
+    for b, n in enumerate(chunks):
+        if n:
+            k, v = w.seq_kv(b)
+            ref, _ = oracle.prefill_sequence(qb[start:start + n], k, v, dtype, w.sm_scale)
+            for i in range(n):
+                assert_attention_close(ob[start + i], ref[i], dtype, f"{what} seq {b} query {i}")
+        start += n
     assert kvq.kvq_get_error() == (0, 0)

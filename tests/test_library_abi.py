@@ -101,6 +101,10 @@ def test_append_host_validation(kw, status):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(mq=0), OK),                      # no queries
+    (dict(tq=0, q=None, out=None), OK),    # no query rows: q and out may be null
+    (dict(tq=0, q=None, qs=None), INVALID),
+    (dict(tq=-1), INVALID),
+    (dict(q=None), INVALID),               # rows without q
     (dict(mq=-1), INVALID),
     (dict(qs=None), INVALID),
     (dict(D=80), UNSUPPORTED),
