@@ -6,7 +6,8 @@ launcher's balanced split, a random forced range length and no workspace, by
 the CUDA-core engine, and by the 16-bit twin (against the oracle's native
 attention); every (sequence, head) checked.  Chunked prefill: random shapes
 and chunk lengths (empty, one query, the whole sequence, across CTA tiles),
-every query row checked."""
+every query row checked.  Static per-tensor scales: random shapes, codes
+bit-exact, decode within tolerance."""
 import numpy as np
 import pytest
 import torch
@@ -14,7 +15,7 @@ import torch
 import int8_quantized_paged_tokenwise_gb300 as kvq
 import oracle
 import workloads as W
-from _harness import Case, assert_attention_close, out_bits
+from _harness import Case, assert_attention_close, out_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -126,4 +127,60 @@ def test_prefill_random_shapes(seed):
             for i in range(n):
                 assert_attention_close(ob[start + i], ref[i], dtype, f"{what} seq {b} query {i}")
         start += n
+    assert kvq.kvq_get_error() == (0, 0)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_static_scale_random_shapes(seed):
+    """The static per-tensor-scale variant ("fix: #552 int8 kv cache
+    quantization cannot be enabled" (InfiniLM PR #553)) on seeded random
+    shapes: codes bit-exact against the oracle's static quantizer, the decode
+    (with and without a workspace) within tolerance of the oracle's attention
+    over scale * code."""
+    rng = np.random.default_rng(5000 + seed)
+    Hkv, G, D, dtype, lens = _shape(rng)
+    w = W.custom(len(lens), G * Hkv, Hkv, D, dtype, lens, seed=6000 + seed)
+    case = Case(w)
+    # calibrated scales (max |x| / 127 over the workload), or a shared or unit one
+    mk = mv = 0.0
+    for b in range(w.num_seqs):
+        k, v = w.seq_kv(b)
+        if len(k):
+            mk = max(mk, float(np.abs(oracle.bits_to_double(k, dtype)).max()))
+            mv = max(mv, float(np.abs(oracle.bits_to_double(v, dtype)).max()))
+    sk, sv = float(np.float32(max(mk, 1e-3) / 127)), float(np.float32(max(mv, 1e-3) / 127))
+    mode = int(rng.integers(0, 3))
+    if mode == 1:
+        sk = sv = max(sk, sv)
+    elif mode == 2:
+        sk = sv = 1.0
+    kc, vc = case.int8[0], case.int8[1]
+    for b in range(w.num_seqs):
+        k, v = w.seq_kv(b)
+        if len(k):
+            s = torch.from_numpy(w.slots(b, 0, len(k))).to("cuda")
+            kvq.kvq_quantize_append_static(to_dev(k, dtype), to_dev(v, dtype), s, kc, vc, sk, sv)
+    none = torch.empty(0, dtype=torch.uint8, device="cuda")
+    outs = {"balanced": kvq.kvq_paged_decode_static(case.q, kc, vc, sk, sv, case.bt, case.cl,
+                                                    w.max_context_len, w.sm_scale),
+            "no workspace": kvq.kvq_paged_decode_static(case.q, kc, vc, sk, sv, case.bt, case.cl,
+                                                        w.max_context_len, w.sm_scale,
+                                                        workspace=none)}
+    what = f"Hkv={Hkv} G={G} D={D} {dtype} lens={lens} scales=({sk}, {sv})"
+    for b in range(w.num_seqs):
+        k, v = w.seq_kv(b)
+        ck, cv, _, _ = case.gather_seq(b)
+        wk = oracle.quantize_rows_static(k, dtype, sk)
+        wv = oracle.quantize_rows_static(v, dtype, sv)
+        assert np.array_equal(ck, wk), f"{what} seq {b}: K codes"
+        assert np.array_equal(cv, wv), f"{what} seq {b}: V codes"
+        if len(k) == 0:
+            ref = np.zeros((w.num_q_heads, D))
+        else:
+            kh, vh = wk.astype(np.float64) * sk, wv.astype(np.float64) * sv
+            qf = oracle.bits_to_double(w.seq_q(b), dtype)
+            ref = np.stack([oracle.attend_one(qf[h], kh[:, h // G], vh[:, h // G], w.sm_scale)
+                            for h in range(w.num_q_heads)])
+        for name, out in outs.items():
+            assert_attention_close(out_bits(out)[b], ref, dtype, f"{what} {name} seq {b}")
     assert kvq.kvq_get_error() == (0, 0)
