@@ -9,12 +9,13 @@
 //
 // Exactness on the GPU.  a is found on the raw 16-bit magnitudes (integer max
 // of the sign-cleared patterns orders finite values by magnitude), then
-// decoded exactly to FP32.  a/127 is an IEEE FP32 division (__fdiv_rn): the
-// exact quotient of a 16-bit value by 127 is either an FP16 value or at least
-// 2^-17 (relative) away from every FP16 value, far above the 2^-24 FP32
-// rounding error, so __float2half_ru gives the exact upward rounding.
-// The code is the exact quotient x / s rounded half to even, found from an
-// approximate reciprocal and an exact FMA remainder (quant_code below).
+// decoded exactly to FP32.  a/127 rounded up to FP16 comes from one FP32
+// product and a check (row_scale_bits below).
+// The code is the exact quotient x / s rounded half to even: for an
+// unsaturated row straight from the correctly rounded reciprocal, with an
+// exact FMA remainder flagging the exact ties (quantize4_fast below), which
+// are recomputed, as are saturated rows, by the remainder-corrected
+// quant_code.
 // No fast-math and no flush-to-zero: bf16 subnormal rows must keep a > 0.
 #include "kvq_internal.h"
 #include "kvq_ptx.cuh"
@@ -33,14 +34,21 @@ __device__ __forceinline__ float bits_to_float(uint32_t b) {
   }
 }
 
-// FP16 bits of the row scale for magnitude pattern `amax_bits`.
+// FP16 bits of the row scale for magnitude pattern `amax_bits`: a/127
+// rounded up to FP16, without a division.  y = a * fl(1/127) is within
+// 2^-23 (relative) of a/127, and a/127 is either an FP16 value or at least
+// 2^-17 (relative) away from every FP16 value, so rounding y up gives the
+// scale unless a/127 is an FP16 value f and y landed above it; then the
+// FP16 value below the result still covers a (127 times it, exact in FP32:
+// 11 by 7 bits, is >= a) and is the scale.  The smallest result is 2^-24,
+// so a > 0 never gets a zero scale.
 template <bool BF16>
 __device__ __forceinline__ uint16_t row_scale_bits(uint32_t amax_bits) {
   if (amax_bits == 0u) return 0x3C00u;                   // all-zero token -> 1.0
   const float a = bits_to_float<BF16>(amax_bits);
-  unsigned short s = __half_as_ushort(__float2half_ru(__fdiv_rn(a, 127.0f)));
-  if (s >= 0x7C00u) s = 0x7BFFu;                         // saturate at 65504
-  if (s == 0u) s = 1u;                                   // a > 0 never gets a zero scale
+  unsigned short s = __half_as_ushort(__float2half_ru(__fmul_rn(a, 1.0f / 127.0f)));
+  if (s >= 0x7C00u) return 0x7BFFu;                      // saturate at 65504
+  if (__fmul_rn(127.0f, __half2float(__ushort_as_half((unsigned short)(s - 1u)))) >= a) --s;
   return s;
 }
 
@@ -81,15 +89,47 @@ __device__ __forceinline__ uint32_t quantize4_as(uint2 x, float s, float inv) {
   return __byte_perm(__byte_perm(c0, c1, 0x0040u), __byte_perm(c2, c3, 0x0040u), 0x5410u);
 }
 
-// Four 16-bit values -> four int8 codes packed little-endian (scale bits sb).
+// Four codes of an unsaturated row (|x / s| <= 127) from inv ~ 1/s (the
+// approximate reciprocal, within 2^-23 relative): k = rint(x * inv), both
+// steps rounded, is the round-half-even code of every quotient that is not
+// an exact tie.  The product is within 127 * 1.5 * 2^-23 < 2^-15 of x / s,
+// while a quotient of a 16-bit x by an FP16 s
+// that is not a tie lies at least 2^-14 from every half-integer (near one,
+// x / s >= 1/4, and with x = mx 2^e, s = ms 2^(e + d) its distance is a
+// nonzero multiple of 1 / (2 ms 2^d), where ms 2^d <= 4 mx <= 2^13).  On an
+// exact tie the product may land on either side, so the exact remainder
+// x - k s = +-s/2 flags it and `tie` asks for quant_code.  The codes are the low bytes of
+// the sums k + 1.5 * 2^23; the FP32 pairs go through the paired instructions.
 template <bool BF16>
-__device__ __forceinline__ uint32_t quantize4(uint2 x, uint16_t sb, float s, float inv) {
-  return sb == 0x7BFFu ? quantize4_as<BF16, true>(x, s, inv)
-                       : quantize4_as<BF16, false>(x, s, inv);
+__device__ __forceinline__ uint32_t quantize4_fast(uint2 x, float s, float inv, bool& tie) {
+  constexpr float kM = 12582912.0f;              // 1.5 * 2^23
+  const float2 xa = make_float2(bits_to_float<BF16>(x.x & 0xFFFFu), bits_to_float<BF16>(x.x >> 16));
+  const float2 xb = make_float2(bits_to_float<BF16>(x.y & 0xFFFFu), bits_to_float<BF16>(x.y >> 16));
+  const float2 i2 = make_float2(inv, inv), m2 = make_float2(kM, kM);
+  const float2 nm2 = make_float2(-kM, -kM), ns2 = make_float2(-s, -s);
+  const float2 ta = __fadd2_rn(__fmul2_rn(xa, i2), m2);
+  const float2 tb = __fadd2_rn(__fmul2_rn(xb, i2), m2);
+  const float2 ra = __ffma2_rn(__fadd2_rn(ta, nm2), ns2, xa);
+  const float2 rb = __ffma2_rn(__fadd2_rn(tb, nm2), ns2, xb);
+  const float h = 0.5f * s;
+  tie = fabsf(ra.x) == h || fabsf(ra.y) == h || fabsf(rb.x) == h || fabsf(rb.y) == h;
+  return __byte_perm(__byte_perm(__float_as_uint(ta.x), __float_as_uint(ta.y), 0x0040u),
+                     __byte_perm(__float_as_uint(tb.x), __float_as_uint(tb.y), 0x0040u),
+                     0x5410u);
 }
 
-// An approximate reciprocal is enough for quant_code: its error (a few ulp)
-// moves x * inv by far less than one for |x / s| <= 128.
+// Four 16-bit values -> four int8 codes packed little-endian (scale bits sb,
+// inv ~ 1/s).
+template <bool BF16>
+__device__ __forceinline__ uint32_t quantize4(uint2 x, uint16_t sb, float s, float inv) {
+  if (sb == 0x7BFFu) return quantize4_as<BF16, true>(x, s, inv);
+  bool tie;
+  const uint32_t c = quantize4_fast<BF16>(x, s, inv, tie);
+  return tie ? quantize4_as<BF16, false>(x, s, inv) : c;
+}
+
+// The approximate reciprocal (relative error within 2^-23) serves both
+// paths: quant_code tolerates a few ulp, quantize4_fast one and a half.
 __device__ __forceinline__ float approx_rcp(float s) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
@@ -180,10 +220,15 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Qu
   for (int i = 0; i < kRowPasses; ++i) {
     const bool act = rt.active(p, i);
     uint32_t km = mag_max4(kx[i]), vm = mag_max4(vx[i]);
+    if constexpr (LPR == 32) {                    // one row per warp: one reduction
+      km = __reduce_max_sync(0xFFFFFFFFu, km);
+      vm = __reduce_max_sync(0xFFFFFFFFu, vm);
+    } else {
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) {
-      km = max(km, __shfl_xor_sync(0xFFFFFFFFu, km, off));
-      vm = max(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, off));
+      for (int off = LPR / 2; off > 0; off >>= 1) {
+        km = max(km, __shfl_xor_sync(0xFFFFFFFFu, km, off));
+        vm = max(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, off));
+      }
     }
     if (!act) continue;
     const uint16_t ks = row_scale_bits<BF16>(km);

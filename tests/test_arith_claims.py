@@ -162,3 +162,86 @@ def test_quantizer_rounding_without_division_is_exact():
                 inside = np.abs(xs.astype(np.float64)) <= 127 * np.float64(s)
                 got = _quant_code_f32(xs[inside], s, inv, sat=False)
                 assert np.array_equal(got, want[inside]), (float(s), ulps, "unsaturated")
+
+
+def _quant_fast_f32(x, s, ulps=0):
+    """The quantizer's fast path for an unsaturated row, step by step in
+    float32: inv = 1/s off by `ulps` ulp, k = rint(x * inv) (the product
+    rounded, then the integer by adding 1.5 * 2^23), and the tie flag
+    |x - k s| == s/2 from the exact remainder."""
+    x = x.astype(np.float32)
+    s = np.float32(s)
+    inv = np.float32(1) / s
+    for _ in range(abs(ulps)):
+        inv = np.nextafter(inv, np.float32(np.inf if ulps > 0 else -np.inf), dtype=np.float32)
+    q = (x * inv).astype(np.float32)
+    big = np.float32(12582912.0)
+    t = (q + big).astype(np.float32)
+    k = (t - big).astype(np.float32)
+    ki = t.view(np.uint32).astype(np.int64) - 0x4B400000
+    r64 = x.astype(np.float64) - k.astype(np.float64) * np.float64(s)
+    assert np.all(r64.astype(np.float32).astype(np.float64) == r64)   # FMA exact
+    tie = np.abs(r64) == 0.5 * np.float64(s)
+    return ki, tie
+
+
+def _row_scale_f32(a):
+    """The row scale's FP16 bits, step by step in float32: y = a * fl(1/127),
+    rounded up to FP16, saturated at 65504, then one step down when 127 times
+    the FP16 value below still covers a."""
+    a = a.astype(np.float32)
+    y = (a * np.float32(1.0 / 127.0)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        rn = y.astype(np.float16)
+    bits = rn.view(np.uint16).astype(np.int64) + (rn.astype(np.float32) < y)
+    sat = bits >= 0x7C00
+    below = np.clip(bits - 1, 0, 0x7BFF).astype(np.uint16).view(np.float16).astype(np.float32)
+    down = (np.float32(127.0) * below).astype(np.float32) >= a
+    return np.where(sat, 0x7BFF, bits - (down & ~sat))
+
+
+def test_row_scale_without_division_is_exact():
+    # every positive finite fp16 and bf16 magnitude: the division-free scale
+    # equals a/127 rounded up to FP16 (saturated at 65504), decided in float64
+    bits = np.arange(1, 1 << 15, dtype=np.uint32)
+    f16 = bits.astype(np.uint16).view(np.float16).astype(np.float32)
+    b16 = (bits << 16).view(np.float32)
+    for a in (f16, b16):
+        a = a[np.isfinite(a)]
+        q = a.astype(np.float64) / 127.0
+        with np.errstate(over="ignore"):
+            rn = q.astype(np.float16)
+        want = rn.view(np.uint16).astype(np.int64) + (rn.astype(np.float64) < q)
+        want = np.where(want >= 0x7C00, 0x7BFF, want)
+        assert np.array_equal(_row_scale_f32(a), want)
+        assert np.all(want >= 1)
+
+
+def test_quantizer_fast_path_is_exact_off_ties():
+    # every finite fp16 and bf16 value of an unsaturated row (|x| <= 127 s)
+    # against 600 FP16 scales (subnormal to 65504, a seeded sample plus the
+    # edges), the reciprocal off by up to two ulp: the fast code equals the exact quotient's round-half-even code
+    # wherever the remainder does not flag a tie, and every flagged element is
+    # an exact tie (|x/s - k| = 1/2 exactly)
+    bits = np.arange(0, 1 << 16, dtype=np.uint32)
+    f16 = bits.astype(np.uint16).view(np.float16).astype(np.float32)
+    b16 = (bits << 16).view(np.float32)
+    rng = np.random.default_rng(7)
+    pats = np.concatenate([rng.integers(1, 0x7BFF, 580), [1, 2, 0x03FF, 0x0400, 0x3C00, 0x3C01,
+                                                          0x2008, 0x5BF0, 0x7800, 0x7BFE, 0x7BFF,
+                                                          0x0001, 0x1C00, 0x3555, 0x4B00,
+                                                          0x57F0, 0x6000, 0x6400, 0x7000, 0x77FF]])
+    ties = 0
+    for xs in (f16, b16):
+        xs = xs[np.isfinite(xs)]
+        for pat in pats:
+            s = np.float32(np.uint16(pat).view(np.float16))
+            sub = xs[np.abs(xs.astype(np.float64)) <= 127 * np.float64(s)]
+            want = np.rint(sub.astype(np.float64) / np.float64(s)).astype(np.int64)
+            for ulps in (-2, 0, 2):                  # the kernel's reciprocal is approximate
+                ki, tie = _quant_fast_f32(sub, s, ulps)
+                assert np.all(tie | (ki == want)), (float(s), ulps)
+                k64 = ki.astype(np.float64)
+                assert np.all(np.abs(sub[tie].astype(np.float64) / np.float64(s) - k64[tie]) == 0.5)
+                ties += int(tie.sum())
+    assert ties > 0                              # the tie branch is exercised
