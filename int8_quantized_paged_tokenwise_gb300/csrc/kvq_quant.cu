@@ -136,58 +136,77 @@ __device__ __forceinline__ float approx_rcp(float s) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t mag_max4(uint2 x) {
-  const uint32_t a = max(x.x & 0x7FFFu, (x.x >> 16) & 0x7FFFu);
-  const uint32_t b = max(x.y & 0x7FFFu, (x.y >> 16) & 0x7FFFu);
-  return max(a, b);
+// Largest magnitude pattern (sign cleared) among a lane's 16-bit values.
+template <int NW>
+__device__ __forceinline__ uint32_t mag_max(const uint32_t (&x)[NW]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) m = __vmaxu2(m, x[w] & 0x7FFF7FFFu);
+  return max(m & 0xFFFFu, m >> 16);
 }
 
-// One group of D/4 lanes per (token, KV head) row; each lane owns four
-// consecutive elements (one 8-byte load of K and of V, one 4-byte store of
-// codes each).  Rows of one warp are adjacent heads of a token, so the
-// 16-bit loads and the int8 stores of a warp are contiguous runs.  Each warp
-// takes kRowPasses such passes and issues every load of them (slots, K and V
-// rows) before it uses any, so that a warp keeps several rows' loads in
-// flight instead of waiting for one row's slot, then its values.
-constexpr int kRowPasses = 4;
-
-template <int D>
+// D / EPL lanes per (token, KV head) row; each lane owns EPL consecutive
+// elements (K and V each: one 8-byte load for EPL = 4, two 16-byte loads for
+// EPL = 16).  Rows of one warp are adjacent heads of a token, so the 16-bit
+// loads and the stores of a warp are contiguous runs.  Each warp takes kPasses
+// such passes and issues every load of them (slots, K and V rows) before it
+// uses any, so that a warp keeps several rows' loads in flight instead of
+// waiting for one row's slot, then its values.  The quantizer takes EPL = 16:
+// its per-row work (absmax, scales, addresses) is then shared by four rows
+// per warp instruction at D = 128.
+template <int D, int EPL>
 struct RowTask {
-  static constexpr int LPR = D / 4;               // lanes per row
+  static constexpr int LPR = D / EPL;             // lanes per row
   static constexpr int RPW = 32 / LPR;            // rows per warp pass
-  int64_t row[kRowPasses], t[kRowPasses], slot[kRowPasses];
-  int j[kRowPasses];
+  static constexpr int NW = EPL / 2;              // 32-bit words of K (or V) per lane
+  static constexpr int kPasses = EPL == 4 ? 4 : 2;
+  static_assert(EPL == 4 || EPL == 16, "8-byte or 32-byte lane slices");
+  int64_t row[kPasses], t[kPasses], slot[kPasses];
+  int j[kPasses];
   int sub;
   // this thread's rows and their slots, K and V words, all loads in flight
-  __device__ __forceinline__ void load(const QuantParams& p, uint2 (&kx)[kRowPasses],
-                                       uint2 (&vx)[kRowPasses]) {
+  __device__ __forceinline__ void load(const QuantParams& p, uint32_t (&kx)[kPasses][NW],
+                                       uint32_t (&vx)[kPasses][NW]) {
     const int lane = threadIdx.x & 31;
     sub = lane % LPR;
     const int64_t wg = ((int64_t)blockIdx.x * kQuantThreads + threadIdx.x) / 32;
-    const int64_t row0 = wg * (kRowPasses * RPW) + lane / LPR;
+    const int64_t row0 = wg * (kPasses * RPW) + lane / LPR;
     // (token, head) of the first row by one division, the next ones by steps
     int64_t tt = row0 / p.num_kv_heads;
     int jj = (int)(row0 - tt * p.num_kv_heads);
 #pragma unroll
-    for (int i = 0; i < kRowPasses; ++i) {
+    for (int i = 0; i < kPasses; ++i) {
       row[i] = row0 + i * RPW;
       slot[i] = -1;
       t[i] = tt;
       j[i] = jj;
-      kx[i] = vx[i] = make_uint2(0, 0);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) kx[i][w] = vx[i][w] = 0u;
       jj += RPW;
-      while (jj >= p.num_kv_heads) {              // RPW <= 2: at most two turns
+      while (jj >= p.num_kv_heads) {              // at most RPW <= 8 turns
         jj -= p.num_kv_heads;
         ++tt;
       }
       if (row[i] < p.num_rows) {
         slot[i] = p.slots[t[i]];
         const uint16_t* kr =
-            static_cast<const uint16_t*>(p.k) + t[i] * p.k_stride + (int64_t)j[i] * D;
+            static_cast<const uint16_t*>(p.k) + t[i] * p.k_stride + (int64_t)j[i] * D + sub * EPL;
         const uint16_t* vr =
-            static_cast<const uint16_t*>(p.v) + t[i] * p.v_stride + (int64_t)j[i] * D;
-        kx[i] = __ldg(reinterpret_cast<const uint2*>(kr) + sub);
-        vx[i] = __ldg(reinterpret_cast<const uint2*>(vr) + sub);
+            static_cast<const uint16_t*>(p.v) + t[i] * p.v_stride + (int64_t)j[i] * D + sub * EPL;
+        if constexpr (EPL == 4) {
+          const uint2 a = __ldg(reinterpret_cast<const uint2*>(kr));
+          const uint2 b = __ldg(reinterpret_cast<const uint2*>(vr));
+          kx[i][0] = a.x; kx[i][1] = a.y;
+          vx[i][0] = b.x; vx[i][1] = b.y;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(kr) + h);
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(vr) + h);
+            kx[i][4 * h] = a.x; kx[i][4 * h + 1] = a.y; kx[i][4 * h + 2] = a.z; kx[i][4 * h + 3] = a.w;
+            vx[i][4 * h] = b.x; vx[i][4 * h + 1] = b.y; vx[i][4 * h + 2] = b.z; vx[i][4 * h + 3] = b.w;
+          }
+        }
       }
     }
   }
@@ -207,19 +226,21 @@ struct RowTask {
   }
 };
 
-template <int D, bool BF16>
+// EPL = 16 when the K and V rows allow 16-byte loads, else 4.
+template <int D, bool BF16, int EPL>
 __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const QuantParams p) {
-  constexpr int LPR = D / 4;
+  using RT = RowTask<D, EPL>;
+  constexpr int NW = RT::NW, LPR = RT::LPR;
   // the next kernel in the stream (a decode launched with programmatic stream
   // serialization) may be scheduled now; it waits for this grid's completion
   griddep_launch_dependents();
-  RowTask<D> rt;
-  uint2 kx[kRowPasses], vx[kRowPasses];
+  RT rt;
+  uint32_t kx[RT::kPasses][NW], vx[RT::kPasses][NW];
   rt.load(p, kx, vx);
 #pragma unroll
-  for (int i = 0; i < kRowPasses; ++i) {
+  for (int i = 0; i < RT::kPasses; ++i) {
     const bool act = rt.active(p, i);
-    uint32_t km = mag_max4(kx[i]), vm = mag_max4(vx[i]);
+    uint32_t km = mag_max<NW>(kx[i]), vm = mag_max<NW>(vx[i]);
     if constexpr (LPR == 32) {                    // one row per warp: one reduction
       km = __reduce_max_sync(0xFFFFFFFFu, km);
       vm = __reduce_max_sync(0xFFFFFFFFu, vm);
@@ -235,11 +256,23 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Qu
     const uint16_t vs = row_scale_bits<BF16>(vm);
     const float ksf = __half2float(__ushort_as_half(ks));
     const float vsf = __half2float(__ushort_as_half(vs));
+    const float kinv = approx_rcp(ksf), vinv = approx_rcp(vsf);
+    uint32_t kc[NW / 2], vc[NW / 2];
+#pragma unroll
+    for (int g = 0; g < NW / 2; ++g) {
+      kc[g] = quantize4<BF16>(make_uint2(kx[i][2 * g], kx[i][2 * g + 1]), ks, ksf, kinv);
+      vc[g] = quantize4<BF16>(make_uint2(vx[i][2 * g], vx[i][2 * g + 1]), vs, vsf, vinv);
+    }
     const int64_t crow = rt.cache_row(p, i);
-    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.k_cache) + crow * D)[rt.sub] =
-        quantize4<BF16>(kx[i], ks, ksf, approx_rcp(ksf));
-    reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.v_cache) + crow * D)[rt.sub] =
-        quantize4<BF16>(vx[i], vs, vsf, approx_rcp(vsf));
+    int8_t* kd = static_cast<int8_t*>(p.k_cache) + crow * D + rt.sub * EPL;
+    int8_t* vd = static_cast<int8_t*>(p.v_cache) + crow * D + rt.sub * EPL;
+    if constexpr (EPL == 16) {
+      *reinterpret_cast<uint4*>(kd) = make_uint4(kc[0], kc[1], kc[2], kc[3]);
+      *reinterpret_cast<uint4*>(vd) = make_uint4(vc[0], vc[1], vc[2], vc[3]);
+    } else {
+      *reinterpret_cast<uint32_t*>(kd) = kc[0];
+      *reinterpret_cast<uint32_t*>(vd) = vc[0];
+    }
     if (rt.sub == 0) {
       p.k_scale[crow] = ks;
       p.v_scale[crow] = vs;
@@ -258,17 +291,18 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_static_kernel(const Qu
                                                                          float inv_k,
                                                                          float inv_v) {
   griddep_launch_dependents();
-  RowTask<D> rt;
-  uint2 kx[kRowPasses], vx[kRowPasses];
+  using RT = RowTask<D, 4>;
+  RT rt;
+  uint32_t kx[RT::kPasses][2], vx[RT::kPasses][2];
   rt.load(p, kx, vx);
 #pragma unroll
-  for (int i = 0; i < kRowPasses; ++i) {
+  for (int i = 0; i < RT::kPasses; ++i) {
     if (!rt.active(p, i)) continue;
     const int64_t crow = rt.cache_row(p, i);
     uint32_t kq = 0, vq = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t kw = (e < 2) ? kx[i].x : kx[i].y, vw = (e < 2) ? vx[i].x : vx[i].y;
+      const uint32_t kw = kx[i][e >> 1], vw = vx[i][e >> 1];
       const uint32_t kb = (e & 1) ? (kw >> 16) : (kw & 0xFFFFu);
       const uint32_t vb = (e & 1) ? (vw >> 16) : (vw & 0xFFFFu);
       const float kr8 =
@@ -285,36 +319,50 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_static_kernel(const Qu
 
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) append_kv16_kernel(const QuantParams p) {
-  RowTask<D> rt;
-  uint2 kx[kRowPasses], vx[kRowPasses];
+  using RT = RowTask<D, 4>;
+  RT rt;
+  uint32_t kx[RT::kPasses][2], vx[RT::kPasses][2];
   rt.load(p, kx, vx);
 #pragma unroll
-  for (int i = 0; i < kRowPasses; ++i) {
+  for (int i = 0; i < RT::kPasses; ++i) {
     if (!rt.active(p, i)) continue;
     const int64_t crow = rt.cache_row(p, i);
-    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.k_cache) + crow * D)[rt.sub] = kx[i];
-    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.v_cache) + crow * D)[rt.sub] = vx[i];
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.k_cache) + crow * D)[rt.sub] =
+        make_uint2(kx[i][0], kx[i][1]);
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.v_cache) + crow * D)[rt.sub] =
+        make_uint2(vx[i][0], vx[i][1]);
   }
 }
 
-// CTAs for `rows` rows: warps of kRowPasses passes of 32 / (D / 4) rows each.
-inline int grid_for(int64_t rows, int D) {
-  const int64_t per_warp = (int64_t)kRowPasses * (32 / (D / 4));
+// CTAs for `rows` rows: warps of RowTask<D, EPL>::kPasses passes of its
+// rows per pass.
+template <int D, int EPL>
+inline int grid_for(int64_t rows) {
+  using RT = RowTask<D, EPL>;
+  const int64_t per_warp = (int64_t)RT::kPasses * RT::RPW;
   const int64_t threads = (rows + per_warp - 1) / per_warp * 32;
   return (int)((threads + kQuantThreads - 1) / kQuantThreads);
 }
 
 }  // namespace
 
+template <int D, bool BF16, int EPL>
+void quantize_append_go(const QuantParams& p, cudaStream_t s) {
+  quantize_append_kernel<D, BF16, EPL><<<grid_for<D, EPL>(p.num_rows), kQuantThreads, 0, s>>>(p);
+}
+
 cudaError_t quantize_append_launch(int D, bool bf16, const QuantParams& p, cudaStream_t s) {
   if (p.num_rows == 0) return cudaSuccess;
-  const int grid = grid_for(p.num_rows, D);
+  // 32-byte lane slices need 16-byte aligned rows (pointers and token strides)
+  const bool wide = (reinterpret_cast<uintptr_t>(p.k) % 16 == 0) &&
+                    (reinterpret_cast<uintptr_t>(p.v) % 16 == 0) && p.k_stride % 8 == 0 &&
+                    p.v_stride % 8 == 0;
   if (D == 128) {
-    if (bf16) quantize_append_kernel<128, true><<<grid, kQuantThreads, 0, s>>>(p);
-    else quantize_append_kernel<128, false><<<grid, kQuantThreads, 0, s>>>(p);
+    if (wide) bf16 ? quantize_append_go<128, true, 16>(p, s) : quantize_append_go<128, false, 16>(p, s);
+    else bf16 ? quantize_append_go<128, true, 4>(p, s) : quantize_append_go<128, false, 4>(p, s);
   } else {
-    if (bf16) quantize_append_kernel<64, true><<<grid, kQuantThreads, 0, s>>>(p);
-    else quantize_append_kernel<64, false><<<grid, kQuantThreads, 0, s>>>(p);
+    if (wide) bf16 ? quantize_append_go<64, true, 16>(p, s) : quantize_append_go<64, false, 16>(p, s);
+    else bf16 ? quantize_append_go<64, true, 4>(p, s) : quantize_append_go<64, false, 4>(p, s);
   }
   return cudaGetLastError();
 }
@@ -322,7 +370,7 @@ cudaError_t quantize_append_launch(int D, bool bf16, const QuantParams& p, cudaS
 cudaError_t quantize_static_launch(int D, bool bf16, const QuantParams& p, float inv_k,
                                    float inv_v, cudaStream_t s) {
   if (p.num_rows == 0) return cudaSuccess;
-  const int grid = grid_for(p.num_rows, D);
+  const int grid = D == 128 ? grid_for<128, 4>(p.num_rows) : grid_for<64, 4>(p.num_rows);
   if (D == 128) {
     if (bf16) quantize_static_kernel<128, true><<<grid, kQuantThreads, 0, s>>>(p, inv_k, inv_v);
     else quantize_static_kernel<128, false><<<grid, kQuantThreads, 0, s>>>(p, inv_k, inv_v);
@@ -335,7 +383,7 @@ cudaError_t quantize_static_launch(int D, bool bf16, const QuantParams& p, float
 
 cudaError_t append_kv16_launch(int D, const QuantParams& p, cudaStream_t s) {
   if (p.num_rows == 0) return cudaSuccess;
-  const int grid = grid_for(p.num_rows, D);
+  const int grid = D == 128 ? grid_for<128, 4>(p.num_rows) : grid_for<64, 4>(p.num_rows);
   if (D == 128) append_kv16_kernel<128><<<grid, kQuantThreads, 0, s>>>(p);
   else append_kv16_kernel<64><<<grid, kQuantThreads, 0, s>>>(p);
   return cudaGetLastError();

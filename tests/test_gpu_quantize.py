@@ -169,3 +169,45 @@ def test_quantize_host_validation():
     assert st == 2                                                          # block_size 32
     with pytest.raises(ValueError):                                        # shape mismatch
         kvq.kvq_quantize_append(k, k, slots, kc[:, :, :, :32].contiguous(), vc, ks, vs)
+
+
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "fp16"), (128, "fp16"), (64, "bf16")])
+def test_quantize_row_layouts(D, dtype):
+    """The append reads 32-byte lane slices when the K and V rows are 16-byte
+    aligned (pointers and token strides) and 8-byte slices otherwise: a
+    contiguous batch, one with a token stride of Hkv*D + 4 elements and one
+    starting 8 bytes into its buffer all write the oracle's codes and scales."""
+    T, Hkv = 97, 3
+    rng = np.random.default_rng(D + len(dtype))
+    x = rng.standard_normal((2, T, Hkv, D)).astype(np.float32) * rng.choice([1e-3, 1, 50], (2, T, Hkv, 1))
+    x[:, 5] = 0.0                                  # an all-zero token
+    # a token of exact ties: absmax 63.5 gives scale 0.5, and (k + 1/2) * 0.5
+    # lies halfway between two codes
+    x[:, 7] = ((np.arange(D) % 100) - 50 + 0.5) * 0.5
+    x[:, 7, :, 0] = 63.5
+    bits = (x.astype(np.float16).view(np.uint16) if dtype == "fp16" else
+            torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    qk, sk = oracle.quantize_rows(bits[0], dtype)
+    qv, sv = oracle.quantize_rows(bits[1], dtype)
+    nb = (T + 15) // 16 + 2
+    slots = torch.from_numpy(rng.permutation(nb * 16)[:T].astype(np.int64)).cuda()
+    dev = [to_dev(bits[i], dtype) for i in range(2)]
+    tdt = dev[0].dtype
+    layouts = {"contiguous": dev}
+    for name, pad, off in (("token stride + 4", 4, 0), ("8-byte offset", 0, 4)):
+        views = []
+        for i in range(2):
+            buf = torch.zeros(off + T * (Hkv * D + pad), dtype=tdt, device="cuda")
+            view = buf[off:].view(T, Hkv * D + pad)[:, :Hkv * D].view(T, Hkv, D)
+            view.copy_(dev[i])
+            views.append(view)
+        layouts[name] = views
+    for name, (k, v) in layouts.items():
+        kc, vc, ks, vs = kvq.alloc_int8_cache(nb, Hkv, D, "cuda")
+        kvq.kvq_quantize_append(k, v, slots, kc, vc, ks, vs)
+        blk, o = slots // 16, slots % 16
+        assert np.array_equal(kc[blk, :, o].cpu().numpy(), qk), name
+        assert np.array_equal(vc[blk, :, o].cpu().numpy(), qv), name
+        assert np.array_equal(ks[blk, :, o].cpu().numpy().view(np.uint16), sk), name
+        assert np.array_equal(vs[blk, :, o].cpu().numpy().view(np.uint16), sv), name
+    assert kvq.kvq_get_error() == (0, 0)
