@@ -113,9 +113,10 @@ def parse_args():
     ap.add_argument("--no-g-sweep", action="store_true")
     ap.add_argument("--profile-seqs", type=int, default=0,
                     help="with --profile-arm: only the workload's first N sequences")
-    ap.add_argument("--profile-arm", choices=["int8", "kv16", "int8cc"], default=None,
+    ap.add_argument("--profile-arm", choices=["int8", "kv16", "int8cc", "append"], default=None,
                     help="profiling run: only this decode arm (one cache on the device), "
-                         "warm-up + steps with L2 flushes, a short timing line; no bench line")
+                         "or the step's INT8 quantize-append (append), warm-up + steps with "
+                         "L2 flushes, a short timing line; no bench line")
     return ap.parse_args()
 
 
@@ -799,10 +800,16 @@ def profile_arm(torch, w, dev, args):
     flush = make_flush(torch, dev)
     nop = lambda: None  # noqa: E731
     dec = {"int8": g.decode_int8, "kv16": g.decode_kv16,
-           "int8cc": g.decode_int8_cuda_cores}[args.profile_arm]
+           "int8cc": g.decode_int8_cuda_cores, "append": g.append_int8}[args.profile_arm]
     _, t = time_arm(torch, flush, nop, dec, args.steps, args.warmup)
-    nbytes = w.decode_bytes_kv16() if kv16 else w.decode_bytes_int8()
     ms = statistics.mean(t)
+    if args.profile_arm == "append":
+        nbytes = w.append_bytes_int8()
+        print(json.dumps({"profile_arm": "append", "workload": w.name,
+                          "append_tokens": w.append_tokens(), "append_us": round(1e3 * ms, 2),
+                          "append_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}))
+        return
+    nbytes = w.decode_bytes_kv16() if kv16 else w.decode_bytes_int8()
     print(json.dumps({"profile_arm": args.profile_arm, "workload": w.name,
                       "decode_us": round(1e3 * ms, 2),
                       "decode_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}))
