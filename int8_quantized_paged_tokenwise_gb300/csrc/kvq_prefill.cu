@@ -17,7 +17,7 @@
 //    bulk copies of its two 32-byte scale rows into a 3-stage ring;
 //  * warps 10-13, converters: INT8 codes to exact FP16 integers (byte
 //    permute under exponent 0x64, minus 1152), K and V both as [64 tokens][D]
-//    tiles, 128-byte swizzled, in 3 buffers: K is the K-major B operand of
+//    tiles, 128-byte swizzled, in 4 buffers: K is the K-major B operand of
 //    Q K^T, V the MN-major B operand of P V; the tile's K scales (times
 //    sm_scale log2 e) and V scales as FP32 columns;
 //  * warp 9, MMA issuer (one thread): per KV tile and half, P V of the
@@ -49,7 +49,7 @@ constexpr int kTcPages = kTcKv / kBlockSize;     // pages per KV tile
 #define KVQ_PF_RAW 3
 #endif
 #ifndef KVQ_PF_CONV
-#define KVQ_PF_CONV 3
+#define KVQ_PF_CONV 4
 #endif
 constexpr int kTcRaw = KVQ_PF_RAW;              // INT8 staging ring depth
 constexpr int kTcConv = KVQ_PF_CONV;            // converted (FP16) operand buffers
