@@ -7,7 +7,8 @@ the CUDA-core engine, and by the 16-bit twin (against the oracle's native
 attention); every (sequence, head) checked.  Chunked prefill: random shapes
 and chunk lengths (empty, one query, the whole sequence, across CTA tiles),
 every query row checked.  Static per-tensor scales: random shapes, codes
-bit-exact, decode within tolerance."""
+bit-exact, decode within tolerance.  The front trim and the dequantize-window
+baseline: random shapes, bit-exact against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -183,4 +184,70 @@ def test_static_scale_random_shapes(seed):
                             for h in range(w.num_q_heads)])
         for name, out in outs.items():
             assert_attention_close(out_bits(out)[b], ref, dtype, f"{what} {name} seq {b}")
+    assert kvq.kvq_get_error() == (0, 0)
+
+
+def _cache_rows(case, b, L):
+    """(K codes, V codes, K scale bits, V scale bits) of sequence b's first L
+    tokens read back through its block table."""
+    t = torch.arange(L, device="cuda")
+    blk = case.bt[b, t // 16].long()
+    off = t % 16
+    kc, vc, ks, vs = case.int8
+    return [kc[blk, :, off].cpu().numpy(), vc[blk, :, off].cpu().numpy(),
+            ks[blk, :, off].cpu().numpy(), vs[blk, :, off].cpu().numpy()]
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_trim_random_shapes(seed):
+    """Front trim keeping the sink ("fix(cuda/kv): correct Int8 KV per-token
+    scale ..." (mlxcel PR #717), follow-up commit) on seeded random shapes,
+    sink lengths and trims (zero, within, past the length): the rows and
+    scales left equal the oracle's trim bit for bit, context_lens follows."""
+    rng = np.random.default_rng(7000 + seed)
+    Hkv, G, D, dtype, lens = _shape(rng)
+    keep = int(rng.choice([0, 1, 4, 16, 33]))
+    trims = [int(rng.choice([0, 1, 15, 16, 17, max(L - keep, 0), L + 5]))
+             if rng.random() < 0.5 else int(rng.integers(0, L + 2)) for L in lens]
+    w = W.custom(len(lens), G * Hkv, Hkv, D, dtype, lens, seed=8000 + seed)
+    case = Case(w)
+    case.write_prefix()
+    before = [_cache_rows(case, b, L) for b, L in enumerate(lens)]
+    tr = torch.tensor(trims, dtype=torch.int32, device="cuda")
+    kvq.kvq_trim_front_keep_sink(*case.int8, case.bt, case.cl, tr, keep)
+    new_lens = case.cl.cpu().numpy()
+    what = f"Hkv={Hkv} D={D} lens={lens} keep={keep} trims={trims}"
+    for b, L in enumerate(lens):
+        n = max(0, min(trims[b], L - min(keep, L)))
+        assert new_lens[b] == L - n, f"{what} seq {b}: length"
+        after = _cache_rows(case, b, L - n)
+        for x, y in zip(before[b], after):
+            assert np.array_equal(oracle.trim_keep_sink(x, keep, trims[b]), y), f"{what} seq {b}"
+    assert kvq.kvq_get_error() == (0, 0)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_dequantize_window_random_shapes(seed):
+    """The dequantize-window baseline ("fix(cuda/kv): correct Int8 KV per-token
+    scale ..." (mlxcel PR #717), "The Int8 bug and fix") on seeded random
+    shapes: every valid token's 16-bit value equals the oracle's code * scale
+    rounded once to the dtype."""
+    rng = np.random.default_rng(9000 + seed)
+    Hkv, G, D, dtype, lens = _shape(rng)
+    w = W.custom(len(lens), G * Hkv, Hkv, D, dtype, lens, seed=9500 + seed)
+    case = Case(w)
+    case.write_prefix()
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    kw, vw = kvq.kvq_dequantize_window(*case.int8, case.bt, case.cl, w.max_context_len, tdt)
+    torch.cuda.synchronize()
+    for b, L in enumerate(lens):
+        t = torch.arange(L, device="cuda")
+        blk = case.bt[b, t // 16].long()
+        off = t % 16
+        got = [x[blk, :, off].cpu().view(torch.int16).numpy().view(np.uint16) for x in (kw, vw)]
+        k, v = w.seq_kv(b)
+        for x, g, nm in ((k, got[0], "K"), (v, got[1], "V")):
+            q, s = oracle.quantize_rows(x, dtype)
+            assert np.array_equal(g, oracle.dequantize_rows(q, s, dtype)), (
+                f"Hkv={Hkv} D={D} {dtype} lens={lens} seq {b} {nm}")
     assert kvq.kvq_get_error() == (0, 0)
